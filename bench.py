@@ -1,0 +1,437 @@
+"""Benchmark of libtopk's ragged per-row top-K on one (or N) GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workloads a,b]
+
+A step is one topk_ragged call over one batch of the workload (all of the
+hot path: load + key + filter + radix select + gather in one kernel launch).
+The headline workload is the decode batch: 64 rows, lengths uniform in
+[8192, 32768], row stride 32768, TopK 2048, N(0,1) logits rounded to the bf16
+grid. Inputs are resident in HBM before timing starts; an L2 flush (a 256 MiB
+write) runs between timed steps, outside the timed events. Per-step device time
+comes from CUDA events on the launching stream.
+
+Prints ONE JSON line on rank 0. Extra keys: ``workloads`` (the five workloads,
+each with rows/s, us per call, effective GB/s and fraction of HBM peak, plus
+the oracle's rows/s on the host cores), ``e2e`` (host buffers, copies inside
+the timed region), ``roofline``, ``cpu_baseline`` and ``clocks``.
+
+``--impl reference`` times the CPU oracle (the plain sort-based definition) on
+the host cores, on the same workload and metric; it is the slow yardstick, not
+a competing GPU implementation.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "rows/s and effective HBM GB/s (fraction of GB300 roofline); µs per decode call"
+HEADLINE = "decode_batch"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+DESCR = {
+    "decode_small": "8 rows, lengths U[1,4096], row stride 4096, TopK 512, N(0,1)",
+    "decode_batch": "64 rows, lengths U[8192,32768], row stride 32768, TopK 2048, N(0,1) on the bf16 grid",
+    "long_coop": "16 rows, lengths U[65536,131072], row stride 131072, TopK 2048, 90% N(0,1) + 10% N(4,0.5)",
+    "mtp": "32 requests x next_n 2, lengths L+j with L~U[100000,160000], row stride 163840, TopK 1024, N(0,1), -inf padding",
+    "prefill": "4096 rows, length 61440+i, row stride 65536, TopK 2048, 30% zeros / 5% Cauchy / 65% N(0,1), one all-equal row",
+}
+
+
+# --------------------------------------------------------------------- helpers
+
+def dist_env() -> tuple[int, int, int]:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (a plain all-reduce of one scalar, no data path)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def read_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (copy, MEASURED_PEAKS.json)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
+
+
+def read_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src_hash = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[2] == src_hash:
+            return float(parts[1])
+    return None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_row_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cpp", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self) -> dict | None:
+        rows = []
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                rows.append((float(p[1]), float(p[2]), p[5], p[6], p[7], p[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for _, _, hw, hwt, swt, swp in rows:
+            for name, v in (("hw_slowdown", hw), ("hw_thermal_slowdown", hwt),
+                            ("sw_thermal_slowdown", swt), ("sw_power_cap", swp)):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- GPU timing
+
+class GpuBench:
+    def __init__(self, device_index: int):
+        import torch
+
+        import sparse_attention_row_gb300 as sar
+        from sparse_attention_row_gb300 import build as b
+
+        b.build_library()
+        self.torch = torch
+        self.sar = sar
+        self.dev = torch.device("cuda", device_index)
+        torch.cuda.set_device(self.dev)
+        self.sel = sar.Selector(device_index)
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=self.dev)
+
+    def upload(self, w: workloads.Workload):
+        t = self.torch
+        x = t.from_numpy(w.logits).to(self.dev)
+        ln = t.from_numpy(w.lengths).to(self.dev)
+        out = t.empty((w.num_rows, w.topk), dtype=t.int32, device=self.dev)
+        return x, ln, out
+
+    def call(self, w, x, ln, out):
+        rc = self.sar.topk_ragged(x, w.row_stride, ln, w.num_rows, w.next_n, w.topk, out,
+                                  self.sel.workspace, None)
+        if rc != 0:
+            raise RuntimeError(f"topk_ragged: {self.sar.topk_status_string(rc)}")
+
+    def time_kernel(self, w, steps: int, warmup: int, world: int = 1) -> dict:
+        """Per-step device time of the single launch, L2 flushed before each step."""
+        t = self.torch
+        x, ln, out = self.upload(w)
+        stream = t.cuda.current_stream()
+        for _ in range(warmup):
+            self.flush.zero_()
+            self.call(w, x, ln, out)
+        starts = [t.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [t.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier(world)
+        t.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(steps):
+            self.flush.zero_()
+            starts[i].record(stream)
+            self.call(w, x, ln, out)
+            ends[i].record(stream)
+        t.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - wall0
+        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        rc, st = self.sar.topk_get_status(self.sel.workspace)
+        if rc != 0 or st & ~self.sar.TOPK_DEV_LENGTH_CLAMPED:
+            raise RuntimeError(f"device status {st:#x}")
+        return {"ms_mean": float(np.mean(ms)), "ms_median": float(np.median(ms)),
+                "ms_min": float(np.min(ms)), "wall_s": wall, "launches": steps, "out": out}
+
+    def time_e2e(self, w, steps: int, warmup: int) -> dict:
+        """Host buffers: pinned H2D of the batch, the call, D2H of the indices, every step."""
+        t = self.torch
+        hx = t.from_numpy(w.logits).pin_memory()
+        hl = t.from_numpy(w.lengths).pin_memory()
+        ho = t.empty((w.num_rows, w.topk), dtype=t.int32).pin_memory()
+        x = t.empty_like(hx, device=self.dev)
+        ln = t.empty_like(hl, device=self.dev)
+        out = t.empty((w.num_rows, w.topk), dtype=t.int32, device=self.dev)
+        stream = t.cuda.current_stream()
+
+        def step():
+            x.copy_(hx, non_blocking=True)
+            ln.copy_(hl, non_blocking=True)
+            self.call(w, x, ln, out)
+            ho.copy_(out, non_blocking=True)
+
+        for _ in range(warmup):
+            step()
+        t.cuda.synchronize()
+        ev0 = t.cuda.Event(enable_timing=True)
+        ev1 = t.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        t.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        ms = ev0.elapsed_time(ev1) / steps
+        return {"ms_per_step": ms, "wall_ms_per_step": 1e3 * wall / steps,
+                "h2d": hx.numel() * 4 + hl.numel() * 4, "d2h": ho.numel() * 4, "launches": steps}
+
+
+# ------------------------------------------------------------- CPU baseline
+
+def time_oracle(w: workloads.Workload, budget_s: float, max_rows: int | None = None) -> dict:
+    import oracle
+
+    cores = os.cpu_count() or 1
+    rows = w.num_rows if max_rows is None else min(max_rows, w.num_rows)
+    x, ln = w.logits[:rows], w.lengths[:rows]
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.topk_ragged(x, ln, w.topk, next_n=w.next_n if rows % w.next_n == 0 else 1, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    rps = reps * rows / el
+    vb = 4 * np.clip(ln.astype(np.int64), 0, w.row_stride).sum()
+    return {"rows_per_s": rps, "gbs": reps * vb / el / 1e9, "cores": cores,
+            "sample": f"{rows} of {w.num_rows} rows x {reps} repetitions ({el:.1f} s wall)"}
+
+
+# ------------------------------------------------------------------- arms
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.make(HEADLINE)
+    cores = os.cpu_count() or 1
+    import oracle
+
+    for _ in range(args.warmup):
+        oracle.topk_ragged(w.logits, w.lengths, w.topk, next_n=w.next_n, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.topk_ragged(w.logits, w.lengths, w.topk, next_n=w.next_n, nthreads=cores)
+    el = time.perf_counter() - t0
+    value = args.steps * w.num_rows / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{HEADLINE}: {DESCR[HEADLINE]}", "num_rows": w.num_rows,
+                   "row_stride": w.row_stride, "topk": w.topk, "next_n": w.next_n},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"the full {HEADLINE} batch ({w.num_rows} rows) per step"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args) -> None:
+    rank, world, local = dist_env()
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    gb = GpuBench(local)
+    peak, peak_src = read_peaks()
+
+    names = [HEADLINE] + [n for n in (args.workloads.split(",") if args.workloads else workloads.NAMES)
+                          if n != HEADLINE and n]
+    table = {}
+    head = None
+    for name in names:
+        w = workloads.make(name)
+        steps = args.steps if name == HEADLINE else max(3, min(args.steps, args.other_steps))
+        if name == HEADLINE:
+            with ClockSampler(local) as clk:
+                r = gb.time_kernel(w, steps, args.warmup, world)
+            clocks = clk.summary()
+        else:
+            r = gb.time_kernel(w, steps, args.warmup, 1)
+        ms = max_over_ranks(r["ms_mean"], world, gb.dev)
+        vbytes = w.valid_bytes()
+        gbs = vbytes / (ms * 1e-3) / 1e9
+        entry = {"rows_per_s": world * w.num_rows / (ms * 1e-3), "us_per_call": ms * 1e3,
+                 "us_per_call_median": r["ms_median"] * 1e3, "effective_gbs": gbs,
+                 "frac_of_hbm_peak": gbs / peak, "frac_of_8tbs_spec": gbs / 8000.0,
+                 "valid_bytes": vbytes, "steps": steps}
+        if rank == 0 and not args.no_cpu:
+            budget = args.cpu_budget if name == HEADLINE else args.cpu_budget / 2
+            cap_rows = None if name != "prefill" else 256
+            cb = time_oracle(w, budget, cap_rows)
+            entry["oracle_rows_per_s"] = cb["rows_per_s"]
+            entry["oracle_cores"] = cb["cores"]
+            if name == HEADLINE:
+                head_cpu = cb
+        table[name] = entry
+        if name == HEADLINE:
+            head = (w, r, ms, gbs, vbytes, clocks)
+        del r
+        torch.cuda.empty_cache()
+
+    w, r, ms, gbs, vbytes, clocks = head
+    e2e = gb.time_e2e(w, max(10, args.steps // 10), args.warmup)
+    e2e_ms = max_over_ranks(e2e["ms_per_step"], world, gb.dev)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC,
+        "value": world * w.num_rows / (ms * 1e-3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{HEADLINE}: {DESCR[HEADLINE]}", "num_rows": w.num_rows,
+                   "row_stride": w.row_stride, "topk": w.topk, "next_n": w.next_n,
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "parallelism": f"replica per GPU x{world}"},
+        "us_per_call": ms * 1e3,
+        "effective_gbs": gbs,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": read_traffic(HEADLINE), "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": vbytes},
+        "cpu_baseline": None if args.no_cpu else {
+            "value": head_cpu["rows_per_s"], "unit": "rows/s", "cores": head_cpu["cores"], "kind": "oracle",
+            "sample": head_cpu["sample"]},
+        "e2e": {"value": world * w.num_rows / (e2e_ms * 1e-3), "unit": "rows/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": e2e_ms},
+        "gpu_launches": r["launches"],
+        "clocks": clocks,
+        "workloads": table,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workloads", default="", help="comma list; default all five")
+    ap.add_argument("--other-steps", type=int, default=300, help="timed steps for the non-headline workloads")
+    ap.add_argument("--cpu-budget", type=float, default=3.0, help="seconds of oracle wall time")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timings")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

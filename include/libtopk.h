@@ -1,0 +1,182 @@
+/*
+ * libtopk: ragged per-row top-K over fp32 logits on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the token selection of long-context sparse attention
+ * (vLLM PR #54110 page, "Feature and motivation": the persistent_topk kernel
+ * serves DSA models in long-context inference). Every row r of a logits matrix
+ * has its own valid length len_r. For every row, the library returns the
+ * indices of its topk largest values among x[r, 0:len_r]. The per-row lengths
+ * and the TopK template (512 / 1024 / 2048) follow the persistent_topk launcher
+ * excerpt on the vLLM PR #41189 page ("Implementation breakdown"). MTP layouts,
+ * where a request contributes next_n adjacent rows, each with its own length,
+ * follow the vLLM PR #54110 page ("Implementation breakdown" item 2: next_n is
+ * the second dimension of a 2-D lengths tensor).
+ *
+ * Selection rule (the pages leave it open; this library fixes it):
+ *   - larger value first; on equal values, the smaller index first;
+ *   - values compare exactly as IEEE floats: -0.0 equals +0.0, subnormals are
+ *     not flushed, +inf and -inf are ordinary values;
+ *   - NaN inside a valid prefix is outside the contract (result unspecified);
+ *   - a row with len_r < topk returns its len_r indices, then -1 padding;
+ *   - the order of the indices inside an output row is unspecified (the
+ *     result is a set; sort it by (value desc, index asc) if order matters).
+ *
+ * Conventions for every entry point:
+ *   - pointers named logits, lengths, out_idx and workspace are DEVICE
+ *     pointers owned by the caller; the library allocates and frees nothing;
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream); all device work is enqueued on it, nothing synchronises it
+ *     except topk_get_status;
+ *   - errors found on the host are returned synchronously as a topk_status
+ *     code and nothing is enqueued; no C++ exception crosses this boundary;
+ *   - conditions found on the device (a clamped length, a timed-out wait) set
+ *     sticky bits in the workspace status word, read with topk_get_status.
+ */
+#ifndef LIBTOPK_H_
+#define LIBTOPK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+  TOPK_OK = 0,
+  TOPK_ERR_INVALID_ARG = 1,         /* null pointer, negative size, next_n not dividing num_rows ... */
+  TOPK_ERR_UNSUPPORTED_TOPK = 2,    /* topk not in {512, 1024, 2048} */
+  TOPK_ERR_MISALIGNED = 3,          /* logits/lengths/out_idx not 4-byte, workspace not 16-byte aligned */
+  TOPK_ERR_WORKSPACE_TOO_SMALL = 4, /* topk_options.workspace_bytes below topk_workspace_size */
+  TOPK_ERR_CUDA = 5,                /* a CUDA runtime call failed (launch, query, copy) */
+  TOPK_ERR_BARRIER_TIMEOUT = 6,     /* reported by topk_get_status: a wait on the device gave up */
+  TOPK_ERR_LENGTH_CLAMPED = 7,      /* reported by topk_get_status: some length was outside [0, row_stride] */
+  TOPK_ERR_PLAN = 8                 /* no launch configuration fits the device (e.g. kernel not resident) */
+} topk_status;
+
+/* Sticky bits of the device status word (first 4 bytes of the workspace). */
+#define TOPK_DEV_LENGTH_CLAMPED 0x1u  /* a length < 0 was read as 0, or > row_stride as row_stride */
+#define TOPK_DEV_BARRIER_TIMEOUT 0x2u /* a CTA of a row group waited longer than the barrier limit */
+#define TOPK_DEV_STAGE_TIMEOUT 0x4u   /* a staging copy did not land within the limit */
+
+/* Tuning and test knobs for topk_ragged_ex. Zero-initialise, then set fields. */
+typedef struct {
+  /* 0 = planner decides; 1 = one CTA per row; 2..16 = that many CTAs split each row. */
+  int force_ctas_per_group;
+  /* 0 = default; rows whose row_stride exceeds this may be split across CTAs. */
+  int64_t long_row_threshold;
+  /* 0 = default (1 s); limit of every device-side wait, in microseconds. */
+  uint32_t barrier_timeout_us;
+  /* Test only. 1 = CTA 1 of row group 0 leaves before its first group barrier,
+   * so the other CTAs' waits run out and set TOPK_DEV_BARRIER_TIMEOUT. The
+   * workspace must then be re-initialised with topk_workspace_init. */
+  int inject_skip_arrival;
+  /* 0 = unchecked; otherwise the workspace's size, checked against topk_workspace_size. */
+  size_t workspace_bytes;
+  /* 0 = every SM; otherwise at most this many co-resident CTAs are planned. */
+  int max_ctas;
+} topk_options;
+
+/* Properties of a device as the planner sees them. */
+typedef struct {
+  int num_sms;        /* streaming multiprocessors */
+  int max_smem_optin; /* opt-in shared memory per block, bytes */
+  int smem_per_cta;   /* dynamic shared memory the kernel needs, bytes */
+  int ctas_per_sm;    /* resident CTAs per SM for the exact kernel instance (occupancy) */
+} topk_device_props;
+
+/* A launch configuration. */
+typedef struct {
+  int ctas_per_group; /* G: CTAs that split one row (1 = a CTA owns whole rows) */
+  int num_groups;     /* row groups; group g handles rows g, g + num_groups, ... */
+  int grid;           /* CTAs launched = num_groups * ctas_per_group */
+  int threads;        /* threads per CTA */
+  int smem_bytes;     /* dynamic shared memory per CTA */
+  int cooperative;    /* 1 when the CTAs of a group wait on one another */
+} topk_plan;
+
+/*
+ * Workspace bytes needed on `device` (the other arguments are accepted for
+ * forward compatibility; the size depends only on the device). The workspace
+ * holds the device status word and, per row group, the histograms, counters
+ * and barrier words that CTAs splitting one row exchange (the role of the
+ * RadixRowState workspace on the vLLM PR #41444 page, "Executive summary").
+ * Returns 0 if the device cannot be queried.
+ */
+size_t topk_workspace_size(int device, int64_t num_rows, int64_t row_stride, int next_n, int topk);
+
+/*
+ * Zeroes a workspace once, after allocation (stream-ordered memset). After that
+ * no per-call clearing is needed: every successful topk_ragged leaves the
+ * workspace zeroed again, apart from the sticky status word, which this call
+ * also clears (the per-call memset it replaces is the one the vLLM PR #41748
+ * page, "Motivation", removes for a 3-5 us saving per decode step).
+ * After a TOPK_DEV_BARRIER_TIMEOUT the workspace must be re-initialised.
+ */
+int topk_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/*
+ * Ragged per-row top-K.
+ *   logits     fp32 [num_rows, row_stride], row-major, 4-byte aligned; row r
+ *              starts at logits + r * row_stride. Only x[r, 0:len_r] is used
+ *              (at most 12 bytes of a row's padding may be read, never used).
+ *   row_stride elements between row starts, >= 1; also the upper bound of
+ *              every length (it plays the role of max_seq_len).
+ *   lengths    int32 [num_rows] (or [num_rows / next_n, next_n] flattened):
+ *              valid length of each row; values outside [0, row_stride] are
+ *              clamped and flagged with TOPK_DEV_LENGTH_CLAMPED.
+ *   num_rows   rows; 0 is a no-op.
+ *   next_n     rows per request (MTP); must divide num_rows.
+ *   topk       512, 1024 or 2048.
+ *   out_idx    int32 [num_rows, topk], written in full.
+ *   workspace  at least topk_workspace_size bytes, 16-byte aligned, zeroed once
+ *              by topk_workspace_init. Calls that may run concurrently on the
+ *              GPU must not share a workspace.
+ *   stream     cudaStream_t.
+ * One kernel launch per call; no allocation, memset or host synchronisation, so
+ * the call can be captured in a CUDA graph. The first call on a device queries
+ * and caches its properties; make it before any stream capture.
+ */
+int topk_ragged(const float* logits, int64_t row_stride, const int32_t* lengths,
+                int64_t num_rows, int next_n, int topk, int32_t* out_idx,
+                void* workspace, void* stream);
+
+/* topk_ragged with options (NULL options = topk_ragged). */
+int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths,
+                   int64_t num_rows, int next_n, int topk, int32_t* out_idx,
+                   void* workspace, void* stream, const topk_options* options);
+
+/*
+ * Synchronises `stream` and copies the workspace's sticky status word
+ * (TOPK_DEV_* bits) to *device_status. For tests and debugging, not for the
+ * hot path. Returns TOPK_OK, or TOPK_ERR_CUDA if the copy failed.
+ */
+int topk_get_status(const void* workspace, void* stream, uint32_t* device_status);
+
+/* Static description of a topk_status code (never NULL). */
+const char* topk_status_string(int code);
+
+/*
+ * Fills *props for `device`: SM count, opt-in shared memory per block, the
+ * kernel's shared memory and its occupancy (queried for the exact kernel, as
+ * the vLLM PR #41189 page's "Implementation breakdown" item 1 requires).
+ */
+int topk_query_device(int device, topk_device_props* props);
+
+/*
+ * The host planner, a pure function of its arguments (no CUDA call), so it can
+ * be checked against made-up devices. It sizes the grid from the occupancy in
+ * *props and never plans more co-resident CTAs than num_sms * ctas_per_sm when
+ * CTAs of a group wait on one another; the deadlock of an oversized
+ * cooperative grid (vLLM PR #41189 page, "Feature and motivation": TopK=1024
+ * with MTP=1) cannot be planned. options may be NULL.
+ */
+int topk_make_plan(const topk_device_props* props, int64_t num_rows, int64_t row_stride,
+                   int next_n, int topk, const topk_options* options, topk_plan* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBTOPK_H_ */

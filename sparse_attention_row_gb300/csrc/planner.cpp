@@ -1,0 +1,78 @@
+// Host planner: picks the launch shape from the device's measured occupancy.
+//
+// The persistent_topk launcher on the vLLM PR #41189 page ("Implementation
+// breakdown") derives the number of row groups from num_sms x occupancy and
+// must stay below it whenever CTAs wait on one another; an oversized
+// cooperative grid deadlocks (same page, "Feature and motivation": TopK=1024,
+// MTP=1). Here the plan is a pure function of the device properties, so the
+// bound can be checked on made-up devices, and the launch that waits across
+// CTAs is a cooperative launch, which the driver refuses rather than hangs if
+// the grid cannot be resident.
+//
+// Shape rules:
+//   - one CTA owns whole rows (G = 1) unless the rows are long (row_stride
+//     above the long-row threshold) and too few to fill the GPU; then G CTAs
+//     split each row, G = min(16, capacity / num_rows, row_stride / 8192);
+//   - G = 1 launches min(num_rows, capacity) persistent CTAs, no waiting;
+//   - G > 1 launches num_groups = min(capacity / G, num_rows, num_sms) groups,
+//     so grid = num_groups * G <= num_sms * ctas_per_sm always.
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/libtopk.h"
+#include "topk_internal.h"
+
+namespace {
+
+bool topk_supported(int topk) { return topk == 512 || topk == 1024 || topk == 2048; }
+
+}  // namespace
+
+extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, int64_t row_stride,
+                              int next_n, int topk, const topk_options* options, topk_plan* plan) {
+  if (props == nullptr || plan == nullptr) return TOPK_ERR_INVALID_ARG;
+  if (num_rows < 0 || row_stride < 1 || next_n < 1 || (num_rows % next_n) != 0)
+    return TOPK_ERR_INVALID_ARG;
+  if (!topk_supported(topk)) return TOPK_ERR_UNSUPPORTED_TOPK;
+  *plan = topk_plan{};
+  plan->threads = ltk::kThreads;
+  plan->smem_bytes = props->smem_per_cta;
+  if (props->num_sms < 1 || props->ctas_per_sm < 1 || props->smem_per_cta > props->max_smem_optin)
+    return TOPK_ERR_PLAN;
+  int64_t cap = static_cast<int64_t>(props->num_sms) * props->ctas_per_sm;
+  if (options != nullptr && options->max_ctas > 0) cap = std::min<int64_t>(cap, options->max_ctas);
+  const int64_t threshold = (options != nullptr && options->long_row_threshold > 0)
+                                ? options->long_row_threshold
+                                : ltk::kDefaultLongRowThreshold;
+  int64_t G = 1;
+  if (options != nullptr && options->force_ctas_per_group != 0) {
+    G = options->force_ctas_per_group;
+    if (G < 1 || G > ltk::kMaxGroup) return TOPK_ERR_INVALID_ARG;
+  } else if (num_rows > 0 && row_stride > threshold && num_rows < cap) {
+    G = cap / num_rows;
+    G = std::min<int64_t>(G, ltk::kMaxGroup);
+    G = std::min<int64_t>(G, std::max<int64_t>(1, row_stride / ltk::kMinSpan));
+    if (G < 2) G = 1;
+  }
+  plan->ctas_per_group = static_cast<int>(G);
+  if (num_rows == 0) {
+    plan->num_groups = 0;
+    plan->grid = 0;
+    plan->cooperative = G > 1;
+    return TOPK_OK;
+  }
+  int64_t groups;
+  if (G == 1) {
+    groups = std::min<int64_t>(num_rows, cap);
+    plan->cooperative = 0;
+  } else {
+    groups = std::min<int64_t>(cap / G, num_rows);
+    groups = std::min<int64_t>(groups, props->num_sms);  // workspace holds num_sms groups
+    if (groups < 1) return TOPK_ERR_PLAN;
+    plan->cooperative = 1;
+  }
+  plan->num_groups = static_cast<int>(groups);
+  plan->grid = static_cast<int>(groups * G);
+  return TOPK_OK;
+}

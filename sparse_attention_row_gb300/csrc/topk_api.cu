@@ -1,0 +1,208 @@
+// C ABI of libtopk: argument checks, per-device property cache, planning and
+// the single launch per call. Every entry point returns a topk_status code and
+// never throws.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "../../include/libtopk.h"
+#include "topk_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceEntry {
+  bool ready = false;
+  topk_device_props props{};
+};
+
+std::mutex g_mu;
+DeviceEntry g_dev[kMaxDevices];
+
+// Environment overrides, read once.
+struct EnvKnobs {
+  int64_t long_row_threshold = 0;
+  int force_ctas_per_group = 0;
+  uint32_t timeout_us = 0;
+};
+
+EnvKnobs read_env() {
+  EnvKnobs e;
+  if (const char* v = getenv("LIBTOPK_LONG_ROW_THRESHOLD")) e.long_row_threshold = atoll(v);
+  if (const char* v = getenv("LIBTOPK_FORCE_CTAS_PER_GROUP")) e.force_ctas_per_group = atoi(v);
+  if (const char* v = getenv("LIBTOPK_BARRIER_TIMEOUT_US")) e.timeout_us = static_cast<uint32_t>(atoll(v));
+  return e;
+}
+
+const EnvKnobs& env_knobs() {
+  static const EnvKnobs e = read_env();
+  return e;
+}
+
+int query_device_locked(int device, topk_device_props* out) {
+  if (device < 0 || device >= kMaxDevices) return TOPK_ERR_INVALID_ARG;
+  DeviceEntry& d = g_dev[device];
+  if (!d.ready) {
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return TOPK_ERR_CUDA;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return TOPK_ERR_CUDA;
+    topk_device_props p{};
+    int rc = TOPK_OK;
+    if (cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess) {
+      rc = TOPK_ERR_CUDA;
+    }
+    p.smem_per_cta = static_cast<int>(ltk::kernel_smem_bytes());
+    if (rc == TOPK_OK && p.smem_per_cta <= p.max_smem_optin) {
+      if (ltk::kernel_configure() != cudaSuccess || ltk::kernel_occupancy(&p.ctas_per_sm) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
+    } else if (rc == TOPK_OK) {
+      p.ctas_per_sm = 0;  // the kernel cannot be resident; planning reports TOPK_ERR_PLAN
+    }
+    if (prev != device) cudaSetDevice(prev);
+    if (rc != TOPK_OK) {
+      cudaGetLastError();
+      return rc;
+    }
+    d.props = p;
+    d.ready = true;
+  }
+  *out = d.props;
+  return TOPK_OK;
+}
+
+int current_props(topk_device_props* out, int* device) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return TOPK_ERR_CUDA;
+  }
+  if (device) *device = dev;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return query_device_locked(dev, out);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* topk_status_string(int code) {
+  switch (code) {
+    case TOPK_OK: return "ok";
+    case TOPK_ERR_INVALID_ARG: return "invalid argument";
+    case TOPK_ERR_UNSUPPORTED_TOPK: return "topk must be 512, 1024 or 2048";
+    case TOPK_ERR_MISALIGNED: return "misaligned pointer";
+    case TOPK_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case TOPK_ERR_CUDA: return "CUDA runtime error";
+    case TOPK_ERR_BARRIER_TIMEOUT: return "a device-side wait timed out";
+    case TOPK_ERR_LENGTH_CLAMPED: return "a row length was outside [0, row_stride]";
+    case TOPK_ERR_PLAN: return "no launch configuration fits the device";
+    default: return "unknown status";
+  }
+}
+
+int topk_query_device(int device, topk_device_props* props) {
+  if (props == nullptr) return TOPK_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return query_device_locked(device, props);
+}
+
+size_t topk_workspace_size(int device, int64_t num_rows, int64_t row_stride, int next_n, int topk) {
+  (void)num_rows;
+  (void)row_stride;
+  (void)next_n;
+  (void)topk;
+  topk_device_props p{};
+  if (topk_query_device(device, &p) != TOPK_OK) return 0;
+  return ltk::workspace_bytes_for(p.num_sms);
+}
+
+int topk_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (workspace == nullptr || bytes < ltk::kWsHeaderBytes) return TOPK_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return TOPK_ERR_MISALIGNED;
+  if (cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return TOPK_ERR_CUDA;
+  }
+  return TOPK_OK;
+}
+
+int topk_get_status(const void* workspace, void* stream, uint32_t* device_status) {
+  if (workspace == nullptr || device_status == nullptr) return TOPK_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return TOPK_ERR_CUDA;
+  }
+  *device_status = word;
+  return TOPK_OK;
+}
+
+int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths, int64_t num_rows,
+                   int next_n, int topk, int32_t* out_idx, void* workspace, void* stream,
+                   const topk_options* options) {
+  if (num_rows < 0 || row_stride < 1 || next_n < 1 || (num_rows % next_n) != 0)
+    return TOPK_ERR_INVALID_ARG;
+  if (!(topk == 512 || topk == 1024 || topk == 2048)) return TOPK_ERR_UNSUPPORTED_TOPK;
+  if (num_rows == 0) return TOPK_OK;
+  if (logits == nullptr || lengths == nullptr || out_idx == nullptr || workspace == nullptr)
+    return TOPK_ERR_INVALID_ARG;
+  if (!aligned(logits, 4) || !aligned(lengths, 4) || !aligned(out_idx, 4) || !aligned(workspace, 16))
+    return TOPK_ERR_MISALIGNED;
+
+  topk_device_props props{};
+  int rc = current_props(&props, nullptr);
+  if (rc != TOPK_OK) return rc;
+  if (options != nullptr && options->workspace_bytes != 0 &&
+      options->workspace_bytes < ltk::workspace_bytes_for(props.num_sms))
+    return TOPK_ERR_WORKSPACE_TOO_SMALL;
+
+  const EnvKnobs& env = env_knobs();
+  topk_options opt{};
+  if (options != nullptr) opt = *options;
+  if (opt.long_row_threshold == 0) opt.long_row_threshold = env.long_row_threshold;
+  if (opt.force_ctas_per_group == 0) opt.force_ctas_per_group = env.force_ctas_per_group;
+  if (opt.barrier_timeout_us == 0) opt.barrier_timeout_us = env.timeout_us;
+
+  topk_plan plan{};
+  rc = topk_make_plan(&props, num_rows, row_stride, next_n, topk, &opt, &plan);
+  if (rc != TOPK_OK) return rc;
+  if (plan.grid < 1) return TOPK_OK;
+
+  ltk::Params p{};
+  p.logits = logits;
+  p.stride = row_stride;
+  p.lengths = lengths;
+  p.num_rows = num_rows;
+  p.out = out_idx;
+  p.topk = topk;
+  p.G = plan.ctas_per_group;
+  p.num_groups = plan.num_groups;
+  p.status = static_cast<uint32_t*>(workspace);
+  p.groups = reinterpret_cast<ltk::GroupWs*>(static_cast<char*>(workspace) + ltk::kWsHeaderBytes);
+  p.timeout_ns = opt.barrier_timeout_us ? static_cast<uint64_t>(opt.barrier_timeout_us) * 1000ull
+                                        : ltk::kDefaultTimeoutNs;
+  p.inject = opt.inject_skip_arrival;
+  if (ltk::launch_topk(p, plan.grid, plan.cooperative != 0, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return TOPK_ERR_CUDA;
+  }
+  return TOPK_OK;
+}
+
+int topk_ragged(const float* logits, int64_t row_stride, const int32_t* lengths, int64_t num_rows,
+                int next_n, int topk, int32_t* out_idx, void* workspace, void* stream) {
+  return topk_ragged_ex(logits, row_stride, lengths, num_rows, next_n, topk, out_idx, workspace,
+                        stream, nullptr);
+}
+
+}  // extern "C"

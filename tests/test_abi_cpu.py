@@ -1,0 +1,59 @@
+"""libtopk loads, exports every declared entry point, and rejects bad arguments on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_row_gb300 as sar
+from sparse_attention_row_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return ctypes.CDLL(sar.library_path())
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "libtopk.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(topk_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert set(sar.EXPORTED) == set(names), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(0, 9):
+        assert sar.topk_status_string(code)
+    assert sar.topk_status_string(2).startswith("topk must be")
+
+
+def test_host_validation_needs_no_gpu(lib):
+    fake = 0x10000  # never dereferenced: validation fails before any CUDA call
+    assert sar.topk_ragged(fake, 4096, fake, 8, 1, 100, fake, fake, None) == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert sar.topk_ragged(fake, 4096, fake, -1, 1, 512, fake, fake, None) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_ragged(fake, 0, fake, 8, 1, 512, fake, fake, None) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_ragged(fake, 4096, fake, 9, 2, 512, fake, fake, None) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_ragged(fake, 4096, fake, 0, 1, 512, fake, fake, None) == sar.TOPK_OK
+    assert sar.topk_ragged(None, 4096, fake, 8, 1, 512, fake, fake, None) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_ragged(fake + 2, 4096, fake, 8, 1, 512, fake, fake, None) == sar.TOPK_ERR_MISALIGNED
+    assert sar.topk_ragged(fake, 4096, fake, 8, 1, 512, fake, fake + 4, None) == sar.TOPK_ERR_MISALIGNED
+    assert sar.topk_workspace_init(None, 1024, None) == sar.TOPK_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(sar, "_LIB_PATH", str(tmp_path / "libtopk.so"))
+    monkeypatch.setattr(sar, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        sar.topk_status_string(0)

@@ -1,0 +1,129 @@
+"""Bit-exact parity of libtopk's CUDA path with the CPU oracle (GPU only)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import workloads
+from tests.gpu_util import Runner, assert_matches_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rn():
+    return Runner()
+
+
+SMALL = [("decode_small", 8), ("decode_batch", 16), ("long_coop", 4), ("mtp", 8), ("prefill", 24)]
+
+
+@pytest.mark.parametrize("name,rows", SMALL)
+def test_workloads_small_auto(rn, name, rows):
+    w = workloads.make(name, rows)
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n)
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=name)
+    assert rn.workspace_clean()
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 9, 16])
+@pytest.mark.parametrize("name,rows", [("decode_batch", 6), ("long_coop", 3), ("mtp", 4), ("prefill", 4)])
+def test_workloads_forced_split(rn, name, rows, G):
+    w = workloads.make(name, rows)
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(force_ctas_per_group=G))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} G={G}")
+    assert rn.workspace_clean()
+
+
+@pytest.mark.parametrize("name", workloads.NAMES)
+def test_workloads_full_size(rn, name):
+    """Every row of the full workload, in the launch configuration the benchmark times."""
+    w = workloads.make(name)
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n)
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=name + " full")
+    assert rn.workspace_clean()
+
+
+def _edge_rows(S: int, K: int, rng) -> tuple[np.ndarray, np.ndarray]:
+    rows, lens = [], []
+    base = rng.standard_normal(S).astype(np.float32)
+    for L in (0, 1, K - 1, K, K + 1, 2 * K + 3, S - 1, S):
+        rows.append(base.copy())
+        lens.append(L)
+    rows.append(np.full(S, 0.75, np.float32)); lens.append(S)                   # all equal
+    rows.append(np.where(rng.random(S) < 0.5, -0.0, 0.0).astype(np.float32)); lens.append(S)  # +-0 mix
+    r = rng.standard_normal(S).astype(np.float32)
+    r[rng.integers(0, S, 50)] = np.inf
+    r[rng.integers(0, S, 50)] = -np.inf
+    rows.append(r); lens.append(S - 3)                                           # +-inf inside
+    d = (rng.integers(-40, 40, S).astype(np.float32) * np.float32(1e-45))
+    rows.append(d); lens.append(S)                                               # subnormals
+    rows.append(np.arange(S, dtype=np.float32)); lens.append(S - 5)              # increasing
+    rows.append(-np.arange(S, dtype=np.float32)); lens.append(S)                 # decreasing
+    neg = -np.abs(rng.standard_normal(S)).astype(np.float32)
+    rows.append(neg); lens.append(S)                                             # all negative
+    few = np.full(S, -1.0, np.float32)
+    few[rng.choice(S, K // 2, replace=False)] = 2.0
+    rows.append(few); lens.append(S)                                             # K/2 distinct winners, ties below
+    return np.stack(rows), np.array(lens, np.int32)
+
+
+@pytest.mark.parametrize("topk", [512, 1024, 2048])
+@pytest.mark.parametrize("S", [4096, 9001, 40000])
+@pytest.mark.parametrize("G", [0, 1, 4])
+def test_edge_cases(rn, topk, S, G):
+    rng = np.random.default_rng(S + topk)
+    x, lens = _edge_rows(S, topk, rng)
+    got = rn.run(x, lens, topk, options=rn.options(force_ctas_per_group=G))
+    assert_matches_oracle(x, lens, got, topk, label=f"edges S={S} K={topk} G={G}")
+    assert rn.workspace_clean()
+
+
+@pytest.mark.parametrize("G", [1, 3])
+def test_poison_beyond_length_is_never_used(rn, G):
+    w = workloads.make("decode_batch", 8)
+    x = w.logits.copy()
+    cols = np.arange(x.shape[1])[None, :]
+    beyond = cols >= w.lengths[:, None]
+    x[beyond & (cols % 2 == 0)] = np.nan
+    x[beyond & (cols % 2 == 1)] = np.inf
+    got = rn.run(x, w.lengths, w.topk, options=rn.options(force_ctas_per_group=G))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, label="poison")
+
+
+@pytest.mark.parametrize("shift", [1, 2, 3])
+@pytest.mark.parametrize("stride_delta", [0, 1, 3])
+def test_unaligned_rows(rn, shift, stride_delta):
+    rng = np.random.default_rng(shift * 7 + stride_delta)
+    S = 20000 + stride_delta
+    x = rng.standard_normal((5, S)).astype(np.float32)
+    lens = np.array([S, S - 1, 3000, 12345, 2049], np.int32)
+    for G in (1, 2):
+        got = rn.run(x, lens, 2048, pad_front=shift, options=rn.options(force_ctas_per_group=G))
+        assert_matches_oracle(x, lens, got, 2048, label=f"shift={shift} S={S} G={G}")
+
+
+def test_lengths_are_clamped_and_flagged(rn):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4, 5000)).astype(np.float32)
+    lens = np.array([-3, 99999, 5000, 600], np.int32)
+    rn.sel.reset()
+    got = rn.run(x, lens, 512, check_status=False)
+    assert_matches_oracle(x, lens, got, 512, label="clamp")
+    assert rn.sel.status() & rn.sar.TOPK_DEV_LENGTH_CLAMPED
+    rn.sel.reset()
+    assert rn.sel.status() == 0
+
+
+def test_many_rows_per_cta_and_per_group(rn):
+    rng = np.random.default_rng(9)
+    S = 6000
+    x = np.round(rng.standard_normal((300, S)) * 4).astype(np.float32) / 4
+    lens = rng.integers(0, S, 300, endpoint=True).astype(np.int32)
+    # 4 CTAs: 75 rows each, beyond the shared-memory length cache
+    got = rn.run(x, lens, 1024, options=rn.options(max_ctas=4, force_ctas_per_group=1))
+    assert_matches_oracle(x, lens, got, 1024, label="G=1 persistent")
+    # 2 groups of 4 CTAs: every group loops over 150 rows, reusing its workspace
+    got = rn.run(x, lens, 1024, options=rn.options(max_ctas=8, force_ctas_per_group=4))
+    assert_matches_oracle(x, lens, got, 1024, label="G=4 persistent")
+    assert rn.workspace_clean()

@@ -1,0 +1,106 @@
+"""The host planner on made-up devices (pure function, no GPU)."""
+import itertools
+import random
+
+import pytest
+
+import sparse_attention_row_gb300 as sar
+from sparse_attention_row_gb300 import build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build_library()
+
+
+def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024):
+    p = sar.TopkDeviceProps()
+    p.num_sms, p.ctas_per_sm, p.smem_per_cta, p.max_smem_optin = num_sms, occ, smem, optin
+    return p
+
+
+def plan(p, rows, stride, next_n=1, topk=2048, **opt):
+    o = sar.TopkOptions()
+    for k, v in opt.items():
+        setattr(o, k, v)
+    return sar.topk_make_plan(p, rows, stride, next_n, topk, o)
+
+
+def test_the_five_workloads_on_a_gb300():
+    gb = props()
+    rc, pl = plan(gb, 8, 4096, topk=512)
+    assert rc == 0 and pl.ctas_per_group == 1 and pl.grid == 8 and not pl.cooperative
+    rc, pl = plan(gb, 64, 32768)
+    assert rc == 0 and pl.ctas_per_group == 1 and pl.grid == 64
+    rc, pl = plan(gb, 16, 131072)
+    assert rc == 0 and pl.ctas_per_group == 9 and pl.grid == 144 and pl.cooperative
+    rc, pl = plan(gb, 64, 163840, next_n=2, topk=1024)
+    assert rc == 0 and pl.ctas_per_group == 2 and pl.grid == 128 and pl.cooperative
+    rc, pl = plan(gb, 4096, 65536)
+    assert rc == 0 and pl.ctas_per_group == 1 and pl.grid == 152 and not pl.cooperative
+
+
+def test_topk1024_mtp1_never_oversubscribes():
+    # the deadlock case of the persistent kernel: long rows, TopK=1024, next_n=1
+    for occ, sms in itertools.product((1, 2, 3), (20, 48, 132, 152, 160)):
+        for rows in (1, 2, 3, 7, 16, 33, 64, 100, 1000, 5000):
+            rc, pl = plan(props(num_sms=sms, occ=occ), rows, 200000, topk=1024)
+            assert rc == 0
+            if pl.cooperative:
+                assert pl.grid <= sms * occ
+
+
+def test_invariants_on_random_shapes():
+    rng = random.Random(5)
+    for _ in range(3000):
+        sms, occ = rng.randint(1, 200), rng.randint(1, 4)
+        rows = rng.choice([0, 1, 2, rng.randint(1, 64), rng.randint(1, 100000)])
+        nn = rng.choice([1, 2, 4])
+        rows -= rows % nn
+        stride = rng.choice([1, 17, 4096, 32768, 32769, 131072, rng.randint(1, 1 << 22)])
+        topk = rng.choice([512, 1024, 2048])
+        force = rng.choice([0, 0, 0, 1, 2, 5, 16])
+        maxc = rng.choice([0, 0, rng.randint(1, 400)])
+        rc, pl = plan(props(num_sms=sms, occ=occ), rows, stride, next_n=nn, topk=topk,
+                      force_ctas_per_group=force, max_ctas=maxc)
+        cap = sms * occ if not maxc else min(sms * occ, maxc)
+        if rc == sar.TOPK_ERR_PLAN:
+            assert force > 1 and cap < force
+            continue
+        assert rc == 0
+        G = pl.ctas_per_group
+        assert 1 <= G <= 16
+        if force:
+            assert G == force
+        assert pl.grid == pl.num_groups * G
+        if rows == 0:
+            assert pl.grid == 0
+            continue
+        assert 1 <= pl.num_groups <= rows
+        if G > 1:
+            assert pl.cooperative == 1
+            assert pl.grid <= cap, (sms, occ, rows, stride, G)
+            assert pl.num_groups <= sms
+        else:
+            assert pl.cooperative == 0 and pl.grid <= cap
+
+
+def test_rejections():
+    gb = props()
+    assert plan(gb, 8, 4096, topk=100)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert plan(gb, 9, 4096, next_n=2)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 0)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 4096, force_ctas_per_group=17)[0] == sar.TOPK_ERR_INVALID_ARG
+    # a device whose opt-in shared memory cannot hold the kernel (a GB10-class ~99 KB part)
+    assert plan(props(optin=99 * 1024), 8, 200000)[0] == sar.TOPK_ERR_PLAN
+    assert plan(props(occ=0), 8, 4096)[0] == sar.TOPK_ERR_PLAN
+
+
+def test_threshold_and_capacity_knobs():
+    gb = props()
+    rc, pl = plan(gb, 16, 131072, long_row_threshold=200000)
+    assert rc == 0 and pl.ctas_per_group == 1
+    rc, pl = plan(gb, 16, 131072, max_ctas=40)
+    assert rc == 0 and pl.ctas_per_group == 2 and pl.grid <= 40
+    rc, pl = plan(gb, 3, 4096, force_ctas_per_group=4)
+    assert rc == 0 and pl.grid == 12 and pl.cooperative

@@ -1,0 +1,79 @@
+"""Workspace hygiene: no per-call memset, graph replay, bounded waits (GPU only)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests.gpu_util import Runner, assert_matches_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rn():
+    return Runner()
+
+
+def test_back_to_back_calls_share_one_workspace(rn):
+    """Alternating shapes and both paths, with no clearing between calls."""
+    cases = []
+    for name, rows in (("long_coop", 3), ("decode_batch", 8), ("mtp", 4), ("decode_small", 8)):
+        w = workloads.make(name, rows)
+        want, _ = oracle.topk_ragged(w.logits, w.lengths, w.topk, next_n=w.next_n)
+        cases.append((w, want))
+    rn.sel.reset()
+    for i in range(120):
+        w, want = cases[i % len(cases)]
+        G = (0, 1, 2, 7)[(i // len(cases)) % 4]
+        got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(force_ctas_per_group=G))
+        if i % 7 == 0 or i >= 112:
+            assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, want=want,
+                                  label=f"call {i} {w.name} G={G}")
+    assert rn.workspace_clean()
+    assert rn.sel.status() == 0
+
+
+def test_graph_replay_with_changing_inputs(rn):
+    torch = rn.torch
+    sar = rn.sar
+    rows, S, K = 12, 131072, 2048
+    xs = torch.zeros((rows, S), dtype=torch.float32, device=rn.dev)
+    ls = torch.zeros(rows, dtype=torch.int32, device=rn.dev)
+    out = torch.zeros((rows, K), dtype=torch.int32, device=rn.dev)
+    opts = rn.options(force_ctas_per_group=6)
+    # first call outside capture (device properties are cached on it)
+    assert sar.topk_ragged_ex(xs, S, ls, rows, 1, K, out, rn.sel.workspace, None, opts) == 0
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        rc = sar.topk_ragged_ex(xs, S, ls, rows, 1, K, out, rn.sel.workspace, None, opts)
+    assert rc == 0
+    rng = np.random.default_rng(4)
+    for it in range(6):
+        x = rng.standard_normal((rows, S)).astype(np.float32)
+        if it % 2:
+            x = np.round(x * 16) / 16
+        lens = rng.integers(0, S, rows, endpoint=True).astype(np.int32)
+        xs.copy_(torch.from_numpy(x))
+        ls.copy_(torch.from_numpy(lens))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_matches_oracle(x, lens, out.cpu().numpy(), K, label=f"replay {it}")
+        assert rn.workspace_clean()
+
+
+def test_timed_out_group_wait_reports_and_recovers(rn):
+    """A CTA that never arrives makes its partners' bounded waits run out."""
+    w = workloads.make("long_coop", 4)
+    rn.sel.reset()
+    opts = rn.options(force_ctas_per_group=2, inject_skip_arrival=1, barrier_timeout_us=20000)
+    rn.run(w.logits, w.lengths, w.topk, options=opts, check_status=False)
+    st = rn.sel.status()
+    assert st & rn.sar.TOPK_DEV_BARRIER_TIMEOUT, f"status {st:#x}"
+    # the context is still usable; re-initialising the workspace restores service
+    rn.sel.reset()
+    got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=2))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, label="after recovery")
+    assert rn.workspace_clean()
