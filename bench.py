@@ -7,7 +7,8 @@ hot path: load + key + filter + radix select + gather in one kernel launch).
 The headline workload is the decode batch: 64 rows, lengths uniform in
 [8192, 32768], row stride 32768, TopK 2048, N(0,1) logits rounded to the bf16
 grid. Inputs are resident in HBM before timing starts; an L2 flush (a 256 MiB
-write) runs between timed steps, outside the timed events. Per-step device time
+write followed by a read of the same buffer, so that L2 ends up clean) runs
+between timed steps, outside the timed events. Per-step device time
 comes from CUDA events on the launching stream.
 
 Prints ONE JSON line on rank 0. Extra keys: ``workloads`` (the five workloads,
@@ -190,6 +191,7 @@ class GpuBench:
         torch.cuda.set_device(self.dev)
         self.sel = sar.Selector(device_index)
         self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=self.dev)
+        self.stream_handle = int(torch.cuda.current_stream().cuda_stream)
 
     def upload(self, w: workloads.Workload):
         t = self.torch
@@ -200,9 +202,16 @@ class GpuBench:
 
     def call(self, w, x, ln, out):
         rc = self.sar.topk_ragged(x, w.row_stride, ln, w.num_rows, w.next_n, w.topk, out,
-                                  self.sel.workspace, None)
+                                  self.sel.workspace, self.stream_handle)
         if rc != 0:
             raise RuntimeError(f"topk_ragged: {self.sar.topk_status_string(rc)}")
+
+    def flush_l2(self):
+        """Evicts the inputs from L2: writes a buffer larger than L2, then reads it
+        back, so L2 holds clean lines and no write-back of the flush itself lands
+        inside the next timed launch."""
+        self.flush.fill_(1.0)
+        self.flush_sink = self.flush.sum()
 
     def time_kernel(self, w, steps: int, warmup: int, world: int = 1) -> dict:
         """Per-step device time of the single launch, L2 flushed before each step."""
@@ -210,15 +219,18 @@ class GpuBench:
         x, ln, out = self.upload(w)
         stream = t.cuda.current_stream()
         for _ in range(warmup):
-            self.flush.zero_()
+            self.flush_l2()
             self.call(w, x, ln, out)
         starts = [t.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [t.cuda.Event(enable_timing=True) for _ in range(steps)]
         barrier(world)
         t.cuda.synchronize()
         wall0 = time.perf_counter()
+        # a short device-side sleep lets the host queue the steps ahead of the GPU,
+        # so the per-step events see device time, not host submission gaps
+        t.cuda._sleep(20_000_000)
         for i in range(steps):
-            self.flush.zero_()
+            self.flush_l2()
             starts[i].record(stream)
             self.call(w, x, ln, out)
             ends[i].record(stream)
@@ -320,6 +332,18 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_only(args) -> None:
+    """Times one workload's kernel alone (for profiling runs); one JSON line."""
+    gb = GpuBench(0)
+    peak, _ = read_peaks()
+    w = workloads.make(args.only)
+    r = gb.time_kernel(w, args.steps, args.warmup)
+    gbs = w.valid_bytes() / (r["ms_mean"] * 1e-3) / 1e9
+    print(json.dumps({"workload": args.only, "us_per_call": r["ms_mean"] * 1e3,
+                      "us_per_call_median": r["ms_median"] * 1e3, "effective_gbs": gbs,
+                      "frac_of_hbm_peak": gbs / peak, "steps": args.steps}), flush=True)
+
+
 def run_ours(args) -> None:
     rank, world, local = dist_env()
     import torch
@@ -390,7 +414,7 @@ def run_ours(args) -> None:
         "data": "synthetic",
         "config": {"workload": f"{HEADLINE}: {DESCR[HEADLINE]}", "num_rows": w.num_rows,
                    "row_stride": w.row_stride, "topk": w.topk, "next_n": w.next_n,
-                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "l2": "flushed before every timed step (256 MiB write then read, outside the events)",
                    "parallelism": f"replica per GPU x{world}"},
         "us_per_call": ms * 1e3,
         "effective_gbs": gbs,
@@ -424,11 +448,13 @@ def main(argv=None) -> None:
     ap.add_argument("--other-steps", type=int, default=300, help="timed steps for the non-headline workloads")
     ap.add_argument("--cpu-budget", type=float, default=3.0, help="seconds of oracle wall time")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timings")
+    ap.add_argument("--only", default="", help="time only this workload's kernel (profiling runs)")
     args = ap.parse_args(argv)
-    if args.warmup < 3:
-        ap.error("--warmup must be at least 3")
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_ours(args)
 

@@ -20,7 +20,7 @@
 
 #include <algorithm>
 
-#include "../../include/libtopk.h"
+#include "libtopk.h"
 #include "topk_internal.h"
 
 namespace {

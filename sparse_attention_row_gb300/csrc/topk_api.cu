@@ -7,7 +7,7 @@
 
 #include <mutex>
 
-#include "../../include/libtopk.h"
+#include "libtopk.h"
 #include "topk_internal.h"
 
 namespace {

@@ -7,21 +7,23 @@
 namespace ltk {
 
 // CTA shape and shared-memory staging.
-constexpr int kThreads = 512;          // threads per CTA (16 warps)
+constexpr int kThreads = 768;          // consumer threads per CTA (24 warps)
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 4096;           // fp32 elements per staging slot (16 KB)
-constexpr int kStages = 6;             // staging slots in flight per CTA (96 KB)
+constexpr int kCtaThreads = kThreads + 32;  // plus one copy-issuing warp
+constexpr int kChunk = 6144;           // fp32 elements per staging slot (24 KB)
+constexpr int kStages = 4;             // staging slots in flight per CTA (96 KB)
 constexpr int kBins = 4096;            // 12-bit radix digits
-constexpr int kBufCap = 8192;          // candidate (key, index) pairs kept per CTA
+constexpr int kBufCap = 12288;         // candidate (key, index) pairs kept per CTA
 constexpr int kMaxTopK = 2048;
 constexpr int kMaxGroup = 16;          // CTAs that may split one row
 constexpr int kLenCache = 64;          // row lengths cached in shared memory
+constexpr int kSmallSet = 64;          // candidate sets up to this size are ranked by one warp
 constexpr int kMinSpan = 8192;         // fewest elements per CTA when a row is split
 constexpr int64_t kDefaultLongRowThreshold = 32768;
 constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 static_assert(kMaxTopK + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");
-static_assert(kBufCap <= 65536, "candidate positions are stored as 16-bit values");
+static_assert(kChunk % (4 * kThreads) == 0, "a chunk is a whole number of float4 per thread");
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.

@@ -1,25 +1,31 @@
-// Ragged per-row top-K for sm_103a: streaming filter + radix select.
+// Ragged per-row top-K for sm_103a: seeded streaming filter + exact radix select.
 //
 // One kernel serves every row length. A CTA (or a group of G CTAs that split
 // one row) streams its part of the row from HBM through a ring of shared-memory
-// slots filled by bulk asynchronous copies (cp.async.bulk, completion counted
-// on an mbarrier). While streaming it keeps a 12-bit histogram of the keys it
-// has kept and a running threshold bin: once K kept keys sit at or above a bin,
-// every later key below that bin can never be selected and is dropped at once.
-// Only the survivors are written to a shared-memory candidate buffer, so each
-// logit is read from HBM exactly once and most of them cost a compare.
+// slots. A dedicated copy warp keeps the ring full with bulk asynchronous
+// copies (cp.async.bulk, completion counted on "full" mbarriers; consumers free
+// slots through "empty" mbarriers), so each logit crosses HBM exactly once.
 //
-// At the end of the row the candidates go through an exact radix select on the
-// composite key (value bits, then inverted index bits), which settles ties by
-// the smaller index. When G > 1 the CTAs of a group merge their histograms
-// through a workspace in global memory, meeting at a group barrier after each
-// radix pass; this replaces the per-row RadixRowState of the persistent_topk
-// kernel (vLLM PR #41444 page, "Executive summary": arrival counter plus
-// histogram per row group). Every workspace word a launch touches is returned
-// to zero before the launch ends, with the fencing that the vLLM PR #41748
-// page's review asks for ("Code Review": zero in parallel, and reset the
-// arrival counter only after the zeros are visible), so no per-call memset is
-// needed and graph replays start from a clean workspace.
+// Filtering: the first staged chunk of a row is histogrammed on the top 12 bits
+// of the keys and seeds a threshold aimed at about 1.5 K survivors over the
+// whole row. Every later element costs one fp32 compare against that threshold;
+// only survivors become (key, index) candidates in shared memory. At the end of
+// the row the seed is verified: if fewer than K elements reached it, the row is
+// streamed again with no threshold (exact whatever the data). A candidate
+// buffer that runs full is shrunk, first to the current threshold bin, then if
+// needed to exactly the K best, raising the threshold each time.
+//
+// Selection: an exact radix select on the composite key (value bits, then index)
+// finds the K-th candidate (T, I); the output is {key > T} + {key == T, index <=
+// I}, so equal values go to the smaller index. When G > 1 the CTAs of a group
+// merge their histograms through a workspace in global memory, meeting at a
+// group barrier after each radix pass; this replaces the per-row RadixRowState
+// of the persistent_topk kernel (vLLM PR #41444 page, "Executive summary":
+// arrival counter plus histogram per row group). Every workspace word a launch
+// touches is returned to zero before the launch ends, with the fencing that the
+// vLLM PR #41748 page's review asks for ("Code Review": zero in parallel, reset
+// the arrival counter only after the zeros are visible), so no per-call memset
+// is needed and graph replays start from a clean workspace.
 //
 // Keys: an fp32 value x maps to a uint32 whose unsigned order is the order of
 // the values: -0.0 is first mapped to +0.0, then positive values get the sign
@@ -37,20 +43,23 @@ struct __align__(128) Smem {
   uint32_t hist[kBins];           // histogram of kept keys (also radix scratch)
   uint32_t bkey[kBufCap];         // candidate keys
   int32_t bidx[kBufCap];          // candidate indices (row-relative)
-  uint16_t listA[kBufCap];        // candidate positions, ping
-  uint16_t listB[kBufCap];        // candidate positions, pong
-  uint16_t emit[kMaxTopK];        // positions selected for output
+  int32_t emit[kMaxTopK];         // selected indices of the row being finished
+  int32_t small[kSmallSet];       // candidate positions ranked by one warp
   unsigned long long full[kStages];
+  unsigned long long empty[kStages];
   int32_t lens[kLenCache];
   uint32_t wtot[kWarps];
   int g_e[kMaxGroup];
   int g_tot[kMaxGroup];
-  int buf_n, buf_mark, n_emit, nA, nB;
+  int buf_n, buf_mark, n_emit, n_small;
   int t, cnt_ge;
   uint32_t thr_lo;
+  float thr_f;
   int find_b, find_gt;
   int abort, last, off, take;
-  uint32_t min_key;
+  uint32_t red;
+  uint32_t sel_T;
+  int sel_I;
 };
 
 // ---------------------------------------------------------------- primitives
@@ -64,6 +73,9 @@ __device__ __forceinline__ uint64_t global_timer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Barrier among the consumer warps only (the copy warp never joins it).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
 
 __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
@@ -81,6 +93,10 @@ __device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
@@ -104,15 +120,16 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
   return ok != 0;
 }
 
-// Waits for an mbarrier phase, giving up after timeout_ns.
+// Waits for an mbarrier phase, giving up after timeout_ns or when *abort is set.
 __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
-                                                  uint64_t timeout_ns) {
+                                                  uint64_t timeout_ns, const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
     if (global_timer() - t0 > timeout_ns) return false;
   }
 }
@@ -150,15 +167,13 @@ __device__ __forceinline__ uint32_t fkey(float x) {
   return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
-// Radix digit of the composite key (key, ~index) at a level:
-// 0: key 31..20, 1: key 19..8, 2: key 7..0, 3: ~idx 31..20, 4: ~idx 19..8, 5: ~idx 7..0.
-__device__ __forceinline__ uint32_t digit_of(int level, uint32_t key, int32_t idx) {
-  const uint32_t v = (level < 3) ? key : ~static_cast<uint32_t>(idx);
-  const int l = (level < 3) ? level : level - 3;
-  return (l == 0) ? (v >> 20) : (l == 1) ? ((v >> 8) & 0xFFFu) : (v & 0xFFu);
+// fp32 value whose ">=" test is equivalent to "key >= k" for every non-NaN input.
+__device__ __forceinline__ float key_floor_value(uint32_t k) {
+  if (k <= 0x007FFFFFu) return -__int_as_float(0x7F800000);  // at or below key(-inf): all pass
+  if (k > 0xFF800000u) return __int_as_float(0x7FC00000);     // above key(+inf): NaN, none pass
+  const uint32_t u = (k & 0x80000000u) ? (k ^ 0x80000000u) : ~k;
+  return __uint_as_float(u);
 }
-
-__device__ __forceinline__ int level_bins(int level) { return (level == 2 || level == 5) ? 256 : kBins; }
 
 // Appends `val` to list[] (capacity `cap`) for every lane with `pred`, one
 // shared atomic per warp. Entries past the capacity are dropped (never written).
@@ -175,133 +190,299 @@ __device__ __forceinline__ void warp_push(T* list, int* counter, int cap, bool p
 
 // ----------------------------------------------------------------- radix find
 
-// Finds the largest bin b of s.hist[0, nb) with sum(hist[b:]) >= need (need >= 1
-// and the total must reach need). Writes b to s.find_b and sum(hist[b+1:]) to
-// s.find_gt. Block-wide; ends with a barrier.
-__device__ void block_find(Smem& s, int nb, int need) {
+// Over s.hist[0, nb) (nb a power of two, 256..4096): with from_top, finds the
+// largest bin b whose suffix sum (bins >= b) reaches `need`; otherwise the
+// smallest bin b whose prefix sum (bins <= b) reaches `need`. Writes b to
+// s.find_b and the count strictly beyond b (above it, or below it) to
+// s.find_gt. Requires need >= 1 and a total of at least need. Consumer-wide;
+// starts and ends with a barrier.
+__device__ void block_find(Smem& s, int nb, int need, bool from_top) {
   const int tid = threadIdx.x;
-  const int per = (nb + kThreads - 1) / kThreads;
-  const int nact = nb / per;
-  const int lo = tid * per;
+  const int lane = static_cast<int>(lane_id());
+  const int warp = tid >> 5;
+  const int nact = nb < 512 ? nb : 512;
+  const int per = nb / nact;
+  csync();
   if (tid == 0) {
     s.find_b = 0;
     s.find_gt = 0;
   }
+  // thread tid covers scan positions [tid*per, tid*per + per); position p is
+  // bin nb-1-p when scanning from the top, bin p otherwise
   uint32_t sum = 0;
   if (tid < nact)
-    for (int j = 0; j < per; ++j) sum += s.hist[lo + j];
-  uint32_t suf = sum;  // suffix sum within the warp (lanes at and above this one)
+    for (int j = 0; j < per; ++j) {
+      const int p = tid * per + j;
+      sum += s.hist[from_top ? nb - 1 - p : p];
+    }
+  uint32_t incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, suf, o);
-    if (lane_id() + o < 32) suf += v;
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
   }
-  const int warp = tid >> 5;
-  if (lane_id() == 0) s.wtot[warp] = suf;
-  __syncthreads();
-  uint32_t above = 0;
-  for (int w = warp + 1; w < kWarps; ++w) above += s.wtot[w];
-  const uint32_t incl = suf + above;  // sum of bins >= lo
-  const uint32_t excl = incl - sum;   // sum of bins >= lo + per
+  if (lane == 31) s.wtot[warp] = incl;
+  csync();
+  for (int w = 0; w < warp; ++w) incl += s.wtot[w];
+  const uint32_t excl = incl - sum;
   if (tid < nact && incl >= static_cast<uint32_t>(need) && excl < static_cast<uint32_t>(need)) {
     uint32_t run = excl;
-    for (int j = per - 1; j >= 0; --j) {
-      const uint32_t h = s.hist[lo + j];
+    for (int j = 0; j < per; ++j) {
+      const int p = tid * per + j;
+      const int b = from_top ? nb - 1 - p : p;
+      const uint32_t h = s.hist[b];
       if (run + h >= static_cast<uint32_t>(need)) {
-        s.find_b = lo + j;
+        s.find_b = b;
         s.find_gt = static_cast<int>(run);
         break;
       }
       run += h;
     }
   }
-  __syncthreads();
+  csync();
 }
 
-// Candidates at s.listX positions: emits those whose digit is above b and moves
-// those equal to b into dst. Warp-uniform loop; no barrier.
-__device__ void partition_list(Smem& s, const uint16_t* src, int n, int level, uint32_t b,
-                               uint16_t* dst, int* dst_n) {
-  const int warp = threadIdx.x >> 5;
-  for (int base = warp * 32; base < n; base += kThreads) {
-    const int i = base + static_cast<int>(lane_id());
-    const bool in = i < n;
-    const uint16_t pos = in ? src[i] : static_cast<uint16_t>(0);
-    const uint32_t d = in ? digit_of(level, s.bkey[pos], s.bidx[pos]) : 0u;
-    warp_push<uint16_t>(s.emit, &s.n_emit, kMaxTopK, in && d > b, pos);
-    warp_push<uint16_t>(dst, dst_n, kBufCap, in && d == b, pos);
+// hist[(key >> shift) & mask] counts buffer entries with (key >> pshift) == prefix.
+__device__ void hist_keys(Smem& s, int nb, uint32_t prefix, int pshift, int shift, uint32_t mask) {
+  const int tid = threadIdx.x;
+  csync();
+  for (int b = tid; b < nb; b += kThreads) s.hist[b] = 0;
+  csync();
+  const int n = s.buf_n;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t k = s.bkey[i];
+    if ((k >> pshift) == prefix) atomicAdd(&s.hist[(k >> shift) & mask], 1u);
   }
+  csync();
 }
 
-// Buffer entries: emits those with key bits 31..20 above b, lists those equal to b.
-__device__ void partition_buffer(Smem& s, uint32_t b) {
+// hist[(idx >> shift) & mask] counts entries with key == T and (idx >> pshift) == prefix.
+__device__ void hist_tied_indices(Smem& s, int nb, uint32_t T, uint32_t prefix, int pshift, int shift,
+                                  uint32_t mask) {
+  const int tid = threadIdx.x;
+  csync();
+  for (int b = tid; b < nb; b += kThreads) s.hist[b] = 0;
+  csync();
+  const int n = s.buf_n;
+  for (int i = tid; i < n; i += kThreads) {
+    if (s.bkey[i] != T) continue;
+    const uint32_t x = static_cast<uint32_t>(s.bidx[i]);
+    if ((x >> pshift) == prefix) atomicAdd(&s.hist[(x >> shift) & mask], 1u);
+  }
+  csync();
+}
+
+// Smallest key among buffer entries with (key >> pshift) == prefix.
+__device__ uint32_t block_min_key(Smem& s, uint32_t prefix, int pshift) {
+  csync();
+  if (threadIdx.x == 0) s.red = 0xFFFFFFFFu;
+  csync();
+  uint32_t mn = 0xFFFFFFFFu;
+  const int n = s.buf_n;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint32_t k = s.bkey[i];
+    if ((k >> pshift) == prefix) mn = min(mn, k);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+  if (lane_id() == 0 && mn != 0xFFFFFFFFu) atomicMin(&s.red, mn);
+  csync();
+  return s.red;
+}
+
+// Largest index among entries with key == T and (idx >> pshift) == prefix.
+__device__ int block_max_tied_index(Smem& s, uint32_t T, uint32_t prefix, int pshift) {
+  csync();
+  if (threadIdx.x == 0) s.red = 0u;
+  csync();
+  uint32_t mx = 0u;
+  const int n = s.buf_n;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    if (s.bkey[i] != T) continue;
+    const uint32_t x = static_cast<uint32_t>(s.bidx[i]);
+    if ((x >> pshift) == prefix) mx = max(mx, x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if (lane_id() == 0 && mx != 0u) atomicMax(&s.red, mx);
+  csync();
+  return static_cast<int>(s.red);
+}
+
+// Number of buffer entries for which pred(key, idx) holds.
+template <class Pred>
+__device__ int block_count(Smem& s, Pred pred) {
+  csync();
+  if (threadIdx.x == 0) s.red = 0u;
+  csync();
   const int warp = threadIdx.x >> 5;
   const int n = s.buf_n;
   for (int base = warp * 32; base < n; base += kThreads) {
     const int i = base + static_cast<int>(lane_id());
-    const bool in = i < n;
-    const uint32_t d = in ? (s.bkey[i] >> 20) : 0u;
-    warp_push<uint16_t>(s.emit, &s.n_emit, kMaxTopK, in && d > b, static_cast<uint16_t>(i));
-    warp_push<uint16_t>(s.listA, &s.nA, kBufCap, in && d == b, static_cast<uint16_t>(i));
+    const bool p = i < n && pred(s.bkey[i], s.bidx[i]);
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, p);
+    if (lane_id() == 0 && m) atomicAdd(&s.red, static_cast<uint32_t>(__popc(m)));
   }
+  csync();
+  return static_cast<int>(s.red);
 }
 
-// Emits exactly `need` positions of A (all sharing the digits of the levels
-// before `level`): the best ones under (key desc, index asc). Uses s.hist as
-// scratch. Block-wide; ends with a barrier.
-__device__ void select_exact(Smem& s, uint16_t* A, uint16_t* B, int nA, int need, int level) {
-  const int tid = threadIdx.x;
-  while (need > 0) {
-    if (need >= nA) {
-      for (int base = (tid >> 5) * 32; base < nA; base += kThreads) {
-        const int i = base + static_cast<int>(lane_id());
-        warp_push<uint16_t>(s.emit, &s.n_emit, kMaxTopK, i < nA, i < nA ? A[i] : static_cast<uint16_t>(0));
-      }
-      break;
-    }
-    if (nA <= 32 || level > 5) {
-      // Direct ranking inside one warp; composite keys are distinct, so exactly
-      // `need` lanes have rank < need. (level > 5 cannot happen with distinct
-      // composite keys; it is kept as a terminating case.)
-      if (tid < 32) {
-        const int lane = static_cast<int>(lane_id());
-        const bool in = lane < nA;
-        const uint16_t pos = in ? A[lane] : static_cast<uint16_t>(0);
-        const uint32_t hi = in ? s.bkey[pos] : 0u;
-        const uint32_t lo = in ? ~static_cast<uint32_t>(s.bidx[pos]) : 0u;
-        int rank = 0;
-        const int lim = nA < 32 ? nA : 32;
-        for (int j = 0; j < lim; ++j) {
-          const uint32_t h2 = __shfl_sync(0xFFFFFFFFu, hi, j);
-          const uint32_t l2 = __shfl_sync(0xFFFFFFFFu, lo, j);
-          rank += (h2 > hi || (h2 == hi && l2 > lo)) ? 1 : 0;
-        }
-        warp_push<uint16_t>(s.emit, &s.n_emit, kMaxTopK, in && rank < need, pos);
-      }
-      break;
-    }
-    const int nb = level_bins(level);
-    for (int b = tid; b < nb; b += kThreads) s.hist[b] = 0;
-    __syncthreads();
-    for (int i = tid; i < nA; i += kThreads) {
-      const uint16_t pos = A[i];
-      atomicAdd(&s.hist[digit_of(level, s.bkey[pos], s.bidx[pos])], 1u);
-    }
-    if (tid == 0) s.nB = 0;
-    __syncthreads();
-    block_find(s, nb, need);
-    const uint32_t b = static_cast<uint32_t>(s.find_b);
-    const int gt = s.find_gt;
-    partition_list(s, A, nA, level, b, B, &s.nB);
-    __syncthreads();
-    need -= gt;
-    nA = s.nB;
-    uint16_t* tmp = A;
-    A = B;
-    B = tmp;
-    ++level;
+// Collects the positions of the entries for which pred holds into s.small
+// (the caller knows there are at most kSmallSet of them); returns the count.
+template <class Pred>
+__device__ int gather_small(Smem& s, Pred pred) {
+  csync();
+  if (threadIdx.x == 0) s.n_small = 0;
+  csync();
+  const int warp = threadIdx.x >> 5;
+  const int n = s.buf_n;
+  for (int base = warp * 32; base < n; base += kThreads) {
+    const int i = base + static_cast<int>(lane_id());
+    const bool p = i < n && pred(s.bkey[i], s.bidx[i]);
+    warp_push<int32_t>(s.small, &s.n_small, kSmallSet, p, i);
   }
-  __syncthreads();
+  csync();
+  return min(s.n_small, kSmallSet);
+}
+
+// One warp ranks the m <= kSmallSet candidates in s.small by (key desc, index
+// asc) and stores the need-th best one (1 <= need <= m) in s.sel_T / s.sel_I.
+// Consumer-wide; ends with a barrier.
+__device__ void rank_small(Smem& s, int m, int need) {
+  if (threadIdx.x < 32) {
+    const int lane = static_cast<int>(lane_id());
+    uint32_t hk[2], lk[2];
+    int ix[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = lane + 32 * h;
+      hk[h] = 0u;
+      lk[h] = 0u;
+      ix[h] = -1;
+      if (e < m) {
+        const int pos = s.small[e];
+        hk[h] = s.bkey[pos];
+        ix[h] = s.bidx[pos];
+        lk[h] = ~static_cast<uint32_t>(ix[h]);
+      }
+    }
+    int rank[2] = {0, 0};
+    for (int j = 0; j < m; ++j) {
+      const int src = j & 31;
+      const uint32_t ohk = __shfl_sync(0xFFFFFFFFu, (j < 32) ? hk[0] : hk[1], src);
+      const uint32_t olk = __shfl_sync(0xFFFFFFFFu, (j < 32) ? lk[0] : lk[1], src);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) rank[h] += (ohk > hk[h] || (ohk == hk[h] && olk > lk[h])) ? 1 : 0;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (lane + 32 * h < m && rank[h] == need - 1) {
+        s.sel_T = hk[h];
+        s.sel_I = ix[h];
+      }
+    }
+  }
+  csync();
+}
+
+// Among entries with key == T, the need-th smallest index (1 <= need <= count).
+// Radix on the index from the top bit down: 11, 10, 10 bits.
+__device__ int select_tied_indices(Smem& s, uint32_t T, int need) {
+  uint32_t prefix = 0;
+  int pshift = 31;
+#pragma unroll 1
+  for (int l = 0; l < 3; ++l) {
+    const int bits = (l == 0) ? 11 : 10;
+    const int shift = (l == 0) ? 20 : (l == 1) ? 10 : 0;
+    const int nb = 1 << bits;
+    hist_tied_indices(s, nb, T, prefix, pshift, shift, static_cast<uint32_t>(nb - 1));
+    block_find(s, nb, need, false);
+    const uint32_t b = static_cast<uint32_t>(s.find_b);
+    need -= s.find_gt;
+    const int c = static_cast<int>(s.hist[b]);
+    prefix = (prefix << bits) | b;
+    pshift = shift;
+    if (need == c) return block_max_tied_index(s, T, prefix, pshift);
+  }
+  return static_cast<int>(prefix);
+}
+
+// The selection of exactly K in-play entries (bits 31..20 >= t) expressed as a
+// composite threshold: the set {key > T} + {key == T and idx <= I}. Small
+// candidate sets are ranked by one warp, larger ones go through radix levels.
+// Uses hist as scratch.
+__device__ void select_threshold(Smem& s, int K, uint32_t& T, int& I) {
+  csync();
+  const uint32_t t = static_cast<uint32_t>(s.t);
+  const int inbin = static_cast<int>(s.hist[t]);
+  int need = K - (s.cnt_ge - inbin);
+  I = 0x7FFFFFFF;
+  if (need >= inbin) {
+    T = block_min_key(s, t, 20);
+    return;
+  }
+  if (inbin <= kSmallSet) {
+    const int m = gather_small(s, [=](uint32_t k, int32_t) { return (k >> 20) == t; });
+    rank_small(s, m, need);
+    T = s.sel_T;
+    I = s.sel_I;
+    return;
+  }
+  hist_keys(s, kBins, t, 20, 8, 0xFFFu);
+  block_find(s, kBins, need, true);
+  const uint32_t b1 = static_cast<uint32_t>(s.find_b);
+  need -= s.find_gt;
+  const int c1 = static_cast<int>(s.hist[b1]);
+  const uint32_t p1 = (t << 12) | b1;
+  if (need >= c1) {
+    T = block_min_key(s, p1, 8);
+    return;
+  }
+  if (c1 <= kSmallSet) {
+    const int m = gather_small(s, [=](uint32_t k, int32_t) { return (k >> 8) == p1; });
+    rank_small(s, m, need);
+    T = s.sel_T;
+    I = s.sel_I;
+    return;
+  }
+  hist_keys(s, 256, p1, 8, 0, 0xFFu);
+  block_find(s, 256, need, true);
+  const uint32_t b2 = static_cast<uint32_t>(s.find_b);
+  need -= s.find_gt;
+  const int c2 = static_cast<int>(s.hist[b2]);
+  T = (p1 << 8) | b2;
+  if (need >= c2) return;
+  if (c2 <= kSmallSet) {
+    const uint32_t TT = T;
+    const int m = gather_small(s, [=](uint32_t k, int32_t) { return k == TT; });
+    rank_small(s, m, need);
+    I = s.sel_I;
+    return;
+  }
+  I = select_tied_indices(s, T, need);
+}
+
+// Puts the indices of the selected entries ({key > T} + {key == T, idx <= I})
+// into s.emit; returns how many.
+__device__ int emit_selected(Smem& s, uint32_t T, int I) {
+  csync();
+  if (threadIdx.x == 0) s.n_emit = 0;
+  csync();
+  const int warp = threadIdx.x >> 5;
+  const int n = s.buf_n;
+  for (int base = warp * 32; base < n; base += kThreads) {
+    const int i = base + static_cast<int>(lane_id());
+    bool sel = false;
+    int32_t x = 0;
+    if (i < n) {
+      const uint32_t k = s.bkey[i];
+      x = s.bidx[i];
+      sel = k > T || (k == T && x <= I);
+    }
+    warp_push<int32_t>(s.emit, &s.n_emit, kMaxTopK, sel, x);
+  }
+  csync();
+  return s.n_emit;
 }
 
 // ------------------------------------------------------------ streaming state
@@ -314,22 +495,27 @@ __device__ void reset_row_state(Smem& s) {
     s.t = 0;
     s.cnt_ge = 0;
     s.thr_lo = 0;
+    s.thr_f = key_floor_value(0u);
     s.n_emit = 0;
-    s.nA = 0;
-    s.nB = 0;
+  }
+}
+
+__device__ __forceinline__ void set_threshold(Smem& s, uint32_t lo) {
+  if (lo > s.thr_lo) {
+    s.thr_lo = lo;
+    s.thr_f = key_floor_value(lo);
   }
 }
 
 // One warp: moves the threshold bin t up as far as the kept counts allow.
 // cnt_ge counts buffered keys with bits 31..20 >= t (all of them are in play);
 // after the move, at least K of them still sit at or above t and fewer than K
-// above it.
+// above it. Raises the filter to the lower edge of bin t.
 __device__ void advance_threshold(Smem& s, int K) {
   const int lane = static_cast<int>(lane_id());
   int cnt = s.cnt_ge + (s.buf_n - s.buf_mark);
   int t = s.t;
   if (cnt >= K) {
-    // fine step over 32 bins
     auto fine = [&]() -> int {
       const int b = t + lane;
       int q = (b < kBins) ? static_cast<int>(s.hist[b]) : 0;
@@ -376,110 +562,91 @@ __device__ void advance_threshold(Smem& s, int K) {
     s.cnt_ge = cnt;
     s.t = t;
     s.buf_mark = s.buf_n;
-    const uint32_t lo = static_cast<uint32_t>(t) << 20;
-    if (lo > s.thr_lo) s.thr_lo = lo;
+    set_threshold(s, static_cast<uint32_t>(t) << 20);
   }
 }
 
-// Drops buffered keys below bin t (they can no longer be selected).
-__device__ void compact_to_bin(Smem& s) {
-  constexpr int kPer = kBufCap / kThreads;
+// Keeps the buffer entries for which keep(key, idx) holds. In place, in rounds
+// of 4 entries per thread: every round reads before it writes, and the write
+// cursor never passes the start of the next round.
+template <class Keep>
+__device__ void compact_buffer(Smem& s, Keep keep) {
+  constexpr int kPer = 4;
+  constexpr int kRound = kPer * kThreads;
   const int tid = threadIdx.x;
+  csync();
   const int n = s.buf_n;
-  const uint32_t tmin = static_cast<uint32_t>(s.t);
-  uint32_t kk[kPer];
-  int32_t ii[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = tid + j * kThreads;
-    kk[j] = 0u;
-    ii[j] = 0;
-    if (e < n) {
-      kk[j] = s.bkey[e];
-      ii[j] = s.bidx[e];
-    }
-  }
-  __syncthreads();
+  csync();
   if (tid == 0) s.buf_n = 0;
-  __syncthreads();
   const uint32_t lt = lanemask_lt();
+  for (int r0 = 0; r0 < n; r0 += kRound) {
+    uint32_t kk[kPer];
+    int32_t ii[kPer];
+    bool kp[kPer];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = tid + j * kThreads;
-    const bool keep = e < n && (kk[j] >> 20) >= tmin;
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, keep);
-    if (m) {
+    for (int j = 0; j < kPer; ++j) {
+      const int e = r0 + j * kThreads + tid;
+      kk[j] = 0u;
+      ii[j] = 0;
+      kp[j] = false;
+      if (e < n) {
+        kk[j] = s.bkey[e];
+        ii[j] = s.bidx[e];
+        kp[j] = keep(kk[j], ii[j]);
+      }
+    }
+    csync();
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, kp[j]);
+      if (m == 0) continue;
       int base = 0;
       if (lane_id() == 0) base = atomicAdd(&s.buf_n, __popc(m));
       base = __shfl_sync(0xFFFFFFFFu, base, 0);
-      if (keep) {
-        const int o = base + __popc(m & lt);
+      if (kp[j]) {
+        const int o = min(base + __popc(m & lt), kBufCap - 1);
         s.bkey[o] = kk[j];
         s.bidx[o] = ii[j];
       }
     }
+    csync();
   }
-  __syncthreads();
+  csync();
   if (tid == 0) s.buf_mark = s.buf_n;
-  __syncthreads();
+  csync();
 }
 
 // Keeps exactly the K best buffered candidates and raises the filter to
 // (K-th key) + 1: a later element equal to that key has a larger index than
 // every kept one, so it can never be selected.
 __device__ void compact_exact(Smem& s, int K) {
-  const int tid = threadIdx.x;
-  const int t = s.t;
-  const int need = K - (s.cnt_ge - static_cast<int>(s.hist[t]));
-  if (tid == 0) {
-    s.n_emit = 0;
-    s.nA = 0;
-    s.min_key = 0xFFFFFFFFu;
-  }
-  __syncthreads();
-  partition_buffer(s, static_cast<uint32_t>(t));
-  __syncthreads();
-  select_exact(s, s.listA, s.listB, s.nA, need, 1);
-  constexpr int kPer = kMaxTopK / kThreads;
-  uint32_t kk[kPer];
-  int32_t ii[kPer];
-  uint32_t mn = 0xFFFFFFFFu;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = tid + j * kThreads;
-    kk[j] = 0u;
-    ii[j] = 0;
-    if (e < K) {
-      const int pos = s.emit[e] & (kBufCap - 1);
-      kk[j] = s.bkey[pos];
-      ii[j] = s.bidx[pos];
-      mn = min(mn, kk[j]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-  if (lane_id() == 0) atomicMin(&s.min_key, mn);
-  for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = tid + j * kThreads;
-    if (e < K) {
-      s.bkey[e] = kk[j];
-      s.bidx[e] = ii[j];
-      atomicAdd(&s.hist[kk[j] >> 20], 1u);
-    }
-  }
-  if (tid == 0) {
-    const uint32_t T = s.min_key;
-    s.buf_n = K;
-    s.buf_mark = K;
-    s.cnt_ge = K;
+  uint32_t T;
+  int I;
+  select_threshold(s, K, T, I);
+  compact_buffer(s, [=](uint32_t k, int32_t i) { return k > T || (k == T && i <= I); });
+  for (int b = threadIdx.x; b < kBins; b += kThreads) s.hist[b] = 0;
+  csync();
+  const int n = s.buf_n;
+  for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&s.hist[s.bkey[i] >> 20], 1u);
+  csync();
+  if (threadIdx.x == 0) {
+    s.buf_mark = n;
+    s.cnt_ge = n;
     s.t = static_cast<int>(T >> 20);
-    s.thr_lo = T + 1u;
-    s.n_emit = 0;
+    set_threshold(s, T + 1u);
   }
-  __syncthreads();
+  csync();
+}
+
+// Frees buffer space: raise the threshold bin, drop what fell below it, and if
+// that is not enough keep exactly the K best.
+__device__ void make_room(Smem& s, int K) {
+  csync();
+  if (threadIdx.x < 32) advance_threshold(s, K);
+  csync();
+  const uint32_t t = static_cast<uint32_t>(s.t);
+  compact_buffer(s, [=](uint32_t k, int32_t) { return (k >> 20) >= t; });
+  if (s.buf_n + kChunk > kBufCap) compact_exact(s, K);
 }
 
 // ----------------------------------------------------------------- row plans
@@ -531,112 +698,123 @@ __device__ __forceinline__ bool get_row(const Params& p, const Smem& s, int64_t 
   return true;
 }
 
-// Copy issuer state, held by thread 0.
-struct Producer {
-  int64_t k;
+// The copy warp's loop (one lane): issues every chunk this CTA will consume,
+// in consumption order, into the ring slot freed by the consumers.
+__device__ void producer_loop(const Params& p, Smem& s, int g, int m) {
+  uint32_t q = 0;
   RowWin w;
-  int j;
-  uint32_t q;  // sequence number of the next chunk to issue
-  bool done;
-};
-
-__device__ void producer_seek(const Params& p, const Smem& s, Producer& P, int g, int m) {
-  while (true) {
-    if (!get_row(p, s, P.k, g, m, P.w)) {
-      P.done = true;
-      return;
+  bool stop = false;
+  for (int64_t k = 0; !stop && get_row(p, s, k, g, m, w); ++k) {
+    for (int j = 0; j < w.nch; ++j, ++q) {
+      const int slot = static_cast<int>(q % kStages);
+      if (q >= kStages &&
+          !mbar_wait_bounded(&s.empty[slot], ((q / kStages) - 1u) & 1u, p.timeout_ns, &s.abort)) {
+        stop = true;
+        break;
+      }
+      const int ws = w.wstart + j * kChunk;
+      const int we = min(ws + kChunk, w.wend);
+      const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
+      fence_proxy_async();
+      mbar_expect_tx(&s.full[slot], bytes);
+      bulk_copy_g2s(s.stage[slot], w.rowp + ws, bytes, &s.full[slot]);
     }
-    if (P.w.nch > 0) {
-      P.j = 0;
-      return;
-    }
-    ++P.k;
   }
-}
-
-__device__ void producer_issue(const Params& p, Smem& s, Producer& P, int g, int m) {
-  if (P.done) return;
-  const int ws = P.w.wstart + P.j * kChunk;
-  const int we = min(ws + kChunk, P.w.wend);
-  const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
-  const int slot = static_cast<int>(P.q % kStages);
-  fence_proxy_async();
-  mbar_expect_tx(&s.full[slot], bytes);
-  bulk_copy_g2s(s.stage[slot], P.w.rowp + ws, bytes, &s.full[slot]);
-  ++P.q;
-  if (++P.j == P.w.nch) {
-    ++P.k;
-    producer_seek(p, s, P, g, m);
-  }
-}
-
-// Waits (bounded) for every copy issued but not consumed, so that none lands
-// after the CTA has left.
-__device__ void drain_copies(Smem& s, const Producer& P, uint32_t consumed, uint64_t timeout_ns) {
-  for (uint32_t q = consumed; q < P.q; ++q)
-    mbar_wait_bounded(&s.full[q % kStages], (q / kStages) & 1u, timeout_ns);
+  // every issued copy must land before the CTA may exit
+  const uint32_t first = q > kStages ? q - kStages : 0u;
+  for (uint32_t i = first; i < q; ++i)
+    mbar_wait_bounded(&s.full[i % kStages], (i / kStages) & 1u, p.timeout_ns, nullptr);
 }
 
 // ------------------------------------------------------------- chunk filter
 
-// Filters one staged chunk: keys at or above the running threshold are kept
-// (appended to the candidate buffer and counted in the histogram).
-__device__ __forceinline__ void filter_chunk(Smem& s, const float* stage, int ws, int nvec, int lo,
-                                             int hi) {
-  const int warp = threadIdx.x >> 5;
+// Filters one chunk of a row window against the running threshold: one fp32
+// compare per element; a warp reserves buffer space once; only survivors are
+// converted to keys, stored and (with kCount) counted in the histogram.
+// src holds the window's elements [ws, ws + 4*nvec) (shared or global memory).
+template <bool kCount, bool kGlobal>
+__device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, int nvec, int lo, int hi) {
+  constexpr int V = kChunk / (4 * kThreads);
+  const int tid = threadIdx.x;
   const int lane = static_cast<int>(lane_id());
-  const uint32_t thr = s.thr_lo;
+  const float thr = s.thr_f;
+  const float4* s4 = reinterpret_cast<const float4*>(src);
   const bool interior = ws >= lo && ws + 4 * nvec <= hi;
-  const float4* st4 = reinterpret_cast<const float4*>(stage);
+  uint32_t m = 0;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int vi = tid + v * kThreads;
+    if (vi < nvec) {
+      const float4 f = kGlobal ? __ldg(s4 + vi) : s4[vi];
+      uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                   (f.w >= thr ? 8u : 0u);
+      if (!interior) {
+        const int i0 = ws + 4 * vi;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i0 + e < lo || i0 + e >= hi) b &= ~(1u << e);
+      }
+      m |= b << (4 * v);
+    }
+  }
+  const int c = __popc(m);
   const uint32_t lt = lanemask_lt();
-  for (int vb = warp * 32; vb < nvec; vb += kThreads) {
-    const int v = vb + lane;
-    const bool in = v < nvec;
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (in) f = st4[v];
-    const int i0 = ws + 4 * v;
-    const uint32_t k0 = fkey(f.x), k1 = fkey(f.y), k2 = fkey(f.z), k3 = fkey(f.w);
-    bool p0 = in && k0 >= thr, p1 = in && k1 >= thr, p2 = in && k2 >= thr, p3 = in && k3 >= thr;
-    if (!interior) {
-      p0 = p0 && i0 >= lo && i0 < hi;
-      p1 = p1 && i0 + 1 >= lo && i0 + 1 < hi;
-      p2 = p2 && i0 + 2 >= lo && i0 + 2 < hi;
-      p3 = p3 && i0 + 3 >= lo && i0 + 3 < hi;
+  const uint32_t q0 = __ballot_sync(0xFFFFFFFFu, c & 1);
+  const uint32_t q1 = __ballot_sync(0xFFFFFFFFu, c & 2);
+  const uint32_t q2 = __ballot_sync(0xFFFFFFFFu, c & 4);
+  const uint32_t q3 = __ballot_sync(0xFFFFFFFFu, c & 8);
+  const int tot = __popc(q0) + 2 * __popc(q1) + 4 * __popc(q2) + 8 * __popc(q3);
+  if (tot == 0) return;
+  int base = 0;
+  if (lane == 0) base = atomicAdd(&s.buf_n, tot);
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  int o = base + __popc(q0 & lt) + 2 * __popc(q1 & lt) + 4 * __popc(q2 & lt) + 8 * __popc(q3 & lt);
+  while (m) {
+    const int j = __ffs(m) - 1;
+    m &= m - 1;
+    const int off = 4 * (tid + (j >> 2) * kThreads) + (j & 3);
+    const uint32_t k = fkey(kGlobal ? __ldg(src + off) : src[off]);
+    const int oo = min(o, kBufCap - 1);
+    s.bkey[oo] = k;
+    s.bidx[oo] = ws + off;
+    if (kCount) atomicAdd(&s.hist[k >> 20], 1u);
+    ++o;
+  }
+}
+
+// Histograms the keys of one staged chunk (elements inside [lo, hi)).
+__device__ __forceinline__ void hist_chunk(Smem& s, const float* src, int ws, int nvec, int lo, int hi) {
+  constexpr int V = kChunk / (4 * kThreads);
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int vi = threadIdx.x + v * kThreads;
+    if (vi < nvec) {
+      const float4 f = s4[vi];
+      const int i0 = ws + 4 * vi;
+      if (i0 >= lo && i0 < hi) atomicAdd(&s.hist[fkey(f.x) >> 20], 1u);
+      if (i0 + 1 >= lo && i0 + 1 < hi) atomicAdd(&s.hist[fkey(f.y) >> 20], 1u);
+      if (i0 + 2 >= lo && i0 + 2 < hi) atomicAdd(&s.hist[fkey(f.z) >> 20], 1u);
+      if (i0 + 3 >= lo && i0 + 3 < hi) atomicAdd(&s.hist[fkey(f.w) >> 20], 1u);
     }
-    const uint32_t m0 = __ballot_sync(0xFFFFFFFFu, p0);
-    const uint32_t m1 = __ballot_sync(0xFFFFFFFFu, p1);
-    const uint32_t m2 = __ballot_sync(0xFFFFFFFFu, p2);
-    const uint32_t m3 = __ballot_sync(0xFFFFFFFFu, p3);
-    const int c0 = __popc(m0), c1 = __popc(m1), c2 = __popc(m2), c3 = __popc(m3);
-    const int tot = c0 + c1 + c2 + c3;
-    if (tot == 0) continue;
-    int base = 0;
-    if (lane == 0) base = atomicAdd(&s.buf_n, tot);
-    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-    if (p0) {
-      const int o = min(base + __popc(m0 & lt), kBufCap - 1);
-      s.bkey[o] = k0;
-      s.bidx[o] = i0;
-      atomicAdd(&s.hist[k0 >> 20], 1u);
-    }
-    if (p1) {
-      const int o = min(base + c0 + __popc(m1 & lt), kBufCap - 1);
-      s.bkey[o] = k1;
-      s.bidx[o] = i0 + 1;
-      atomicAdd(&s.hist[k1 >> 20], 1u);
-    }
-    if (p2) {
-      const int o = min(base + c0 + c1 + __popc(m2 & lt), kBufCap - 1);
-      s.bkey[o] = k2;
-      s.bidx[o] = i0 + 2;
-      atomicAdd(&s.hist[k2 >> 20], 1u);
-    }
-    if (p3) {
-      const int o = min(base + c0 + c1 + c2 + __popc(m3 & lt), kBufCap - 1);
-      s.bkey[o] = k3;
-      s.bidx[o] = i0 + 3;
-      atomicAdd(&s.hist[k3 >> 20], 1u);
-    }
+  }
+}
+
+// Streams the window [lo, hi) of row w straight from global memory with no
+// seed: every element starts eligible and the threshold rises as candidates
+// accumulate. Used only when a seeded pass kept fewer than K elements.
+__device__ void restream_row(Smem& s, const Params& p, const RowWin& w) {
+  csync();
+  reset_row_state(s);
+  csync();
+  for (int j = 0; j < w.nch; ++j) {
+    if (s.buf_n + kChunk > kBufCap) make_room(s, p.topk);
+    const int ws = w.wstart + j * kChunk;
+    const int we = min(ws + kChunk, w.wend);
+    filter_chunk<true, true>(s, w.rowp + ws, ws, (we - ws) >> 2, w.lo, w.hi);
+    csync();
+    if (threadIdx.x < 32) advance_threshold(s, p.topk);
+    csync();
   }
 }
 
@@ -647,31 +825,34 @@ __device__ void write_trivial_row(const Params& p, int64_t r, int len) {
   for (int j = threadIdx.x; j < p.topk; j += kThreads) o[j] = (j < len) ? j : -1;
 }
 
+// After the last chunk: settle the threshold bin and re-stream the window if
+// the seed kept fewer than K elements. Consumer-wide.
+__device__ void close_window(Smem& s, const Params& p, const RowWin& w) {
+  csync();
+  if (threadIdx.x < 32) advance_threshold(s, p.topk);
+  csync();
+  if (s.thr_lo != 0u && s.cnt_ge < p.topk) restream_row(s, p, w);
+}
+
 // G == 1: the CTA holds every candidate of the row.
 __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
   const int K = p.topk;
-  const int t = s.t;
-  const int need = K - (s.cnt_ge - static_cast<int>(s.hist[t]));
-  if (threadIdx.x == 0) {
-    s.n_emit = 0;
-    s.nA = 0;
-  }
-  __syncthreads();
-  partition_buffer(s, static_cast<uint32_t>(t));
-  __syncthreads();
-  select_exact(s, s.listA, s.listB, s.nA, need, 1);
+  uint32_t T;
+  int I;
+  select_threshold(s, K, T, I);
+  const int ne = min(emit_selected(s, T, I), K);
   int32_t* o = p.out + r * static_cast<int64_t>(K);
-  for (int j = threadIdx.x; j < K; j += kThreads) o[j] = s.bidx[s.emit[j] & (kBufCap - 1)];
-  __syncthreads();
+  for (int j = threadIdx.x; j < ne; j += kThreads) o[j] = s.emit[j];
+  csync();
   reset_row_state(s);
-  __syncthreads();
+  csync();
 }
 
 // Group barrier over the workspace: arrive (release), then wait (acquire)
 // until `target` arrivals, at most timeout_ns. Returns false if this CTA must
 // abandon the launch (time-out, or the test-only injected departure).
 __device__ bool group_sync(Smem& s, uint32_t* ctr, uint32_t target, const Params& p, bool skip) {
-  __syncthreads();
+  csync();
   if (threadIdx.x == 0) {
     if (skip) {
       s.abort = 1;
@@ -690,7 +871,7 @@ __device__ bool group_sync(Smem& s, uint32_t* ctr, uint32_t target, const Params
       __threadfence();
     }
   }
-  __syncthreads();
+  csync();
   return s.abort == 0;
 }
 
@@ -709,6 +890,7 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
   first_barrier = false;
 
   // pass A: bits 31..20 of every member's candidates still in play
+  csync();
   for (int b = s.t + tid; b < kBins; b += kThreads) {
     const uint32_t h = s.hist[b];
     if (h) atomicAdd(&gw->h1[b], h);
@@ -716,27 +898,13 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
   epoch += G;
   if (!group_sync(s, &gw->bar_count, epoch, p, skip)) return false;
   for (int b = tid; b < kBins; b += kThreads) s.hist[b] = __ldcg(&gw->h1[b]);
-  if (tid == 0) {
-    s.n_emit = 0;
-    s.nA = 0;
-  }
-  __syncthreads();
-  block_find(s, kBins, K);
+  block_find(s, kBins, K, true);
   const uint32_t T1 = static_cast<uint32_t>(s.find_b);
   const int needA = K - s.find_gt;
-  partition_buffer(s, T1);
-  __syncthreads();
-  const int gtA = s.n_emit;
-  const int nA = s.nA;
+  const int gtA = block_count(s, [=](uint32_t k, int32_t) { return (k >> 20) > T1; });
 
   // pass B: bits 19..8 of the candidates in bin T1
-  for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
-  __syncthreads();
-  for (int i = tid; i < nA; i += kThreads) {
-    const uint16_t pos = s.listA[i];
-    atomicAdd(&s.hist[digit_of(1, s.bkey[pos], 0)], 1u);
-  }
-  __syncthreads();
+  hist_keys(s, kBins, T1, 20, 8, 0xFFFu);
   for (int b = tid; b < kBins; b += kThreads) {
     const uint32_t h = s.hist[b];
     if (h) atomicAdd(&gw->h2[b], h);
@@ -745,24 +913,14 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
   if (!group_sync(s, &gw->bar_count, epoch, p, false)) return false;
   clear_slice(gw->h1, kBins, m, G);  // every member read h1 before arriving here
   for (int b = tid; b < kBins; b += kThreads) s.hist[b] = __ldcg(&gw->h2[b]);
-  if (tid == 0) s.nB = 0;
-  __syncthreads();
-  block_find(s, kBins, needA);
+  block_find(s, kBins, needA, true);
   const uint32_t T2 = static_cast<uint32_t>(s.find_b);
   const int needB = needA - s.find_gt;
-  partition_list(s, s.listA, nA, 1, T2, s.listB, &s.nB);
-  __syncthreads();
-  const int gtB = s.n_emit - gtA;
-  const int nB = s.nB;
+  const uint32_t P2 = (T1 << 12) | T2;
+  const int gtB = block_count(s, [=](uint32_t k, int32_t) { return (k >> 20) == T1 && ((k >> 8) & 0xFFFu) > T2; });
 
   // pass C: bits 7..0, histogram kept per member so ties can be ranked by member
-  for (int b = tid; b < 256; b += kThreads) s.hist[b] = 0;
-  __syncthreads();
-  for (int i = tid; i < nB; i += kThreads) {
-    const uint16_t pos = s.listB[i];
-    atomicAdd(&s.hist[s.bkey[pos] & 0xFFu], 1u);
-  }
-  __syncthreads();
+  hist_keys(s, 256, P2, 8, 0, 0xFFu);
   for (int b = tid; b < 256; b += kThreads) __stcg(&gw->h3[m][b], s.hist[b]);
   if (tid == 0) {
     __stcg(&gw->cnt[m][0], static_cast<uint32_t>(gtA));
@@ -776,10 +934,10 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
     for (int mm = 0; mm < G; ++mm) sum += __ldcg(&gw->h3[mm][b]);
     s.hist[b] = sum;
   }
-  __syncthreads();
-  block_find(s, 256, needB);
+  block_find(s, 256, needB, true);
   const uint32_t T3 = static_cast<uint32_t>(s.find_b) & 0xFFu;
   const int needC = needB - s.find_gt;
+  const uint32_t T = (P2 << 8) | T3;
   if (tid < G) {
     const int mm = tid;
     uint32_t gtc = 0;
@@ -787,7 +945,7 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
     s.g_e[mm] = static_cast<int>(__ldcg(&gw->h3[mm][T3]));
     s.g_tot[mm] = static_cast<int>(__ldcg(&gw->cnt[mm][0]) + __ldcg(&gw->cnt[mm][1]) + gtc);
   }
-  __syncthreads();
+  csync();
   if (tid == 0) {
     // ties at the exact threshold key go to the smaller indices: members hold
     // consecutive index ranges, so the members before this one take theirs first
@@ -801,92 +959,121 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
       off += s.g_tot[mm] + take;
       pre += s.g_e[mm];
     }
-    s.nA = 0;
   }
-  __syncthreads();
-  partition_list(s, s.listB, nB, 2, T3, s.listA, &s.nA);
-  __syncthreads();
-  select_exact(s, s.listA, s.listB, s.nA, s.take, 3);
+  csync();
+  const int take = s.take;
   const int off = s.off;
-  const int ne = min(s.n_emit, kMaxTopK);
+  const int mine = s.g_e[m];
+  int I = -1;
+  if (take >= mine) {
+    I = 0x7FFFFFFF;
+  } else if (take > 0) {
+    if (mine <= kSmallSet) {
+      const int cnt = gather_small(s, [=](uint32_t k, int32_t) { return k == T; });
+      rank_small(s, cnt, take);
+      I = s.sel_I;
+    } else {
+      I = select_tied_indices(s, T, take);
+    }
+  }
+  const int ne = emit_selected(s, T, I);
   int32_t* o = p.out + r * static_cast<int64_t>(K);
   for (int j = tid; j < ne; j += kThreads)
-    if (off + j < K) o[off + j] = s.bidx[s.emit[j] & (kBufCap - 1)];
-  __syncthreads();
+    if (off + j < K) o[off + j] = s.emit[j];
+  csync();
   reset_row_state(s);
-  __syncthreads();
+  csync();
   return true;
 }
 
 // ------------------------------------------------------------------- kernel
 
-__global__ void __launch_bounds__(kThreads, 1) topk_ragged_kernel(const Params p) {
+__global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
   const int g = static_cast<int>(blockIdx.x) / p.G;
   const int m = static_cast<int>(blockIdx.x) % p.G;
 
-  reset_row_state(s);
+  if (tid < kThreads) reset_row_state(s);
   if (tid == 0) {
     s.abort = 0;
-    for (int i = 0; i < kStages; ++i) mbar_init(&s.full[i], 1u);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1u);
+      mbar_init(&s.empty[i], kWarps);
+    }
     fence_mbar_init();
   }
-  for (int k = tid; k < kLenCache; k += kThreads) {
+  for (int k = tid; k < kLenCache; k += kCtaThreads) {
     const int64_t r = g + static_cast<int64_t>(k) * p.num_groups;
     s.lens[k] = (r < p.num_rows) ? clamp_len(p, p.lengths[r]) : 0;
   }
   __syncthreads();
 
-  Producer P;
-  P.k = 0;
-  P.q = 0;
-  P.j = 0;
-  P.done = false;
-  if (tid == 0) {
-    producer_seek(p, s, P, g, m);
-    for (int i = 0; i < kStages; ++i) producer_issue(p, s, P, g, m);
+  if (tid >= kThreads) {
+    if (tid == kThreads) producer_loop(p, s, g, m);
+    return;
   }
 
+  const int K = p.topk;
   uint32_t q = 0;  // chunks consumed
   uint32_t epoch = 0;
   bool first_barrier = true;
   bool aborted = false;
   RowWin w;
   for (int64_t k = 0; !aborted && get_row(p, s, k, g, m, w); ++k) {
-    if (w.len <= p.topk) {
+    if (w.len <= K) {
       if (m == 0) write_trivial_row(p, w.r, w.len);
       continue;
     }
+    const int span = w.hi - w.lo;
     for (int j = 0; j < w.nch; ++j) {
-      if (s.buf_n + kChunk > kBufCap) {
-        compact_to_bin(s);
-        if (s.cnt_ge + kChunk > kBufCap) compact_exact(s, p.topk);
-      }
+      if (s.buf_n + kChunk > kBufCap) make_room(s, K);
       const int slot = static_cast<int>(q % kStages);
-      const bool ok = mbar_wait_bounded(&s.full[slot], (q / kStages) & 1u, p.timeout_ns);
+      const bool ok = mbar_wait_bounded(&s.full[slot], (q / kStages) & 1u, p.timeout_ns, &s.abort);
+      const int ws = w.wstart + j * kChunk;
+      const int we = min(ws + kChunk, w.wend);
+      const int nvec = (we - ws) >> 2;
       if (!ok) {
         s.abort = 1;
         atomicOr(p.status, 0x4u);
+      } else if (j == 0 && span > K) {
+        // seed: histogram the first chunk, aim the threshold at ~1.5 K survivors
+        // over the window (exactly K when the window is this one chunk)
+        hist_chunk(s, s.stage[slot], ws, nvec, w.lo, w.hi);
+        const int in_chunk = min(w.hi, we) - max(w.lo, ws);
+        int target = K;
+        if (w.nch > 1) {
+          const int64_t tt = (3ll * K * in_chunk + 2ll * span - 1) / (2ll * span);
+          target = static_cast<int>(tt < 1 ? 1 : tt);
+        }
+        target = min(target, in_chunk);
+        block_find(s, kBins, target, true);
+        if (tid == 0) {
+          // the histogram now counts every element of this chunk; the ones at or
+          // above bin t are exactly those the filter below appends, which the
+          // next threshold update counts through buf_n - buf_mark
+          s.t = s.find_b;
+          s.cnt_ge = 0;
+          s.buf_mark = 0;
+          set_threshold(s, static_cast<uint32_t>(s.find_b) << 20);
+        }
+        csync();
+        filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
       } else {
-        const int ws = w.wstart + j * kChunk;
-        const int we = min(ws + kChunk, w.wend);
-        filter_chunk(s, s.stage[slot], ws, (we - ws) >> 2, w.lo, w.hi);
+        filter_chunk<true, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
       }
-      __syncthreads();
+      __syncwarp();
+      if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
+      ++q;
+      csync();
       if (s.abort) {
         aborted = true;
         break;
       }
-      if (tid < 32) {
-        advance_threshold(s, p.topk);
-        if (tid == 0) producer_issue(p, s, P, g, m);
-      }
-      ++q;
-      __syncthreads();
     }
     if (aborted) break;
+    close_window(s, p, w);
     if (p.G == 1) {
       finish_local(s, p, w.r);
     } else if (!finish_group(s, p, w.r, g, m, epoch, first_barrier)) {
@@ -895,25 +1082,25 @@ __global__ void __launch_bounds__(kThreads, 1) topk_ragged_kernel(const Params p
   }
 
   if (aborted) {
-    if (tid == 0) drain_copies(s, P, q, p.timeout_ns);
+    s.abort = 1;
     return;
   }
   if (p.G > 1) {
     // last CTA of the group to finish clears the per-member words and counters
     GroupWs* gw = p.groups + g;
-    __syncthreads();
+    csync();
     if (tid == 0) {
       __threadfence();
       const uint32_t old = atom_add_acq_rel_gpu(&gw->exit_count, 1u);
       s.last = (old == static_cast<uint32_t>(p.G - 1)) ? 1 : 0;
     }
-    __syncthreads();
+    csync();
     if (s.last) {
       uint32_t* h3 = &gw->h3[0][0];
       for (int i = tid; i < kMaxGroup * 256; i += kThreads) __stcg(h3 + i, 0u);
       uint32_t* c = &gw->cnt[0][0];
       for (int i = tid; i < kMaxGroup * 4; i += kThreads) __stcg(c + i, 0u);
-      __syncthreads();
+      csync();
       if (tid == 0) {
         __threadfence();
         __stcg(&gw->bar_count, 0u);
@@ -933,14 +1120,14 @@ cudaError_t kernel_configure() {
 }
 
 cudaError_t kernel_occupancy(int* ctas_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, topk_ragged_kernel, kThreads,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, topk_ragged_kernel, kCtaThreads,
                                                        sizeof(Smem));
 }
 
 cudaError_t launch_topk(const Params& p, int grid, bool cooperative, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kCtaThreads);
   cfg.dynamicSmemBytes = sizeof(Smem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
