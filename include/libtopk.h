@@ -142,6 +142,26 @@ int topk_ragged(const float* logits, int64_t row_stride, const int32_t* lengths,
                 int64_t num_rows, int next_n, int topk, int32_t* out_idx,
                 void* workspace, void* stream);
 
+/*
+ * topk_ragged without a workspace argument, for callers that cannot allocate
+ * device memory (they may only enqueue work on the streams and buffers they
+ * are given). The pages describe no such entry point; it has no counterpart
+ * there. Scratch comes from a fixed device array inside the library, about
+ * 3.8 MB per GPU that loads it, held until the process exits; it fits every
+ * plan on a GPU with up to 152 SMs, and a plan needing more row groups returns
+ * TOPK_ERR_WORKSPACE_TOO_SMALL. Arguments, layout and host-side errors are
+ * those of topk_ragged. No allocation is made, ever.
+ *   - The first call on a device looks up the array and zeroes it on `stream`;
+ *     make that first call before any stream capture.
+ *   - All calls on a device share the one array: calls that may overlap on
+ *     the GPU (different streams without ordering) race and must not be made.
+ *   - The device status word is not readable through this entry point; after a
+ *     device-side time-out the shared array is left dirty until the process
+ *     restarts (use topk_ragged with a workspace where that matters).
+ */
+int topk_ragged_static(const float* logits, int64_t row_stride, const int32_t* lengths,
+                       int64_t num_rows, int next_n, int topk, int32_t* out_idx, void* stream);
+
 /* topk_ragged with options (NULL options = topk_ragged). */
 int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths,
                    int64_t num_rows, int next_n, int topk, int32_t* out_idx,

@@ -17,7 +17,7 @@ import threading
 
 __all__ = [
     "TOPK_OK", "TopkError", "TopkOptions", "TopkDeviceProps", "TopkPlan",
-    "topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex",
+    "topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex", "topk_ragged_static",
     "topk_get_status", "topk_status_string", "topk_query_device", "topk_make_plan",
     "library_path", "Selector",
 ]
@@ -41,7 +41,7 @@ TOPK_DEV_LENGTH_CLAMPED = 0x1
 TOPK_DEV_BARRIER_TIMEOUT = 0x2
 TOPK_DEV_STAGE_TIMEOUT = 0x4
 
-EXPORTED = ("topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex",
+EXPORTED = ("topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex", "topk_ragged_static",
             "topk_get_status", "topk_status_string", "topk_query_device", "topk_make_plan")
 
 
@@ -100,6 +100,8 @@ def _load():
         lib.topk_ragged_ex.restype = i32
         lib.topk_ragged_ex.argtypes = [vp, i64, vp, i64, i32, i32, vp, vp, vp,
                                        ctypes.POINTER(TopkOptions)]
+        lib.topk_ragged_static.restype = i32
+        lib.topk_ragged_static.argtypes = [vp, i64, vp, i64, i32, i32, vp, vp]
         lib.topk_get_status.restype = i32
         lib.topk_get_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.topk_status_string.restype = ctypes.c_char_p
@@ -162,6 +164,13 @@ def topk_ragged_ex(logits, row_stride: int, lengths, num_rows: int, next_n: int,
     opt = ctypes.byref(options) if options is not None else None
     return int(_load().topk_ragged_ex(_ptr(logits), row_stride, _ptr(lengths), num_rows, next_n,
                                       topk, _ptr(out_idx), _ptr(workspace), _stream(stream), opt))
+
+
+def topk_ragged_static(logits, row_stride: int, lengths, num_rows: int, next_n: int, topk: int,
+                       out_idx, stream=None) -> int:
+    """topk_ragged for callers that cannot allocate: no workspace argument."""
+    return int(_load().topk_ragged_static(_ptr(logits), row_stride, _ptr(lengths), num_rows, next_n,
+                                          topk, _ptr(out_idx), _stream(stream)))
 
 
 def topk_get_status(workspace, stream=None) -> tuple[int, int]:
