@@ -44,7 +44,11 @@ struct __align__(128) Smem {
   uint32_t bkey[kBufCap];         // candidate keys
   int32_t bidx[kBufCap];          // candidate indices (row-relative)
   int32_t emit[kMaxTopK];         // selected indices of the row being finished
-  int32_t small[kSmallSet];       // candidate positions ranked by one warp
+  int32_t small[kSmallSet];       // candidate positions ranked by rank_small
+  uint32_t rk[kSmallSet];         // their keys, copied for ranking
+  int32_t ri[kSmallSet];          // their indices
+  uint32_t sub[256];              // 8-bit sub-histogram of the threshold bin
+  uint32_t bsum[kBins / 32];      // 32-bin block sums used by block_find
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
   int32_t lens[kLenCache];
@@ -57,6 +61,7 @@ struct __align__(128) Smem {
   float thr_f;
   int find_b, find_gt;
   int abort, last, off, take;
+  int n_list;
   uint32_t red;
   uint32_t sel_T;
   int sel_I;
@@ -190,53 +195,71 @@ __device__ __forceinline__ void warp_push(T* list, int* counter, int cap, bool p
 
 // ----------------------------------------------------------------- radix find
 
-// Over s.hist[0, nb) (nb a power of two, 256..4096): with from_top, finds the
+// Over hist[0, nb) (nb a power of two, 32..4096): with from_top, finds the
 // largest bin b whose suffix sum (bins >= b) reaches `need`; otherwise the
 // smallest bin b whose prefix sum (bins <= b) reaches `need`. Writes b to
 // s.find_b and the count strictly beyond b (above it, or below it) to
-// s.find_gt. Requires need >= 1 and a total of at least need. Consumer-wide;
-// starts and ends with a barrier.
-__device__ void block_find(Smem& s, int nb, int need, bool from_top) {
+// s.find_gt. Requires need >= 1 and a total of at least need.
+// Short dependency chains: every warp sums whole 32-bin blocks with one warp
+// reduction each; one warp then scans the block sums (4 per lane) and the one
+// block holding the crossing. Consumer-wide; starts and ends with a barrier.
+__device__ void block_find(Smem& s, const uint32_t* hist, int nb, int need, bool from_top) {
   const int tid = threadIdx.x;
   const int lane = static_cast<int>(lane_id());
   const int warp = tid >> 5;
-  const int nact = nb < 512 ? nb : 512;
-  const int per = nb / nact;
+  const int nblk = nb >> 5;
   csync();
-  if (tid == 0) {
-    s.find_b = 0;
-    s.find_gt = 0;
+  for (int q = warp; q < nblk; q += kWarps) {
+    const int pos = 32 * q + lane;  // scan position: bin nb-1-pos from the top, bin pos from the bottom
+    const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, hist[from_top ? nb - 1 - pos : pos]);
+    if (lane == 0) s.bsum[q] = sum;
   }
-  // thread tid covers scan positions [tid*per, tid*per + per); position p is
-  // bin nb-1-p when scanning from the top, bin p otherwise
-  uint32_t sum = 0;
-  if (tid < nact)
-    for (int j = 0; j < per; ++j) {
-      const int p = tid * per + j;
-      sum += s.hist[from_top ? nb - 1 - p : p];
-    }
-  uint32_t incl = sum;
+  csync();
+  if (warp == 0) {
+    uint32_t b4[4];
+    uint32_t own = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s.wtot[warp] = incl;
-  csync();
-  for (int w = 0; w < warp; ++w) incl += s.wtot[w];
-  const uint32_t excl = incl - sum;
-  if (tid < nact && incl >= static_cast<uint32_t>(need) && excl < static_cast<uint32_t>(need)) {
-    uint32_t run = excl;
-    for (int j = 0; j < per; ++j) {
-      const int p = tid * per + j;
-      const int b = from_top ? nb - 1 - p : p;
-      const uint32_t h = s.hist[b];
-      if (run + h >= static_cast<uint32_t>(need)) {
-        s.find_b = b;
-        s.find_gt = static_cast<int>(run);
-        break;
+    for (int k = 0; k < 4; ++k) {
+      const int q = 4 * lane + k;
+      b4[k] = (q < nblk) ? s.bsum[q] : 0u;
+      own += b4[k];
+    }
+    uint32_t incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
+    const int L = hit ? __ffs(hit) - 1 : 31;
+    uint32_t run = incl - own;
+    int qsel = 0;
+    if (lane == L) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (run + b4[k] >= static_cast<uint32_t>(need)) {
+          qsel = 4 * lane + k;
+          break;
+        }
+        run += b4[k];
       }
-      run += h;
+    }
+    qsel = __shfl_sync(0xFFFFFFFFu, qsel, L);
+    run = __shfl_sync(0xFFFFFFFFu, run, L);
+    const int pos = 32 * qsel + lane;
+    const int bin = from_top ? nb - 1 - pos : pos;
+    const uint32_t h = hist[bin];
+    uint32_t in2 = h;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, in2, o);
+      if (lane >= o) in2 += v;
+    }
+    const uint32_t hit2 = __ballot_sync(0xFFFFFFFFu, run + in2 >= static_cast<uint32_t>(need));
+    const int L2 = hit2 ? __ffs(hit2) - 1 : 0;
+    if (lane == L2) {
+      s.find_b = bin;
+      s.find_gt = static_cast<int>(run + in2 - h);
     }
   }
   csync();
@@ -345,44 +368,46 @@ __device__ int gather_small(Smem& s, Pred pred) {
   return min(s.n_small, kSmallSet);
 }
 
-// One warp ranks the m <= kSmallSet candidates in s.small by (key desc, index
-// asc) and stores the need-th best one (1 <= need <= m) in s.sel_T / s.sel_I.
-// Consumer-wide; ends with a barrier.
-__device__ void rank_small(Smem& s, int m, int need) {
-  if (threadIdx.x < 32) {
-    const int lane = static_cast<int>(lane_id());
-    uint32_t hk[2], lk[2];
-    int ix[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int e = lane + 32 * h;
-      hk[h] = 0u;
-      lk[h] = 0u;
-      ix[h] = -1;
-      if (e < m) {
-        const int pos = s.small[e];
-        hk[h] = s.bkey[pos];
-        ix[h] = s.bidx[pos];
-        lk[h] = ~static_cast<uint32_t>(ix[h]);
-      }
+// Ranks the m <= kSmallSet candidates listed (as buffer positions) in s.small
+// by (key desc, index asc): thread j < m counts the candidates that beat
+// candidate j, reading four at a time so the loads overlap. The need-th best
+// (1 <= need <= m) goes to s.sel_T / s.sel_I. Returns this thread's rank
+// (kSmallSet for threads without a candidate). Consumer-wide; ends with a barrier.
+__device__ int rank_small(Smem& s, int m, int need) {
+  const int j = threadIdx.x;
+  if (j < kSmallSet) {
+    uint32_t k = 0u;
+    int32_t x = 0x7FFFFFFF;
+    if (j < m) {
+      const int pos = s.small[j];
+      k = s.bkey[pos];
+      x = s.bidx[pos];
     }
-    int rank[2] = {0, 0};
-    for (int j = 0; j < m; ++j) {
-      const int src = j & 31;
-      const uint32_t ohk = __shfl_sync(0xFFFFFFFFu, (j < 32) ? hk[0] : hk[1], src);
-      const uint32_t olk = __shfl_sync(0xFFFFFFFFu, (j < 32) ? lk[0] : lk[1], src);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) rank[h] += (ohk > hk[h] || (ohk == hk[h] && olk > lk[h])) ? 1 : 0;
+    s.rk[j] = k;  // padding entries (key 0, largest index) never beat a real candidate
+    s.ri[j] = x;
+  }
+  csync();
+  int rank = kSmallSet;
+  if (j < m) {
+    const uint32_t kj = s.rk[j];
+    const int32_t ij = s.ri[j];
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    for (int i0 = 0; i0 < m; i0 += 4) {
+      const uint4 k4 = *reinterpret_cast<const uint4*>(&s.rk[i0]);
+      const int4 x4 = *reinterpret_cast<const int4*>(&s.ri[i0]);
+      r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
+      r1 += (k4.y > kj || (k4.y == kj && x4.y < ij)) ? 1 : 0;
+      r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
+      r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
     }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (lane + 32 * h < m && rank[h] == need - 1) {
-        s.sel_T = hk[h];
-        s.sel_I = ix[h];
-      }
+    rank = r0 + r1 + r2 + r3;
+    if (rank == need - 1) {
+      s.sel_T = kj;
+      s.sel_I = ij;
     }
   }
   csync();
+  return rank;
 }
 
 // Among entries with key == T, the need-th smallest index (1 <= need <= count).
@@ -396,7 +421,7 @@ __device__ int select_tied_indices(Smem& s, uint32_t T, int need) {
     const int shift = (l == 0) ? 20 : (l == 1) ? 10 : 0;
     const int nb = 1 << bits;
     hist_tied_indices(s, nb, T, prefix, pshift, shift, static_cast<uint32_t>(nb - 1));
-    block_find(s, nb, need, false);
+    block_find(s, s.hist, nb, need, false);
     const uint32_t b = static_cast<uint32_t>(s.find_b);
     need -= s.find_gt;
     const int c = static_cast<int>(s.hist[b]);
@@ -429,7 +454,7 @@ __device__ void select_threshold(Smem& s, int K, uint32_t& T, int& I) {
     return;
   }
   hist_keys(s, kBins, t, 20, 8, 0xFFFu);
-  block_find(s, kBins, need, true);
+  block_find(s, s.hist, kBins, need, true);
   const uint32_t b1 = static_cast<uint32_t>(s.find_b);
   need -= s.find_gt;
   const int c1 = static_cast<int>(s.hist[b1]);
@@ -446,7 +471,7 @@ __device__ void select_threshold(Smem& s, int K, uint32_t& T, int& I) {
     return;
   }
   hist_keys(s, 256, p1, 8, 0, 0xFFu);
-  block_find(s, 256, need, true);
+  block_find(s, s.hist, 256, need, true);
   const uint32_t b2 = static_cast<uint32_t>(s.find_b);
   need -= s.find_gt;
   const int c2 = static_cast<int>(s.hist[b2]);
@@ -834,15 +859,137 @@ __device__ void close_window(Smem& s, const Params& p, const RowWin& w) {
   if (s.thr_lo != 0u && s.cnt_ge < p.topk) restream_row(s, p, w);
 }
 
-// G == 1: the CTA holds every candidate of the row.
+// G == 1: the CTA holds every candidate of the row. One pass over the buffer
+// writes the sure winners (keys above the threshold bin t) to the output,
+// lists the entries of bin t and histograms their key bits 19..12; a 256-bin
+// find picks the sub-bin holding the K-th key, a pass over the short list
+// writes the sub-bins above it, and the few entries of that sub-bin are ranked
+// directly. Output slots come from one shared atomic per warp.
 __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
+  constexpr int kIt = kBufCap / kThreads;
+  constexpr int kListIt = (kMaxTopK + kThreads - 1) / kThreads;
   const int K = p.topk;
-  uint32_t T;
-  int I;
-  select_threshold(s, K, T, I);
-  const int ne = min(emit_selected(s, T, I), K);
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const uint32_t lt = lanemask_lt();
   int32_t* o = p.out + r * static_cast<int64_t>(K);
-  for (int j = threadIdx.x; j < ne; j += kThreads) o[j] = s.emit[j];
+  csync();
+  const uint32_t t = static_cast<uint32_t>(s.t);
+  const int inbin = static_cast<int>(s.hist[t]);
+  const int need = K - (s.cnt_ge - inbin);
+  const int n = s.buf_n;
+  bool done = false;
+  if (inbin <= kMaxTopK) {
+    for (int b = tid; b < 256; b += kThreads) s.sub[b] = 0;
+    if (tid == 0) {
+      s.n_emit = 0;
+      s.n_list = 0;
+    }
+    csync();
+    // pass 1 over the buffer
+    const int jmax = (n + kThreads - 1) / kThreads;
+    uint32_t bw[kIt], bc[kIt];
+    int tw = 0, tc = 0;
+#pragma unroll
+    for (int j = 0; j < kIt; ++j) {
+      bw[j] = 0u;
+      bc[j] = 0u;
+      if (j < jmax) {
+        const int i = tid + j * kThreads;
+        const uint32_t k = (i < n) ? s.bkey[i] : 0u;
+        const uint32_t d = k >> 20;
+        const bool cand = i < n && d == t;
+        bw[j] = __ballot_sync(0xFFFFFFFFu, i < n && d > t);
+        bc[j] = __ballot_sync(0xFFFFFFFFu, cand);
+        if (cand) atomicAdd(&s.sub[(k >> 12) & 0xFFu], 1u);
+        tw += __popc(bw[j]);
+        tc += __popc(bc[j]);
+      }
+    }
+    int ow = 0, oc = 0;
+    if (lane == 0) {
+      if (tw) ow = atomicAdd(&s.n_emit, tw);
+      if (tc) oc = atomicAdd(&s.n_list, tc);
+    }
+    ow = __shfl_sync(0xFFFFFFFFu, ow, 0);
+    oc = __shfl_sync(0xFFFFFFFFu, oc, 0);
+#pragma unroll
+    for (int j = 0; j < kIt; ++j) {
+      if (j < jmax) {
+        const int i = tid + j * kThreads;
+        if ((bw[j] >> lane) & 1u) {
+          const int q = ow + __popc(bw[j] & lt);
+          if (q < K) o[q] = s.bidx[i];
+        }
+        if ((bc[j] >> lane) & 1u) s.emit[min(oc + __popc(bc[j] & lt), kMaxTopK - 1)] = i;
+        ow += __popc(bw[j]);
+        oc += __popc(bc[j]);
+      }
+    }
+    csync();
+    const int nL = min(s.n_list, kMaxTopK);
+    if (need >= nL) {
+      const int base = s.n_emit;
+      for (int j = tid; j < nL; j += kThreads)
+        if (base + j < K) o[base + j] = s.bidx[s.emit[j]];
+      done = true;
+    } else {
+      block_find(s, s.sub, 256, need, true);
+      const uint32_t b1 = static_cast<uint32_t>(s.find_b);
+      const int need1 = need - s.find_gt;
+      const int c1 = static_cast<int>(s.sub[b1]);
+      if (c1 <= kSmallSet) {
+        // list pass: sub-bins above b1 are winners, sub-bin b1 goes to s.small
+        if (tid == 0) s.n_small = 0;
+        csync();
+        uint32_t lw[kListIt], lk[kListIt];
+        int pw = 0, pk = 0;
+        int pos[kListIt];
+#pragma unroll
+        for (int j = 0; j < kListIt; ++j) {
+          const int e = tid + j * kThreads;
+          pos[j] = (e < nL) ? s.emit[e] : 0;
+          const uint32_t dg = (e < nL) ? ((s.bkey[pos[j]] >> 12) & 0xFFu) : 0u;
+          lw[j] = __ballot_sync(0xFFFFFFFFu, e < nL && dg > b1);
+          lk[j] = __ballot_sync(0xFFFFFFFFu, e < nL && dg == b1);
+          pw += __popc(lw[j]);
+          pk += __popc(lk[j]);
+        }
+        int qw = 0, qk = 0;
+        if (lane == 0) {
+          if (pw) qw = atomicAdd(&s.n_emit, pw);
+          if (pk) qk = atomicAdd(&s.n_small, pk);
+        }
+        qw = __shfl_sync(0xFFFFFFFFu, qw, 0);
+        qk = __shfl_sync(0xFFFFFFFFu, qk, 0);
+#pragma unroll
+        for (int j = 0; j < kListIt; ++j) {
+          if ((lw[j] >> lane) & 1u) {
+            const int q = qw + __popc(lw[j] & lt);
+            if (q < K) o[q] = s.bidx[pos[j]];
+          }
+          if ((lk[j] >> lane) & 1u) s.small[min(qk + __popc(lk[j] & lt), kSmallSet - 1)] = pos[j];
+          qw += __popc(lw[j]);
+          qk += __popc(lk[j]);
+        }
+        csync();
+        const int base = s.n_emit;
+        const int m = min(s.n_small, kSmallSet);
+        const int rank = rank_small(s, m, need1);
+        if (rank < need1 && base + rank < K) o[base + rank] = s.ri[tid];
+        done = true;
+      }
+    }
+  }
+  if (!done) {
+    // crowded threshold bin (heavy ties): radix select over the whole buffer;
+    // rewrites the full output row
+    uint32_t T;
+    int I;
+    select_threshold(s, K, T, I);
+    const int ne = min(emit_selected(s, T, I), K);
+    for (int j = tid; j < ne; j += kThreads) o[j] = s.emit[j];
+  }
   csync();
   reset_row_state(s);
   csync();
@@ -898,7 +1045,7 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
   epoch += G;
   if (!group_sync(s, &gw->bar_count, epoch, p, skip)) return false;
   for (int b = tid; b < kBins; b += kThreads) s.hist[b] = __ldcg(&gw->h1[b]);
-  block_find(s, kBins, K, true);
+  block_find(s, s.hist, kBins, K, true);
   const uint32_t T1 = static_cast<uint32_t>(s.find_b);
   const int needA = K - s.find_gt;
   const int gtA = block_count(s, [=](uint32_t k, int32_t) { return (k >> 20) > T1; });
@@ -913,7 +1060,7 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
   if (!group_sync(s, &gw->bar_count, epoch, p, false)) return false;
   clear_slice(gw->h1, kBins, m, G);  // every member read h1 before arriving here
   for (int b = tid; b < kBins; b += kThreads) s.hist[b] = __ldcg(&gw->h2[b]);
-  block_find(s, kBins, needA, true);
+  block_find(s, s.hist, kBins, needA, true);
   const uint32_t T2 = static_cast<uint32_t>(s.find_b);
   const int needB = needA - s.find_gt;
   const uint32_t P2 = (T1 << 12) | T2;
@@ -934,7 +1081,7 @@ __device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, 
     for (int mm = 0; mm < G; ++mm) sum += __ldcg(&gw->h3[mm][b]);
     s.hist[b] = sum;
   }
-  block_find(s, 256, needB, true);
+  block_find(s, s.hist, 256, needB, true);
   const uint32_t T3 = static_cast<uint32_t>(s.find_b) & 0xFFu;
   const int needC = needB - s.find_gt;
   const uint32_t T = (P2 << 8) | T3;
@@ -1048,7 +1195,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
           target = static_cast<int>(tt < 1 ? 1 : tt);
         }
         target = min(target, in_chunk);
-        block_find(s, kBins, target, true);
+        block_find(s, s.hist, kBins, target, true);
         if (tid == 0) {
           // the histogram now counts every element of this chunk; the ones at or
           // above bin t are exactly those the filter below appends, which the
