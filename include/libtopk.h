@@ -119,8 +119,9 @@ int topk_workspace_init(void* workspace, size_t bytes, void* stream);
 /*
  * Ragged per-row top-K.
  *   logits     fp32 [num_rows, row_stride], row-major, 4-byte aligned; row r
- *              starts at logits + r * row_stride. Only x[r, 0:len_r] is used
- *              (at most 12 bytes of a row's padding may be read, never used).
+ *              starts at logits + r * row_stride; the buffer holds all
+ *              num_rows * row_stride elements. Only x[r, 0:len_r] is used;
+ *              elements of a row past len_r may be read, never used.
  *   row_stride elements between row starts, >= 1; also the upper bound of
  *              every length (it plays the role of max_seq_len).
  *   lengths    int32 [num_rows] (or [num_rows / next_n, next_n] flattened):

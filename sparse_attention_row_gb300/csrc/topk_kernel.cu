@@ -695,7 +695,8 @@ __device__ __forceinline__ int row_len(const Params& p, const Smem& s, int64_t k
   return clamp_len(p, __ldg(p.lengths + r));
 }
 
-// Part of row k (of this CTA's group) that this CTA streams, and its copy windows.
+// Part of row k (of this CTA's group) that this CTA streams, and its copy
+// windows.
 __device__ __forceinline__ bool get_row(const Params& p, const Smem& s, int64_t k, int g, int m,
                                         RowWin& w) {
   w.r = g + k * p.num_groups;
@@ -723,14 +724,37 @@ __device__ __forceinline__ bool get_row(const Params& p, const Smem& s, int64_t 
   return true;
 }
 
+// With whole rows per CTA, the copy warp issues the first chunk of the CTA's
+// first row before the row lengths are known: the copy window is sized by the
+// row stride, which covers the first chunk of any length. It becomes that
+// row's chunk 0, or a chunk the consumers discard if the row needs no streaming.
+__device__ __noinline__ void producer_first(const Params& p, Smem& s, int g) {
+  const float* rowp = p.logits + static_cast<int64_t>(g) * p.stride;
+  const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
+  const int64_t ws = -mis;
+  const int64_t wend = ws + ((p.stride - ws + 3) & ~static_cast<int64_t>(3));
+  const int64_t we = min(ws + kChunk, wend);
+  const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
+  fence_proxy_async();
+  mbar_expect_tx(&s.full[0], bytes);
+  bulk_copy_g2s(s.stage[0], rowp + ws, bytes, &s.full[0]);
+}
+
 // The copy warp's loop (one lane): issues every chunk this CTA will consume,
-// in consumption order, into the ring slot freed by the consumers.
-__device__ void producer_loop(const Params& p, Smem& s, int g, int m) {
-  uint32_t q = 0;
+// in consumption order, into the ring slot freed by the consumers. With whole
+// rows per CTA, chunk 0 of the first row was issued by producer_first.
+__device__ __noinline__ void producer_loop(const Params& p, Smem& s, int g, int m) {
+  const bool spec = (p.G == 1);
+  uint32_t q = spec ? 1u : 0u;
   RowWin w;
   bool stop = false;
   for (int64_t k = 0; !stop && get_row(p, s, k, g, m, w); ++k) {
-    for (int j = 0; j < w.nch; ++j, ++q) {
+    int j0 = 0;
+    if (k == 0 && spec) {
+      if (w.nch == 0) continue;  // the early chunk is discarded by the consumers
+      j0 = 1;
+    }
+    for (int j = j0; j < w.nch; ++j, ++q) {
       const int slot = static_cast<int>(q % kStages);
       if (q >= kStages &&
           !mbar_wait_bounded(&s.empty[slot], ((q / kStages) - 1u) & 1u, p.timeout_ns, &s.abort)) {
@@ -793,7 +817,31 @@ __device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, 
   int base = 0;
   if (lane == 0) base = atomicAdd(&s.buf_n, tot);
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
-  int o = base + __popc(q0 & lt) + 2 * __popc(q1 & lt) + 4 * __popc(q2 & lt) + 8 * __popc(q3 & lt);
+  int o = __popc(q0 & lt) + 2 * __popc(q1 & lt) + 4 * __popc(q2 & lt) + 8 * __popc(q3 & lt);
+  constexpr int kStaged = (2 * kMaxTopK) / kWarps;  // 16-bit slots per warp in s.emit
+  if (tot <= kStaged) {
+    // each lane only notes where its survivors are (a short divergent loop);
+    // the whole warp then converts and stores them, 32 at a time. s.emit is
+    // idle while a row streams, so it holds the per-warp lists.
+    uint16_t* stg = reinterpret_cast<uint16_t*>(s.emit) + (tid >> 5) * kStaged;
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      stg[o++] = static_cast<uint16_t>(4 * (tid + (j >> 2) * kThreads) + (j & 3));
+    }
+    __syncwarp();
+    for (int e = lane; e < tot; e += 32) {
+      const int off = stg[e];
+      const uint32_t k = fkey(kGlobal ? __ldg(src + off) : src[off]);
+      const int oo = min(base + e, kBufCap - 1);
+      s.bkey[oo] = k;
+      s.bidx[oo] = ws + off;
+      if (kCount) atomicAdd(&s.hist[k >> 20], 1u);
+    }
+    __syncwarp();
+    return;
+  }
+  o += base;
   while (m) {
     const int j = __ffs(m) - 1;
     m &= m - 1;
@@ -1142,7 +1190,6 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
   const int g = static_cast<int>(blockIdx.x) / p.G;
   const int m = static_cast<int>(blockIdx.x) % p.G;
 
-  if (tid < kThreads) reset_row_state(s);
   if (tid == 0) {
     s.abort = 0;
     for (int i = 0; i < kStages; ++i) {
@@ -1151,12 +1198,16 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
     }
     fence_mbar_init();
   }
-  for (int k = tid; k < kLenCache; k += kCtaThreads) {
-    const int64_t r = g + static_cast<int64_t>(k) * p.num_groups;
-    s.lens[k] = (r < p.num_rows) ? clamp_len(p, p.lengths[r]) : 0;
+  __syncthreads();
+  if (tid == kThreads && p.G == 1) producer_first(p, s, g);
+  if (tid < kThreads) {
+    reset_row_state(s);
+    for (int k = tid; k < kLenCache; k += kThreads) {
+      const int64_t r = g + static_cast<int64_t>(k) * p.num_groups;
+      s.lens[k] = (r < p.num_rows) ? clamp_len(p, p.lengths[r]) : 0;
+    }
   }
   __syncthreads();
-
   if (tid >= kThreads) {
     if (tid == kThreads) producer_loop(p, s, g, m);
     return;
@@ -1171,6 +1222,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
   for (int64_t k = 0; !aborted && get_row(p, s, k, g, m, w); ++k) {
     if (w.len <= K) {
       if (m == 0) write_trivial_row(p, w.r, w.len);
+      if (p.G == 1 && k == 0) {
+        // discard the early copy the copy warp issued for this row
+        if (!mbar_wait_bounded(&s.full[0], 0u, p.timeout_ns, &s.abort)) atomicOr(p.status, 0x4u);
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&s.empty[0]);
+        q = 1;
+      }
       continue;
     }
     const int span = w.hi - w.lo;
