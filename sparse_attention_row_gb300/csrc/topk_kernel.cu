@@ -30,6 +30,13 @@
 // Keys: an fp32 value x maps to a uint32 whose unsigned order is the order of
 // the values: -0.0 is first mapped to +0.0, then positive values get the sign
 // bit set and negative values are bit-inverted.
+//
+// Code size: a decode-sized launch runs every phase once per SM, right after
+// other kernels have evicted this one's code from L2, so each instruction line
+// it executes is a cold fetch (ncu shows "no instruction" as the second stall
+// reason there). Phases run once per row (radix finds, ranking) and the rare
+// paths (buffer shrinking, re-streaming, the group merge, the radix fallback)
+// are therefore out of line, and the row finish uses short rolled loops.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -203,7 +210,7 @@ __device__ __forceinline__ void warp_push(T* list, int* counter, int cap, bool p
 // Short dependency chains: every warp sums whole 32-bin blocks with one warp
 // reduction each; one warp then scans the block sums (4 per lane) and the one
 // block holding the crossing. Consumer-wide; starts and ends with a barrier.
-__device__ void block_find(Smem& s, const uint32_t* hist, int nb, int need, bool from_top) {
+__device__ __noinline__ void block_find(Smem& s, const uint32_t* hist, int nb, int need, bool from_top) {
   const int tid = threadIdx.x;
   const int lane = static_cast<int>(lane_id());
   const int warp = tid >> 5;
@@ -373,7 +380,7 @@ __device__ int gather_small(Smem& s, Pred pred) {
 // candidate j, reading four at a time so the loads overlap. The need-th best
 // (1 <= need <= m) goes to s.sel_T / s.sel_I. Returns this thread's rank
 // (kSmallSet for threads without a candidate). Consumer-wide; ends with a barrier.
-__device__ int rank_small(Smem& s, int m, int need) {
+__device__ __noinline__ int rank_small(Smem& s, int m, int need) {
   const int j = threadIdx.x;
   if (j < kSmallSet) {
     uint32_t k = 0u;
@@ -436,7 +443,7 @@ __device__ int select_tied_indices(Smem& s, uint32_t T, int need) {
 // composite threshold: the set {key > T} + {key == T and idx <= I}. Small
 // candidate sets are ranked by one warp, larger ones go through radix levels.
 // Uses hist as scratch.
-__device__ void select_threshold(Smem& s, int K, uint32_t& T, int& I) {
+__device__ __noinline__ void select_threshold(Smem& s, int K, uint32_t& T, int& I) {
   csync();
   const uint32_t t = static_cast<uint32_t>(s.t);
   const int inbin = static_cast<int>(s.hist[t]);
@@ -489,7 +496,7 @@ __device__ void select_threshold(Smem& s, int K, uint32_t& T, int& I) {
 
 // Puts the indices of the selected entries ({key > T} + {key == T, idx <= I})
 // into s.emit; returns how many.
-__device__ int emit_selected(Smem& s, uint32_t T, int I) {
+__device__ __noinline__ int emit_selected(Smem& s, uint32_t T, int I) {
   csync();
   if (threadIdx.x == 0) s.n_emit = 0;
   csync();
@@ -644,7 +651,7 @@ __device__ void compact_buffer(Smem& s, Keep keep) {
 // Keeps exactly the K best buffered candidates and raises the filter to
 // (K-th key) + 1: a later element equal to that key has a larger index than
 // every kept one, so it can never be selected.
-__device__ void compact_exact(Smem& s, int K) {
+__device__ __noinline__ void compact_exact(Smem& s, int K) {
   uint32_t T;
   int I;
   select_threshold(s, K, T, I);
@@ -665,7 +672,7 @@ __device__ void compact_exact(Smem& s, int K) {
 
 // Frees buffer space: raise the threshold bin, drop what fell below it, and if
 // that is not enough keep exactly the K best.
-__device__ void make_room(Smem& s, int K) {
+__device__ __noinline__ void make_room(Smem& s, int K) {
   csync();
   if (threadIdx.x < 32) advance_threshold(s, K);
   csync();
@@ -876,7 +883,7 @@ __device__ __forceinline__ void hist_chunk(Smem& s, const float* src, int ws, in
 // Streams the window [lo, hi) of row w straight from global memory with no
 // seed: every element starts eligible and the threshold rises as candidates
 // accumulate. Used only when a seeded pass kept fewer than K elements.
-__device__ void restream_row(Smem& s, const Params& p, const RowWin& w) {
+__device__ __noinline__ void restream_row(Smem& s, const Params& p, const RowWin w) {
   csync();
   reset_row_state(s);
   csync();
@@ -914,7 +921,6 @@ __device__ void close_window(Smem& s, const Params& p, const RowWin& w) {
 // writes the sub-bins above it, and the few entries of that sub-bin are ranked
 // directly. Output slots come from one shared atomic per warp.
 __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
-  constexpr int kIt = kBufCap / kThreads;
   constexpr int kListIt = (kMaxTopK + kThreads - 1) / kThreads;
   const int K = p.topk;
   const int tid = threadIdx.x;
@@ -934,26 +940,21 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
       s.n_list = 0;
     }
     csync();
-    // pass 1 over the buffer
-    const int jmax = (n + kThreads - 1) / kThreads;
-    uint32_t bw[kIt], bc[kIt];
+    // pass 1 over the buffer, in two short loops (counts, then writes) so the
+    // code stays small: one reservation per warp for winners and for the list
     int tw = 0, tc = 0;
-#pragma unroll
-    for (int j = 0; j < kIt; ++j) {
-      bw[j] = 0u;
-      bc[j] = 0u;
-      if (j < jmax) {
-        const int i = tid + j * kThreads;
-        const uint32_t k = (i < n) ? s.bkey[i] : 0u;
-        const uint32_t d = k >> 20;
-        const bool cand = i < n && d == t;
-        bw[j] = __ballot_sync(0xFFFFFFFFu, i < n && d > t);
-        bc[j] = __ballot_sync(0xFFFFFFFFu, cand);
-        if (cand) atomicAdd(&s.sub[(k >> 12) & 0xFFu], 1u);
-        tw += __popc(bw[j]);
-        tc += __popc(bc[j]);
+#pragma unroll 1
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t k = s.bkey[i];
+      const uint32_t d = k >> 20;
+      tw += (d > t) ? 1 : 0;
+      if (d == t) {
+        ++tc;
+        atomicAdd(&s.sub[(k >> 12) & 0xFFu], 1u);
       }
     }
+    tw = __reduce_add_sync(0xFFFFFFFFu, tw);
+    tc = __reduce_add_sync(0xFFFFFFFFu, tc);
     int ow = 0, oc = 0;
     if (lane == 0) {
       if (tw) ow = atomicAdd(&s.n_emit, tw);
@@ -961,18 +962,20 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
     }
     ow = __shfl_sync(0xFFFFFFFFu, ow, 0);
     oc = __shfl_sync(0xFFFFFFFFu, oc, 0);
-#pragma unroll
-    for (int j = 0; j < kIt; ++j) {
-      if (j < jmax) {
-        const int i = tid + j * kThreads;
-        if ((bw[j] >> lane) & 1u) {
-          const int q = ow + __popc(bw[j] & lt);
-          if (q < K) o[q] = s.bidx[i];
-        }
-        if ((bc[j] >> lane) & 1u) s.emit[min(oc + __popc(bc[j] & lt), kMaxTopK - 1)] = i;
-        ow += __popc(bw[j]);
-        oc += __popc(bc[j]);
+    const int jmax = (n + kThreads - 1) / kThreads;  // the same trips for the whole warp
+#pragma unroll 1
+    for (int j = 0; j < jmax; ++j) {
+      const int i = tid + j * kThreads;
+      const uint32_t d = (i < n) ? (s.bkey[i] >> 20) : 0u;
+      const uint32_t bw = __ballot_sync(0xFFFFFFFFu, i < n && d > t);
+      const uint32_t bc = __ballot_sync(0xFFFFFFFFu, i < n && d == t);
+      if ((bw >> lane) & 1u) {
+        const int q = ow + __popc(bw & lt);
+        if (q < K) o[q] = s.bidx[i];
       }
+      if ((bc >> lane) & 1u) s.emit[min(oc + __popc(bc & lt), kMaxTopK - 1)] = i;
+      ow += __popc(bw);
+      oc += __popc(bc);
     }
     csync();
     const int nL = min(s.n_list, kMaxTopK);
@@ -1075,7 +1078,7 @@ __device__ __forceinline__ void clear_slice(uint32_t* a, int n, int m, int G) {
 }
 
 // G > 1: three radix passes whose histograms are merged across the group.
-__device__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, uint32_t& epoch,
+__device__ __noinline__ bool finish_group(Smem& s, const Params& p, int64_t r, int g, int m, uint32_t& epoch,
                              bool& first_barrier) {
   const int tid = threadIdx.x;
   const int K = p.topk;
