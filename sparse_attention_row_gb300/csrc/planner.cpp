@@ -12,7 +12,13 @@
 // Shape rules:
 //   - one CTA owns whole rows (G = 1) unless the rows are long (row_stride
 //     above the long-row threshold) and too few to fill the GPU; then G CTAs
-//     split each row, G = min(16, capacity / num_rows, row_stride / 8192);
+//     may split each row, G = min(16, capacity / num_rows, row_stride / 8192);
+//   - a split is kept only if it takes at least kSplitGain elements off the
+//     longest share a CTA streams (row_stride * (G - 1) / G >= kSplitGain).
+//     Measured on a GB300: a CTA filters about 6144 elements per 1.1 us, and
+//     merging a row across a group costs about 16 us more than finishing it in
+//     one CTA, so smaller savings lose (64 rows of 163840 run faster whole,
+//     16 rows of 131072 faster split nine ways);
 //   - G = 1 launches min(num_rows, capacity) persistent CTAs, no waiting;
 //   - G > 1 launches num_groups = min(capacity / G, num_rows, num_sms) groups,
 //     so grid = num_groups * G <= num_sms * ctas_per_sm always.
@@ -53,7 +59,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     G = cap / num_rows;
     G = std::min<int64_t>(G, ltk::kMaxGroup);
     G = std::min<int64_t>(G, std::max<int64_t>(1, row_stride / ltk::kMinSpan));
-    if (G < 2) G = 1;
+    if (G < 2 || row_stride * (G - 1) / G < ltk::kSplitGain) G = 1;
   }
   plan->ctas_per_group = static_cast<int>(G);
   if (num_rows == 0) {

@@ -20,6 +20,7 @@ constexpr int kLenCache = 64;          // row lengths cached in shared memory
 constexpr int kSmallSet = 64;          // candidate sets up to this size are ranked by one warp
 constexpr int kMinSpan = 8192;         // fewest elements per CTA when a row is split
 constexpr int64_t kDefaultLongRowThreshold = 32768;
+constexpr int64_t kSplitGain = 90000;  // elements a row split must save per CTA (measured)
 constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 static_assert(kMaxTopK + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");

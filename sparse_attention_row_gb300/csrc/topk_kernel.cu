@@ -52,9 +52,9 @@ struct __align__(128) Smem {
   int32_t bidx[kBufCap];          // candidate indices (row-relative)
   int32_t emit[kMaxTopK];         // selected indices of the row being finished
   int32_t small[kSmallSet];       // candidate positions ranked by rank_small
-  uint32_t rk[kSmallSet];         // their keys, copied for ranking
-  int32_t ri[kSmallSet];          // their indices
-  uint32_t sub[256];              // 8-bit sub-histogram of the threshold bin
+  alignas(16) uint32_t rk[kSmallSet];  // their keys, copied for ranking
+  alignas(16) int32_t ri[kSmallSet];   // their indices
+  alignas(16) uint32_t sub[256];  // 8-bit sub-histogram of the threshold bin
   uint32_t bsum[kBins / 32];      // 32-bin block sums used by block_find
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
@@ -905,21 +905,83 @@ __device__ void write_trivial_row(const Params& p, int64_t r, int len) {
   for (int j = threadIdx.x; j < p.topk; j += kThreads) o[j] = (j < len) ? j : -1;
 }
 
+// Clears what the row finish accumulates into (the sub-histogram, the list
+// counters) and pads the ranking slots; thread u of `nthreads` takes its share.
+__device__ __forceinline__ void prepare_finish(Smem& s, int u, int nthreads) {
+  for (int b = u; b < 256; b += nthreads) s.sub[b] = 0;
+  if (u < kSmallSet) {
+    s.rk[u] = 0u;  // padding never beats a real candidate
+    s.ri[u] = 0x7FFFFFFF;
+  }
+  if (u == 0) {
+    s.n_emit = 0;
+    s.n_list = 0;
+    s.n_small = 0;
+  }
+}
+
 // After the last chunk: settle the threshold bin and re-stream the window if
-// the seed kept fewer than K elements. Consumer-wide.
+// the seed kept fewer than K elements. While warp 0 moves the threshold, the
+// other warps prepare the finish. Consumer-wide; ends with a barrier.
 __device__ void close_window(Smem& s, const Params& p, const RowWin& w) {
   csync();
-  if (threadIdx.x < 32) advance_threshold(s, p.topk);
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    advance_threshold(s, p.topk);
+  } else {
+    prepare_finish(s, tid - 32, kThreads - 32);
+  }
   csync();
-  if (s.thr_lo != 0u && s.cnt_ge < p.topk) restream_row(s, p, w);
+  if (s.thr_lo != 0u && s.cnt_ge < p.topk) {
+    restream_row(s, p, w);  // may use the ranking slots; prepare again
+    prepare_finish(s, tid, kThreads);
+    csync();
+  }
+}
+
+// One warp, over h[0, 256): the largest bin b whose suffix sum (bins >= b)
+// reaches need (1 <= need <= total). Lane l sums bins 255-8l down to 248-8l;
+// a scan over the lanes finds the lane holding the crossing, which walks its
+// eight bins. Writes b to s.find_b and the count above b to s.find_gt.
+__device__ __forceinline__ void warp_find_top256(Smem& s, const uint32_t* h, int need) {
+  const int lane = static_cast<int>(lane_id());
+  const uint4 lo4 = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
+  const uint4 hi4 = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
+  const uint32_t v[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};  // bins 255-8l, 254-8l, ...
+  uint32_t own = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) own += v[k];
+  uint32_t incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
+  const int L = hit ? __ffs(hit) - 1 : 31;
+  if (lane == L) {
+    uint32_t run = incl - own;
+    int b = 255 - 8 * lane - 7;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (run + v[k] >= static_cast<uint32_t>(need)) {
+        b = 255 - 8 * lane - k;
+        break;
+      }
+      run += v[k];
+    }
+    s.find_b = b;
+    s.find_gt = static_cast<int>(run);
+  }
 }
 
 // G == 1: the CTA holds every candidate of the row. One pass over the buffer
 // writes the sure winners (keys above the threshold bin t) to the output,
-// lists the entries of bin t and histograms their key bits 19..12; a 256-bin
-// find picks the sub-bin holding the K-th key, a pass over the short list
-// writes the sub-bins above it, and the few entries of that sub-bin are ranked
-// directly. Output slots come from one shared atomic per warp.
+// lists the entries of bin t and histograms their key bits 19..12; one warp
+// picks the sub-bin holding the K-th key, a pass over the short list writes
+// the sub-bins above it and stages that sub-bin's few entries for ranking, and
+// they are ranked directly. Output slots come from one shared atomic per warp.
+// Starts right after close_window's barrier; five barriers in all.
 __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
   constexpr int kListIt = (kMaxTopK + kThreads - 1) / kThreads;
   const int K = p.topk;
@@ -927,19 +989,12 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
   const int lane = static_cast<int>(lane_id());
   const uint32_t lt = lanemask_lt();
   int32_t* o = p.out + r * static_cast<int64_t>(K);
-  csync();
   const uint32_t t = static_cast<uint32_t>(s.t);
   const int inbin = static_cast<int>(s.hist[t]);
   const int need = K - (s.cnt_ge - inbin);
   const int n = s.buf_n;
   bool done = false;
   if (inbin <= kMaxTopK) {
-    for (int b = tid; b < 256; b += kThreads) s.sub[b] = 0;
-    if (tid == 0) {
-      s.n_emit = 0;
-      s.n_list = 0;
-    }
-    csync();
     // pass 1 over the buffer, in two short loops (counts, then writes) so the
     // code stays small: one reservation per warp for winners and for the list
     int tw = 0, tc = 0;
@@ -985,14 +1040,14 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
         if (base + j < K) o[base + j] = s.bidx[s.emit[j]];
       done = true;
     } else {
-      block_find(s, s.sub, 256, need, true);
+      if (tid < 32) warp_find_top256(s, s.sub, need);
+      csync();
       const uint32_t b1 = static_cast<uint32_t>(s.find_b);
       const int need1 = need - s.find_gt;
       const int c1 = static_cast<int>(s.sub[b1]);
       if (c1 <= kSmallSet) {
-        // list pass: sub-bins above b1 are winners, sub-bin b1 goes to s.small
-        if (tid == 0) s.n_small = 0;
-        csync();
+        // list pass: sub-bins above b1 are winners; the entries of sub-bin b1
+        // go straight into the ranking slots
         uint32_t lw[kListIt], lk[kListIt];
         int pw = 0, pk = 0;
         int pos[kListIt];
@@ -1019,15 +1074,34 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
             const int q = qw + __popc(lw[j] & lt);
             if (q < K) o[q] = s.bidx[pos[j]];
           }
-          if ((lk[j] >> lane) & 1u) s.small[min(qk + __popc(lk[j] & lt), kSmallSet - 1)] = pos[j];
+          if ((lk[j] >> lane) & 1u) {
+            const int slot = min(qk + __popc(lk[j] & lt), kSmallSet - 1);
+            s.rk[slot] = s.bkey[pos[j]];
+            s.ri[slot] = s.bidx[pos[j]];
+          }
           qw += __popc(lw[j]);
           qk += __popc(lk[j]);
         }
         csync();
+        // rank the staged entries by (key desc, index asc); the need1 best are
+        // selected. Slots past m hold padding that beats nothing.
         const int base = s.n_emit;
         const int m = min(s.n_small, kSmallSet);
-        const int rank = rank_small(s, m, need1);
-        if (rank < need1 && base + rank < K) o[base + rank] = s.ri[tid];
+        if (tid < m) {
+          const uint32_t kj = s.rk[tid];
+          const int32_t ij = s.ri[tid];
+          int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+          for (int i0 = 0; i0 < m; i0 += 4) {
+            const uint4 k4 = *reinterpret_cast<const uint4*>(&s.rk[i0]);
+            const int4 x4 = *reinterpret_cast<const int4*>(&s.ri[i0]);
+            r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
+            r1 += (k4.y > kj || (k4.y == kj && x4.y < ij)) ? 1 : 0;
+            r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
+            r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
+          }
+          const int rank = r0 + r1 + r2 + r3;
+          if (rank < need1 && base + rank < K) o[base + rank] = ij;
+        }
         done = true;
       }
     }
@@ -1193,16 +1267,17 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
   const int g = static_cast<int>(blockIdx.x) / p.G;
   const int m = static_cast<int>(blockIdx.x) % p.G;
 
-  if (tid == 0) {
+  if (tid == kThreads) {
+    // the copy thread sets up the ring and, with whole rows per CTA, issues
+    // the first copy right away; everyone else meets it at the barrier below
     s.abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1u);
       mbar_init(&s.empty[i], kWarps);
     }
     fence_mbar_init();
+    if (p.G == 1) producer_first(p, s, g);
   }
-  __syncthreads();
-  if (tid == kThreads && p.G == 1) producer_first(p, s, g);
   if (tid < kThreads) {
     reset_row_state(s);
     for (int k = tid; k < kLenCache; k += kThreads) {

@@ -34,8 +34,9 @@ def test_the_five_workloads_on_a_gb300():
     assert rc == 0 and pl.ctas_per_group == 1 and pl.grid == 64
     rc, pl = plan(gb, 16, 131072)
     assert rc == 0 and pl.ctas_per_group == 9 and pl.grid == 144 and pl.cooperative
+    # two CTAs per row would save 81920 elements each, less than the merge costs
     rc, pl = plan(gb, 64, 163840, next_n=2, topk=1024)
-    assert rc == 0 and pl.ctas_per_group == 2 and pl.grid == 128 and pl.cooperative
+    assert rc == 0 and pl.ctas_per_group == 1 and pl.grid == 64 and not pl.cooperative
     rc, pl = plan(gb, 4096, 65536)
     assert rc == 0 and pl.ctas_per_group == 1 and pl.grid == 152 and not pl.cooperative
 
@@ -85,6 +86,19 @@ def test_invariants_on_random_shapes():
             assert pl.cooperative == 0 and pl.grid <= cap
 
 
+def test_split_gain_rule():
+    gb = props()
+    for rows, stride in ((16, 131072), (4, 200000), (32, 96000), (64, 163840), (8, 65536), (2, 98304)):
+        rc, pl = plan(gb, rows, stride)
+        assert rc == 0
+        G = pl.ctas_per_group
+        if G > 1:
+            assert stride * (G - 1) // G >= 90000
+        else:
+            g = min(16, 152 // rows, max(1, stride // 8192))
+            assert g < 2 or stride <= 32768 or stride * (g - 1) // g < 90000
+
+
 def test_rejections():
     gb = props()
     assert plan(gb, 8, 4096, topk=100)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
@@ -100,7 +114,9 @@ def test_threshold_and_capacity_knobs():
     gb = props()
     rc, pl = plan(gb, 16, 131072, long_row_threshold=200000)
     assert rc == 0 and pl.ctas_per_group == 1
-    rc, pl = plan(gb, 16, 131072, max_ctas=40)
+    rc, pl = plan(gb, 16, 400000, max_ctas=40)
     assert rc == 0 and pl.ctas_per_group == 2 and pl.grid <= 40
+    rc, pl = plan(gb, 16, 131072, max_ctas=40)  # a 2-way split saves too little
+    assert rc == 0 and pl.ctas_per_group == 1
     rc, pl = plan(gb, 3, 4096, force_ctas_per_group=4)
     assert rc == 0 and pl.grid == 12 and pl.cooperative
