@@ -76,6 +76,10 @@ typedef struct {
   size_t workspace_bytes;
   /* 0 = every SM; otherwise at most this many co-resident CTAs are planned. */
   int max_ctas;
+  /* How the CTAs splitting a row merge their candidates. 0 = planner decides;
+   * 1 = through the workspace, with a grid-level barrier (any G); 2 = inside a
+   * thread-block cluster, through its distributed shared memory (G <= 8). */
+  int merge;
 } topk_options;
 
 /* Properties of a device as the planner sees them. */
@@ -84,6 +88,9 @@ typedef struct {
   int max_smem_optin; /* opt-in shared memory per block, bytes */
   int smem_per_cta;   /* dynamic shared memory the kernel needs, bytes */
   int ctas_per_sm;    /* resident CTAs per SM for the exact kernel instance (occupancy) */
+  /* cluster_groups[c], c = 2..8: clusters of c CTAs of the kernel that can be
+   * resident at once (0 = none; entries 0 and 1 are unused). */
+  int cluster_groups[9];
 } topk_device_props;
 
 /* A launch configuration. */
@@ -93,7 +100,8 @@ typedef struct {
   int grid;           /* CTAs launched = num_groups * ctas_per_group */
   int threads;        /* threads per CTA */
   int smem_bytes;     /* dynamic shared memory per CTA */
-  int cooperative;    /* 1 when the CTAs of a group wait on one another */
+  int cooperative;    /* 1 when the CTAs of a group wait on one another through the workspace */
+  int cluster;        /* 1 when the CTAs of a group form a cluster and merge in its shared memory */
 } topk_plan;
 
 /*
@@ -189,9 +197,11 @@ int topk_query_device(int device, topk_device_props* props);
  * The host planner, a pure function of its arguments (no CUDA call), so it can
  * be checked against made-up devices. It sizes the grid from the occupancy in
  * *props and never plans more co-resident CTAs than num_sms * ctas_per_sm when
- * CTAs of a group wait on one another; the deadlock of an oversized
- * cooperative grid (vLLM PR #41189 page, "Feature and motivation": TopK=1024
- * with MTP=1) cannot be planned. options may be NULL.
+ * CTAs of a group wait on one another through the workspace; the deadlock of
+ * an oversized cooperative grid (vLLM PR #41189 page, "Feature and
+ * motivation": TopK=1024 with MTP=1) cannot be planned. A cluster merge waits
+ * only inside a cluster, whose CTAs the hardware schedules together, and plans
+ * at most cluster_groups[G] groups. options may be NULL.
  */
 int topk_make_plan(const topk_device_props* props, int64_t num_rows, int64_t row_stride,
                    int next_n, int topk, const topk_options* options, topk_plan* plan);

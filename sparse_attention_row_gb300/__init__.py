@@ -37,6 +37,10 @@ TOPK_ERR_BARRIER_TIMEOUT = 6
 TOPK_ERR_LENGTH_CLAMPED = 7
 TOPK_ERR_PLAN = 8
 
+TOPK_MERGE_AUTO = 0
+TOPK_MERGE_WORKSPACE = 1
+TOPK_MERGE_CLUSTER = 2
+
 TOPK_DEV_LENGTH_CLAMPED = 0x1
 TOPK_DEV_BARRIER_TIMEOUT = 0x2
 TOPK_DEV_STAGE_TIMEOUT = 0x4
@@ -57,14 +61,16 @@ class TopkOptions(ctypes.Structure):
                 ("barrier_timeout_us", ctypes.c_uint32),
                 ("inject_skip_arrival", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t),
-                ("max_ctas", ctypes.c_int)]
+                ("max_ctas", ctypes.c_int),
+                ("merge", ctypes.c_int)]
 
 
 class TopkDeviceProps(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int),
                 ("max_smem_optin", ctypes.c_int),
                 ("smem_per_cta", ctypes.c_int),
-                ("ctas_per_sm", ctypes.c_int)]
+                ("ctas_per_sm", ctypes.c_int),
+                ("cluster_groups", ctypes.c_int * 9)]
 
 
 class TopkPlan(ctypes.Structure):
@@ -73,7 +79,8 @@ class TopkPlan(ctypes.Structure):
                 ("grid", ctypes.c_int),
                 ("threads", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int),
-                ("cooperative", ctypes.c_int)]
+                ("cooperative", ctypes.c_int),
+                ("cluster", ctypes.c_int)]
 
 
 def library_path() -> str:

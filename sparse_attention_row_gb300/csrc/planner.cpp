@@ -19,9 +19,17 @@
 //     merging a row across a group costs about 16 us more than finishing it in
 //     one CTA, so smaller savings lose (64 rows of 163840 run faster whole,
 //     16 rows of 131072 faster split nine ways);
+//   - where the device runs thread-block clusters of G CTAs (G <= 8), the CTAs
+//     of a group form one cluster and merge in its distributed shared memory;
+//     the split is then the largest size up to 8 whose clusters can all be
+//     resident with one per row, and kept if it saves at least
+//     kSplitGainCluster elements per CTA; otherwise they merge through the
+//     workspace with a grid-level barrier;
 //   - G = 1 launches min(num_rows, capacity) persistent CTAs, no waiting;
-//   - G > 1 launches num_groups = min(capacity / G, num_rows, num_sms) groups,
-//     so grid = num_groups * G <= num_sms * ctas_per_sm always.
+//   - a workspace merge launches num_groups = min(capacity / G, num_rows,
+//     num_sms) groups cooperatively, so grid = num_groups * G <= num_sms *
+//     ctas_per_sm always; a cluster merge launches at most cluster_groups[G]
+//     groups, and its CTAs wait only on CTAs of their own cluster.
 #include <stdint.h>
 
 #include <algorithm>
@@ -51,26 +59,57 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   const int64_t threshold = (options != nullptr && options->long_row_threshold > 0)
                                 ? options->long_row_threshold
                                 : ltk::kDefaultLongRowThreshold;
+  const int merge = (options != nullptr) ? options->merge : 0;
+  if (merge < 0 || merge > 2) return TOPK_ERR_INVALID_ARG;
+  auto clusters_of = [&](int64_t c) -> int64_t {
+    return (c >= 2 && c <= ltk::kMaxCluster) ? props->cluster_groups[c] : 0;
+  };
   int64_t G = 1;
+  bool cluster = false;
   if (options != nullptr && options->force_ctas_per_group != 0) {
     G = options->force_ctas_per_group;
     if (G < 1 || G > ltk::kMaxGroup) return TOPK_ERR_INVALID_ARG;
+    if (G > 1) {
+      if (merge == 2 && clusters_of(G) < 1) return TOPK_ERR_PLAN;
+      cluster = merge == 2 || (merge == 0 && clusters_of(G) >= 1);
+    }
   } else if (num_rows > 0 && row_stride > threshold && num_rows < cap) {
     G = cap / num_rows;
     G = std::min<int64_t>(G, ltk::kMaxGroup);
     G = std::min<int64_t>(G, std::max<int64_t>(1, row_stride / ltk::kMinSpan));
-    if (G < 2 || row_stride * (G - 1) / G < ltk::kSplitGain) G = 1;
+    // the largest cluster size whose clusters hold every row at once
+    int64_t gc = (merge != 1 && G >= 2) ? std::min<int64_t>(G, ltk::kMaxCluster) : 0;
+    while (gc >= 2 && clusters_of(gc) < num_rows) --gc;
+    if (gc >= 2) {
+      G = gc;
+      cluster = true;
+    } else if (merge == 2) {
+      G = 1;
+    }
+    const int64_t gain = cluster ? ltk::kSplitGainCluster : ltk::kSplitGain;
+    if (G < 2 || row_stride * (G - 1) / G < gain) {
+      G = 1;
+      cluster = false;
+    }
   }
   plan->ctas_per_group = static_cast<int>(G);
+  plan->cluster = cluster ? 1 : 0;
   if (num_rows == 0) {
     plan->num_groups = 0;
     plan->grid = 0;
-    plan->cooperative = G > 1;
+    plan->cooperative = (G > 1 && !cluster) ? 1 : 0;
     return TOPK_OK;
   }
   int64_t groups;
   if (G == 1) {
     groups = std::min<int64_t>(num_rows, cap);
+    plan->cooperative = 0;
+  } else if (cluster) {
+    // clusters never wait on one another; the hardware co-schedules each one
+    groups = std::min<int64_t>(num_rows, clusters_of(G));
+    groups = std::min<int64_t>(groups, cap / G);
+    groups = std::min<int64_t>(groups, props->num_sms);  // workspace holds num_sms groups
+    if (groups < 1) return TOPK_ERR_PLAN;
     plan->cooperative = 0;
   } else {
     groups = std::min<int64_t>(cap / G, num_rows);

@@ -27,6 +27,7 @@ struct EnvKnobs {
   int64_t long_row_threshold = 0;
   int force_ctas_per_group = 0;
   uint32_t timeout_us = 0;
+  int merge = 0;
 };
 
 EnvKnobs read_env() {
@@ -34,6 +35,7 @@ EnvKnobs read_env() {
   if (const char* v = getenv("LIBTOPK_LONG_ROW_THRESHOLD")) e.long_row_threshold = atoll(v);
   if (const char* v = getenv("LIBTOPK_FORCE_CTAS_PER_GROUP")) e.force_ctas_per_group = atoi(v);
   if (const char* v = getenv("LIBTOPK_BARRIER_TIMEOUT_US")) e.timeout_us = static_cast<uint32_t>(atoll(v));
+  if (const char* v = getenv("LIBTOPK_MERGE")) e.merge = atoi(v);
   return e;
 }
 
@@ -60,6 +62,12 @@ int query_device_locked(int device, topk_device_props* out) {
     if (rc == TOPK_OK && p.smem_per_cta <= p.max_smem_optin) {
       if (ltk::kernel_configure() != cudaSuccess || ltk::kernel_occupancy(&p.ctas_per_sm) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
+      for (int c = 2; rc == TOPK_OK && c <= ltk::kMaxCluster; ++c) {
+        if (ltk::kernel_max_clusters(c, &p.cluster_groups[c]) != cudaSuccess) {
+          cudaGetLastError();  // a device without clusters: no cluster merge is planned
+          p.cluster_groups[c] = 0;
+        }
+      }
     } else if (rc == TOPK_OK) {
       p.ctas_per_sm = 0;  // the kernel cannot be resident; planning reports TOPK_ERR_PLAN
     }
@@ -171,6 +179,7 @@ int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengt
   if (opt.long_row_threshold == 0) opt.long_row_threshold = env.long_row_threshold;
   if (opt.force_ctas_per_group == 0) opt.force_ctas_per_group = env.force_ctas_per_group;
   if (opt.barrier_timeout_us == 0) opt.barrier_timeout_us = env.timeout_us;
+  if (opt.merge == 0) opt.merge = env.merge;
 
   topk_plan plan{};
   rc = topk_make_plan(&props, num_rows, row_stride, next_n, topk, &opt, &plan);
@@ -191,6 +200,7 @@ int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengt
   p.timeout_ns = opt.barrier_timeout_us ? static_cast<uint64_t>(opt.barrier_timeout_us) * 1000ull
                                         : ltk::kDefaultTimeoutNs;
   p.inject = opt.inject_skip_arrival;
+  p.cluster = plan.cluster;
   if (ltk::launch_topk(p, plan.grid, plan.cooperative != 0, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess) {
     cudaGetLastError();

@@ -16,11 +16,13 @@ constexpr int kBins = 4096;            // 12-bit radix digits
 constexpr int kBufCap = 12288;         // candidate (key, index) pairs kept per CTA
 constexpr int kMaxTopK = 2048;
 constexpr int kMaxGroup = 16;          // CTAs that may split one row
+constexpr int kMaxCluster = 8;         // CTAs of a group that may form one thread-block cluster
 constexpr int kLenCache = 64;          // row lengths cached in shared memory
 constexpr int kSmallSet = 64;          // candidate sets up to this size are ranked by one warp
 constexpr int kMinSpan = 8192;         // fewest elements per CTA when a row is split
 constexpr int64_t kDefaultLongRowThreshold = 32768;
-constexpr int64_t kSplitGain = 90000;  // elements a row split must save per CTA (measured)
+constexpr int64_t kSplitGain = 90000;         // elements a workspace-merged split must save per CTA (measured)
+constexpr int64_t kSplitGainCluster = 24000;  // elements a cluster-merged split must save per CTA
 constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 static_assert(kMaxTopK + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");
@@ -57,11 +59,13 @@ struct Params {
   GroupWs* groups;
   uint64_t timeout_ns;
   int inject;
+  int cluster;       // 1: the G CTAs of a group are one cluster and merge through its shared memory
 };
 
 size_t kernel_smem_bytes();
 cudaError_t kernel_configure();                 // sets the shared-memory opt-in (current device)
 cudaError_t kernel_occupancy(int* ctas_per_sm);  // occupancy of the exact kernel
+cudaError_t kernel_max_clusters(int cluster_size, int* clusters);  // co-resident clusters of that size
 cudaError_t launch_topk(const Params& p, int grid, bool cooperative, cudaStream_t stream);
 
 }  // namespace ltk

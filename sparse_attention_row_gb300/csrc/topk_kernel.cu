@@ -58,6 +58,7 @@ struct __align__(128) Smem {
   uint32_t bsum[kBins / 32];      // 32-bin block sums used by block_find
   unsigned long long full[kStages];
   unsigned long long empty[kStages];
+  unsigned long long xbar[2];     // cluster merge barriers (one arrival per member CTA)
   int32_t lens[kLenCache];
   uint32_t wtot[kWarps];
   int g_e[kMaxGroup];
@@ -68,10 +69,15 @@ struct __align__(128) Smem {
   float thr_f;
   int find_b, find_gt;
   int abort, last, off, take;
+  int first_issued;
   int n_list;
   uint32_t red;
   uint32_t sel_T;
   int sel_I;
+  int x_t, x_in;                  // cluster merge: t_max, then the count in bin t*
+  int x_n0;                       // cluster merge: this CTA's buffer size when the merge began
+  int x_ln;                       // cluster merge: the leader's buffer size, as read here
+  int x_push;                     // cluster merge: entries the other members appended (leader only)
 };
 
 // ---------------------------------------------------------------- primitives
@@ -162,6 +168,53 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v
   uint32_t old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+
+// Distributed shared memory of a thread-block cluster: the address of the same
+// shared variable in the CTA of cluster rank `rank`, and accesses through it.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(p)), "r"(rank));
+  return a;
+}
+
+__device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// Arrives on an mbarrier of another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Hardware barrier over every thread of the cluster; used once, at kernel
+// start, where every thread of every CTA reaches it.
+__device__ __forceinline__ void cluster_barrier_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
@@ -529,6 +582,7 @@ __device__ void reset_row_state(Smem& s) {
     s.thr_lo = 0;
     s.thr_f = key_floor_value(0u);
     s.n_emit = 0;
+    s.x_push = 0;  // other members append to a leader only after the next merge's first sync
   }
 }
 
@@ -702,13 +756,11 @@ __device__ __forceinline__ int row_len(const Params& p, const Smem& s, int64_t k
   return clamp_len(p, __ldg(p.lengths + r));
 }
 
-// Part of row k (of this CTA's group) that this CTA streams, and its copy
+// Part of row r (length len) that member m of a group streams, and its copy
 // windows.
-__device__ __forceinline__ bool get_row(const Params& p, const Smem& s, int64_t k, int g, int m,
-                                        RowWin& w) {
-  w.r = g + k * p.num_groups;
-  if (w.r >= p.num_rows) return false;
-  w.len = row_len(p, s, k, w.r);
+__device__ __forceinline__ void row_window(const Params& p, int64_t r, int len, int m, RowWin& w) {
+  w.r = r;
+  w.len = len;
   w.rowp = p.logits + w.r * p.stride;
   w.nch = 0;
   w.lo = w.hi = w.wstart = w.wend = 0;
@@ -728,30 +780,55 @@ __device__ __forceinline__ bool get_row(const Params& p, const Smem& s, int64_t 
       w.nch = (w.wend - w.wstart + kChunk - 1) / kChunk;
     }
   }
+}
+
+// Row k of this CTA's group, and this CTA's part of it.
+__device__ __forceinline__ bool get_row(const Params& p, const Smem& s, int64_t k, int g, int m,
+                                        RowWin& w) {
+  const int64_t r = g + k * p.num_groups;
+  if (r >= p.num_rows) return false;
+  row_window(p, r, row_len(p, s, k, r), m, w);
   return true;
 }
 
-// With whole rows per CTA, the copy warp issues the first chunk of the CTA's
-// first row before the row lengths are known: the copy window is sized by the
-// row stride, which covers the first chunk of any length. It becomes that
-// row's chunk 0, or a chunk the consumers discard if the row needs no streaming.
-__device__ __noinline__ void producer_first(const Params& p, Smem& s, int g) {
-  const float* rowp = p.logits + static_cast<int64_t>(g) * p.stride;
-  const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
-  const int64_t ws = -mis;
-  const int64_t wend = ws + ((p.stride - ws + 3) & ~static_cast<int64_t>(3));
-  const int64_t we = min(ws + kChunk, wend);
-  const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
+// The copy warp issues the first chunk of the CTA's first row at kernel start,
+// before the consumers have filled the length cache (in a cluster launch, right
+// after the cluster barrier). With whole rows per CTA
+// the copy window is sized by the row stride, which covers the first chunk of
+// any length: it becomes that row's chunk 0, or a chunk the consumers discard
+// if the row needs no streaming. When a row is split, the copy thread reads the
+// row's length itself and issues chunk 0 of its part, if it has one. Returns
+// whether a copy was issued.
+__device__ __noinline__ bool producer_first(const Params& p, Smem& s, int g, int m) {
+  if (p.G == 1) {
+    const float* rowp = p.logits + static_cast<int64_t>(g) * p.stride;
+    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
+    const int64_t ws = -mis;
+    const int64_t wend = ws + ((p.stride - ws + 3) & ~static_cast<int64_t>(3));
+    const int64_t we = min(ws + kChunk, wend);
+    const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
+    fence_proxy_async();
+    mbar_expect_tx(&s.full[0], bytes);
+    bulk_copy_g2s(s.stage[0], rowp + ws, bytes, &s.full[0]);
+    return true;
+  }
+  if (g >= p.num_rows) return false;
+  RowWin w;
+  row_window(p, g, clamp_len(p, __ldg(p.lengths + g)), m, w);
+  if (w.nch == 0) return false;
+  const int we = min(w.wstart + kChunk, w.wend);
+  const uint32_t bytes = static_cast<uint32_t>(we - w.wstart) * 4u;
   fence_proxy_async();
   mbar_expect_tx(&s.full[0], bytes);
-  bulk_copy_g2s(s.stage[0], rowp + ws, bytes, &s.full[0]);
+  bulk_copy_g2s(s.stage[0], w.rowp + w.wstart, bytes, &s.full[0]);
+  return true;
 }
 
 // The copy warp's loop (one lane): issues every chunk this CTA will consume,
-// in consumption order, into the ring slot freed by the consumers. With whole
-// rows per CTA, chunk 0 of the first row was issued by producer_first.
-__device__ __noinline__ void producer_loop(const Params& p, Smem& s, int g, int m) {
-  const bool spec = (p.G == 1);
+// in consumption order, into the ring slot freed by the consumers. `first`:
+// producer_first issued chunk 0 of the first row.
+__device__ __noinline__ void producer_loop(const Params& p, Smem& s, int g, int m, bool first) {
+  const bool spec = first;
   uint32_t q = spec ? 1u : 0u;
   RowWin w;
   bool stop = false;
@@ -777,8 +854,8 @@ __device__ __noinline__ void producer_loop(const Params& p, Smem& s, int g, int 
     }
   }
   // every issued copy must land before the CTA may exit
-  const uint32_t first = q > kStages ? q - kStages : 0u;
-  for (uint32_t i = first; i < q; ++i)
+  const uint32_t oldest = q > kStages ? q - kStages : 0u;
+  for (uint32_t i = oldest; i < q; ++i)
     mbar_wait_bounded(&s.full[i % kStages], (i / kStages) & 1u, p.timeout_ns, nullptr);
 }
 
@@ -1258,6 +1335,203 @@ __device__ __noinline__ bool finish_group(Smem& s, const Params& p, int64_t r, i
   return true;
 }
 
+// ------------------------------------------------------------- cluster merge
+
+// Barrier among the consumer warps of every CTA of the cluster, with a bounded
+// wait: threads 0..G-1 of each CTA arrive on the merge barrier of CTA `tid`,
+// then every consumer thread waits until its own CTA's barrier has collected
+// G arrivals. Two barriers alternate, so a CTA that has passed one sync cannot
+// land its next arrival on a phase another CTA is still waiting for. The copy
+// warp takes no part (a hardware cluster barrier would wait for it). Returns
+// false, with TOPK_DEV_BARRIER_TIMEOUT set, if the wait ran out. Consumer-wide.
+__device__ bool cluster_sync(Smem& s, const Params& p, uint32_t& xph) {
+  csync();  // this CTA's writes, local and remote, come before its arrivals
+  const int b = static_cast<int>(xph & 1u);
+  const uint32_t parity = (xph >> 1) & 1u;
+  ++xph;
+  if (threadIdx.x < static_cast<unsigned>(p.G)) mbar_arrive_remote(dsmem_addr(&s.xbar[b], threadIdx.x));
+  bool ok = mbar_try_wait_cluster(&s.xbar[b], parity);
+  if (!ok) {
+    const uint64_t t0 = global_timer();
+    while (!ok) {
+#pragma unroll 1
+      for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait_cluster(&s.xbar[b], parity);
+      if (!ok && global_timer() - t0 > p.timeout_ns) break;
+    }
+    if (!ok) {
+      atomicOr(p.status, 0x2u);
+      s.abort = 1;
+    }
+  }
+  csync();
+  return s.abort == 0;
+}
+
+// Count of bin b over the members of the cluster: this CTA's own count plus
+// the other members' (read from their shared memory).
+__device__ __forceinline__ uint32_t merged_count(Smem& s, int b, int m, int G) {
+  uint32_t c = s.hist[b];
+  for (int r = 0; r < G; ++r)
+    if (r != m) c += dsmem_ld(dsmem_addr(&s.hist[b], static_cast<uint32_t>(r)));
+  return c;
+}
+
+// block_find from the top over the members' merged counts of bins >= tmax
+// (those counts are exact; bins below are never reached because the suffix at
+// tmax already holds need). Writes the bin to s.find_b, the count above it to
+// s.find_gt and its own count to s.x_in. Consumer-wide; ends with a barrier.
+__device__ void cluster_find(Smem& s, int tmax, int need, int m, int G) {
+  const int lane = static_cast<int>(lane_id());
+  const int warp = threadIdx.x >> 5;
+  const int nblk = (kBins - tmax + 31) >> 5;
+  for (int q = warp; q < nblk; q += kWarps) {
+    const int b = kBins - 1 - (32 * q + lane);
+    const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, (b >= tmax) ? merged_count(s, b, m, G) : 0u);
+    if (lane == 0) s.bsum[q] = sum;
+  }
+  csync();
+  if (warp == 0) {
+    uint32_t b4[4];
+    uint32_t own = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = 4 * lane + k;
+      b4[k] = (q < nblk) ? s.bsum[q] : 0u;
+      own += b4[k];
+    }
+    uint32_t incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
+    const int L = hit ? __ffs(hit) - 1 : 31;
+    uint32_t run = incl - own;
+    int qsel = 0;
+    if (lane == L) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (run + b4[k] >= static_cast<uint32_t>(need)) {
+          qsel = 4 * lane + k;
+          break;
+        }
+        run += b4[k];
+      }
+    }
+    qsel = __shfl_sync(0xFFFFFFFFu, qsel, L);
+    run = __shfl_sync(0xFFFFFFFFu, run, L);
+    const int bin = kBins - 1 - (32 * qsel + lane);
+    const uint32_t h = (bin >= tmax) ? merged_count(s, bin, m, G) : 0u;
+    uint32_t in2 = h;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, in2, o);
+      if (lane >= o) in2 += v;
+    }
+    const uint32_t hit2 = __ballot_sync(0xFFFFFFFFu, run + in2 >= static_cast<uint32_t>(need));
+    const int L2 = hit2 ? __ffs(hit2) - 1 : 0;
+    if (lane == L2) {
+      s.find_b = bin;
+      s.find_gt = static_cast<int>(run + in2 - h);
+      s.x_in = static_cast<int>(h);
+    }
+  }
+  csync();
+}
+
+// This member's buffered entries in bins >= ts, appended to the leader's
+// buffer from position n0 on (one remote reservation per warp).
+__device__ void push_to_leader(Smem& s, uint32_t ts, int n0) {
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const int n = s.buf_n;
+  int c = 0;
+#pragma unroll 1
+  for (int i = tid; i < n; i += kThreads) c += ((s.bkey[i] >> 20) >= ts) ? 1 : 0;
+  c = __reduce_add_sync(0xFFFFFFFFu, c);
+  int base = 0;
+  if (lane == 0 && c) base = static_cast<int>(dsmem_atom_add(dsmem_addr(&s.x_push, 0u), static_cast<uint32_t>(c)));
+  base = n0 + __shfl_sync(0xFFFFFFFFu, base, 0);
+  const uint32_t kaddr = dsmem_addr(&s.bkey[0], 0u);
+  const uint32_t iaddr = dsmem_addr(&s.bidx[0], 0u);
+  const uint32_t lt = lanemask_lt();
+  const int jmax = (n + kThreads - 1) / kThreads;
+#pragma unroll 1
+  for (int j = 0; j < jmax; ++j) {
+    const int i = tid + j * kThreads;
+    const uint32_t k = (i < n) ? s.bkey[i] : 0u;
+    const bool sel = i < n && (k >> 20) >= ts;
+    const uint32_t bm = __ballot_sync(0xFFFFFFFFu, sel);
+    const int q = base + __popc(bm & lt);
+    if (sel && q < kBufCap) {
+      dsmem_st(kaddr + 4u * static_cast<uint32_t>(q), k);
+      dsmem_st(iaddr + 4u * static_cast<uint32_t>(q), static_cast<uint32_t>(s.bidx[i]));
+    }
+    base += __popc(bm);
+  }
+}
+
+// Merge of one split row inside a cluster, after every member closed its
+// window. Every member's buffer holds at least the best K of its own part, so
+// the union holds the row's best K, and each member with threshold bin t_m > 0
+// keeps at least K keys in bins >= t_m: the K-th key of the row lies in a bin
+// >= t_max, the largest t_m. From X1 to X3 no member changes its counts,
+// threshold or buffer size, so every member reads the others' counts of bins
+// >= t_max and finds the same bin t* of the K-th key; the members then append
+// their entries of bins >= t* to the leader's (rank 0) buffer, and the leader
+// finishes the row like a whole-row CTA, its own entries below t* ignored.
+// If the leader's buffer cannot take them as it is, it first keeps only its
+// bins >= t* (one more sync); if even the union does not fit, every member
+// goes to the workspace merge. Returns 1 on the leader, 0 on the members, 2
+// for the workspace merge (everywhere), -1 on a time-out.
+__device__ __noinline__ int cluster_merge(Smem& s, const Params& p, int m, uint32_t& xph) {
+  const int tid = threadIdx.x;
+  const int G = p.G;
+  if (tid == 0) s.x_n0 = s.buf_n;  // what the others read as this CTA's size until X3
+  if (!cluster_sync(s, p, xph)) return -1;  // X1: every window is closed
+  if (tid < 32) {
+    uint32_t tm = 0;
+    if (tid < G) tm = (tid == m) ? static_cast<uint32_t>(s.t) : dsmem_ld(dsmem_addr(&s.t, static_cast<uint32_t>(tid)));
+    tm = __reduce_max_sync(0xFFFFFFFFu, tm);
+    if (tid == 0) {
+      s.x_t = static_cast<int>(tm);
+      s.x_ln = (m == 0) ? s.x_n0 : static_cast<int>(dsmem_ld(dsmem_addr(&s.x_n0, 0u)));
+    }
+  }
+  csync();
+  cluster_find(s, s.x_t, p.topk, m, G);
+  const int ts = s.find_b;
+  const int inbin = s.x_in;
+  const int tot = s.find_gt + inbin;
+  int n0 = s.x_ln;
+  if (n0 + tot > kBufCap) {
+    if (tot > kBufCap) return 2;  // heavy ties at t*: same decision in every member
+    if (m == 0) compact_buffer(s, [=](uint32_t k, int32_t) { return (k >> 20) >= static_cast<uint32_t>(ts); });
+    if (!cluster_sync(s, p, xph)) return -1;  // X2: the leader kept only its bins >= t*
+    if (tid == 0) s.x_ln = (m == 0) ? s.buf_n : static_cast<int>(dsmem_ld(dsmem_addr(&s.buf_n, 0u)));
+    csync();
+    n0 = s.x_ln;
+  }
+  if (m != 0) push_to_leader(s, static_cast<uint32_t>(ts), n0);
+  if (!cluster_sync(s, p, xph)) return -1;  // X3: the union is in the leader's buffer
+  if (m != 0) return 0;
+  if (tid == 0) {
+    s.t = ts;
+    s.cnt_ge = tot;
+    s.hist[ts] = static_cast<uint32_t>(inbin);
+    int n = n0 + s.x_push;
+    if (n > kBufCap) {  // cannot happen when the counts agree; never read past the buffer
+      atomicOr(p.status, 0x4u);
+      n = kBufCap;
+    }
+    s.buf_n = n;
+    s.x_push = 0;
+  }
+  csync();
+  return 1;
+}
+
 // ------------------------------------------------------------------- kernel
 
 __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Params p) {
@@ -1275,8 +1549,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
       mbar_init(&s.full[i], 1u);
       mbar_init(&s.empty[i], kWarps);
     }
+    if (p.cluster) {
+      mbar_init(&s.xbar[0], static_cast<uint32_t>(p.G));
+      mbar_init(&s.xbar[1], static_cast<uint32_t>(p.G));
+    }
     fence_mbar_init();
-    if (p.G == 1) producer_first(p, s, g);
+    // a cluster launch issues no copy before every CTA of its cluster runs
+    s.first_issued = (!p.cluster && producer_first(p, s, g, m)) ? 1 : 0;
   }
   if (tid < kThreads) {
     reset_row_state(s);
@@ -1286,14 +1565,22 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
     }
   }
   __syncthreads();
+  if (p.cluster) {
+    // every CTA of the cluster runs, and its merge barriers exist, before any
+    // CTA copies into cluster shared memory or arrives on another's barrier
+    cluster_barrier_all();
+    if (tid == kThreads) s.first_issued = producer_first(p, s, g, m) ? 1 : 0;
+  }
   if (tid >= kThreads) {
-    if (tid == kThreads) producer_loop(p, s, g, m);
+    if (tid == kThreads) producer_loop(p, s, g, m, s.first_issued != 0);
     return;
   }
 
   const int K = p.topk;
   uint32_t q = 0;  // chunks consumed
   uint32_t epoch = 0;
+  uint32_t xph = 0;       // cluster merge syncs passed
+  bool used_ws = false;   // some row of a split group went through the workspace merge
   bool first_barrier = true;
   bool aborted = false;
   RowWin w;
@@ -1359,6 +1646,19 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
     close_window(s, p, w);
     if (p.G == 1) {
       finish_local(s, p, w.r);
+    } else if (p.cluster) {
+      const int mode = cluster_merge(s, p, m, xph);
+      if (mode == 1) {
+        finish_local(s, p, w.r);
+      } else if (mode == 0) {
+        reset_row_state(s);
+        csync();
+      } else if (mode == 2) {
+        used_ws = true;
+        if (!finish_group(s, p, w.r, g, m, epoch, first_barrier)) aborted = true;
+      } else {
+        aborted = true;
+      }
     } else if (!finish_group(s, p, w.r, g, m, epoch, first_barrier)) {
       aborted = true;
     }
@@ -1368,7 +1668,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
     s.abort = 1;
     return;
   }
-  if (p.G > 1) {
+  if (p.cluster) {
+    // no CTA leaves while another may still reach into its shared memory
+    if (!cluster_sync(s, p, xph)) return;
+  }
+  if (p.G > 1 && (!p.cluster || used_ws)) {
     // last CTA of the group to finish clears the per-member words and counters
     GroupWs* gw = p.groups + g;
     csync();
@@ -1407,6 +1711,21 @@ cudaError_t kernel_occupancy(int* ctas_per_sm) {
                                                        sizeof(Smem));
 }
 
+cudaError_t kernel_max_clusters(int cluster_size, int* clusters) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster_size));
+  cfg.blockDim = dim3(kCtaThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, topk_ragged_kernel, &cfg);
+}
+
 cudaError_t launch_topk(const Params& p, int grid, bool cooperative, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1414,10 +1733,19 @@ cudaError_t launch_topk(const Params& p, int grid, bool cooperative, cudaStream_
   cfg.dynamicSmemBytes = sizeof(Smem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = cooperative ? 1 : 0;
+  cfg.numAttrs = 0;
+  if (p.cluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.G);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+  } else if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.numAttrs = 1;
+  }
   return cudaLaunchKernelEx(&cfg, topk_ragged_kernel, p);
 }
 

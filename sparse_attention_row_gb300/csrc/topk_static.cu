@@ -105,6 +105,7 @@ extern "C" int topk_ragged_static(const float* logits, int64_t row_stride, const
   p.groups = reinterpret_cast<ltk::GroupWs*>(static_cast<char*>(scratch) + ltk::kWsHeaderBytes);
   p.timeout_ns = ltk::kDefaultTimeoutNs;
   p.inject = 0;
+  p.cluster = plan.cluster;
   if (ltk::launch_topk(p, plan.grid, plan.cooperative != 0, s) != cudaSuccess) {
     cudaGetLastError();
     return TOPK_ERR_CUDA;

@@ -26,12 +26,18 @@ def test_workloads_small_auto(rn, name, rows):
     assert rn.workspace_clean()
 
 
-@pytest.mark.parametrize("G", [1, 2, 3, 5, 9, 16])
+# merge 1: the CTAs of a row merge through the workspace (grid barrier);
+# merge 2: they form a thread-block cluster and merge in its shared memory
+SPLITS = [(1, 0), (2, 1), (2, 2), (3, 1), (3, 2), (5, 2), (8, 2), (9, 1), (16, 1)]
+
+
+@pytest.mark.parametrize("G,merge", SPLITS)
 @pytest.mark.parametrize("name,rows", [("decode_batch", 6), ("long_coop", 3), ("mtp", 4), ("prefill", 4)])
-def test_workloads_forced_split(rn, name, rows, G):
+def test_workloads_forced_split(rn, name, rows, G, merge):
     w = workloads.make(name, rows)
-    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(force_ctas_per_group=G))
-    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} G={G}")
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n,
+                 options=rn.options(force_ctas_per_group=G, merge=merge))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} G={G} merge={merge}")
     assert rn.workspace_clean()
 
 
@@ -70,12 +76,15 @@ def _edge_rows(S: int, K: int, rng) -> tuple[np.ndarray, np.ndarray]:
 
 @pytest.mark.parametrize("topk", [512, 1024, 2048])
 @pytest.mark.parametrize("S", [4096, 9001, 40000])
-@pytest.mark.parametrize("G", [0, 1, 4])
-def test_edge_cases(rn, topk, S, G):
+@pytest.mark.parametrize("G,merge", [(0, 0), (1, 0), (4, 1), (4, 2), (8, 2)])
+def test_edge_cases(rn, topk, S, G, merge):
+    # with G = 8 and K = 2048 the all-equal row keeps 8 x K candidates at one
+    # key, more than the leader's buffer: the cluster merge hands over to the
+    # workspace merge
     rng = np.random.default_rng(S + topk)
     x, lens = _edge_rows(S, topk, rng)
-    got = rn.run(x, lens, topk, options=rn.options(force_ctas_per_group=G))
-    assert_matches_oracle(x, lens, got, topk, label=f"edges S={S} K={topk} G={G}")
+    got = rn.run(x, lens, topk, options=rn.options(force_ctas_per_group=G, merge=merge))
+    assert_matches_oracle(x, lens, got, topk, label=f"edges S={S} K={topk} G={G} merge={merge}")
     assert rn.workspace_clean()
 
 

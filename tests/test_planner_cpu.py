@@ -13,10 +13,18 @@ def _built():
     build.build_library()
 
 
-def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024):
+def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None):
+    """A made-up device; clusters maps a cluster size to its co-resident count (none by default)."""
     p = sar.TopkDeviceProps()
     p.num_sms, p.ctas_per_sm, p.smem_per_cta, p.max_smem_optin = num_sms, occ, smem, optin
+    for c, n in (clusters or {}).items():
+        p.cluster_groups[c] = n
     return p
+
+
+def gb300_clusters():
+    # co-resident clusters of c CTAs of the kernel (one CTA per SM), as queried on a GB300
+    return {2: 76, 3: 46, 4: 36, 5: 28, 6: 23, 7: 15, 8: 15}
 
 
 def plan(p, rows, stride, next_n=1, topk=2048, **opt):
@@ -97,6 +105,64 @@ def test_split_gain_rule():
         else:
             g = min(16, 152 // rows, max(1, stride // 8192))
             assert g < 2 or stride <= 32768 or stride * (g - 1) // g < 90000
+
+
+def test_cluster_plans_for_the_five_workloads():
+    gb = props(clusters=gb300_clusters())
+    # 16 rows: clusters of 7 or 8 would not all be resident (15 of them), so 6
+    rc, pl = plan(gb, 16, 131072)
+    assert rc == 0 and pl.ctas_per_group == 6 and pl.cluster and not pl.cooperative and pl.grid == 96
+    rc, pl = plan(gb, 12, 131072)
+    assert rc == 0 and pl.ctas_per_group == 8 and pl.cluster and pl.grid == 96
+    rc, pl = plan(gb, 64, 163840, next_n=2, topk=1024)
+    assert rc == 0 and pl.ctas_per_group == 2 and pl.cluster and pl.grid == 128
+    rc, pl = plan(gb, 64, 32768)
+    assert rc == 0 and pl.ctas_per_group == 1 and not pl.cluster
+    rc, pl = plan(gb, 4096, 65536)
+    assert rc == 0 and pl.ctas_per_group == 1 and not pl.cluster and pl.grid == 152
+    # the workspace merge when asked for, and its own (larger) gain rule
+    rc, pl = plan(gb, 16, 131072, merge=1)
+    assert rc == 0 and pl.ctas_per_group == 9 and pl.cooperative and not pl.cluster
+    rc, pl = plan(gb, 64, 163840, next_n=2, topk=1024, merge=1)
+    assert rc == 0 and pl.ctas_per_group == 1
+
+
+def test_cluster_forcing_and_limits():
+    gb = props(clusters=gb300_clusters())
+    rc, pl = plan(gb, 5, 100000, force_ctas_per_group=3)
+    assert rc == 0 and pl.cluster and pl.grid == 15
+    rc, pl = plan(gb, 5, 100000, force_ctas_per_group=3, merge=1)
+    assert rc == 0 and not pl.cluster and pl.cooperative
+    assert plan(gb, 5, 100000, force_ctas_per_group=9, merge=2)[0] == sar.TOPK_ERR_PLAN
+    assert plan(props(), 5, 100000, force_ctas_per_group=2, merge=2)[0] == sar.TOPK_ERR_PLAN
+    assert plan(gb, 5, 100000, merge=3)[0] == sar.TOPK_ERR_INVALID_ARG
+    # a device without clusters falls back to the workspace merge by itself
+    rc, pl = plan(props(), 16, 131072)
+    assert rc == 0 and pl.ctas_per_group == 9 and not pl.cluster
+
+
+def test_cluster_invariants_on_random_shapes():
+    rng = random.Random(11)
+    for _ in range(3000):
+        sms, occ = rng.randint(8, 200), rng.randint(1, 2)
+        cl = {c: rng.choice([0, rng.randint(1, sms // c)]) for c in range(2, 9)}
+        rows = rng.choice([1, 2, rng.randint(1, 64), rng.randint(1, 5000)])
+        stride = rng.choice([4096, 32769, 131072, rng.randint(1, 1 << 22)])
+        force = rng.choice([0, 0, 2, 3, 8, 12])
+        merge = rng.choice([0, 0, 1, 2])
+        rc, pl = plan(props(num_sms=sms, occ=occ, clusters=cl), rows, stride, force_ctas_per_group=force,
+                      merge=merge)
+        if rc != 0:
+            assert rc == sar.TOPK_ERR_PLAN
+            assert force > 1 and (merge == 2 or force > sms * occ)
+            continue
+        G = pl.ctas_per_group
+        if pl.cluster:
+            assert 2 <= G <= 8 and merge != 1 and not pl.cooperative
+            assert 1 <= pl.num_groups <= min(rows, cl[G])
+        elif G > 1:
+            assert pl.cooperative and merge != 2 and pl.grid <= sms * occ
+        assert pl.grid == pl.num_groups * G
 
 
 def test_rejections():

@@ -26,8 +26,9 @@ def test_back_to_back_calls_share_one_workspace(rn):
     rn.sel.reset()
     for i in range(120):
         w, want = cases[i % len(cases)]
-        G = (0, 1, 2, 7)[(i // len(cases)) % 4]
-        got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(force_ctas_per_group=G))
+        G, merge = ((0, 0), (1, 0), (2, 1), (7, 2), (2, 2), (7, 1))[(i // len(cases)) % 6]
+        got = rn.run(w.logits, w.lengths, w.topk, w.next_n,
+                     options=rn.options(force_ctas_per_group=G, merge=merge))
         if i % 7 == 0 or i >= 112:
             assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, want=want,
                                   label=f"call {i} {w.name} G={G}")
@@ -35,14 +36,15 @@ def test_back_to_back_calls_share_one_workspace(rn):
     assert rn.sel.status() == 0
 
 
-def test_graph_replay_with_changing_inputs(rn):
+@pytest.mark.parametrize("merge", [1, 2])
+def test_graph_replay_with_changing_inputs(rn, merge):
     torch = rn.torch
     sar = rn.sar
     rows, S, K = 12, 131072, 2048
     xs = torch.zeros((rows, S), dtype=torch.float32, device=rn.dev)
     ls = torch.zeros(rows, dtype=torch.int32, device=rn.dev)
     out = torch.zeros((rows, K), dtype=torch.int32, device=rn.dev)
-    opts = rn.options(force_ctas_per_group=6)
+    opts = rn.options(force_ctas_per_group=6, merge=merge)
     # first call outside capture (device properties are cached on it)
     assert sar.topk_ragged_ex(xs, S, ls, rows, 1, K, out, rn.sel.workspace, None, opts) == 0
     torch.cuda.synchronize()
@@ -68,12 +70,12 @@ def test_timed_out_group_wait_reports_and_recovers(rn):
     """A CTA that never arrives makes its partners' bounded waits run out."""
     w = workloads.make("long_coop", 4)
     rn.sel.reset()
-    opts = rn.options(force_ctas_per_group=2, inject_skip_arrival=1, barrier_timeout_us=20000)
+    opts = rn.options(force_ctas_per_group=2, merge=1, inject_skip_arrival=1, barrier_timeout_us=20000)
     rn.run(w.logits, w.lengths, w.topk, options=opts, check_status=False)
     st = rn.sel.status()
     assert st & rn.sar.TOPK_DEV_BARRIER_TIMEOUT, f"status {st:#x}"
     # the context is still usable; re-initialising the workspace restores service
     rn.sel.reset()
-    got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=2))
+    got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=2, merge=1))
     assert_matches_oracle(w.logits, w.lengths, got, w.topk, label="after recovery")
     assert rn.workspace_clean()
