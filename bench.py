@@ -206,6 +206,15 @@ class GpuBench:
         if rc != 0:
             raise RuntimeError(f"topk_ragged: {self.sar.topk_status_string(rc)}")
 
+    def plan(self, w) -> dict:
+        """The launch shape the planner picks for the workload (as topk_ragged does)."""
+        props = self.sar.topk_query_device(self.dev.index)
+        rc, pl = self.sar.topk_make_plan(props, w.num_rows, w.row_stride, w.next_n, w.topk)
+        if rc != 0:
+            return {"error": self.sar.topk_status_string(rc)}
+        merge = "cluster" if pl.cluster else ("workspace" if pl.ctas_per_group > 1 else "none")
+        return {"ctas_per_row": pl.ctas_per_group, "grid": pl.grid, "merge": merge}
+
     def flush_l2(self):
         """Evicts the inputs from L2: writes a buffer larger than L2, then reads it
         back, so L2 holds clean lines and no write-back of the flush itself lands
@@ -375,7 +384,7 @@ def run_ours(args) -> None:
         entry = {"rows_per_s": world * w.num_rows / (ms * 1e-3), "us_per_call": ms * 1e3,
                  "us_per_call_median": r["ms_median"] * 1e3, "effective_gbs": gbs,
                  "frac_of_hbm_peak": gbs / peak, "frac_of_8tbs_spec": gbs / 8000.0,
-                 "valid_bytes": vbytes, "steps": steps}
+                 "valid_bytes": vbytes, "steps": steps, "plan": gb.plan(w)}
         if rank == 0 and not args.no_cpu:
             budget = args.cpu_budget if name == HEADLINE else args.cpu_budget / 2
             cap_rows = None if name != "prefill" else 256

@@ -69,7 +69,6 @@ struct __align__(128) Smem {
   float thr_f;
   int find_b, find_gt;
   int abort, last, off, take;
-  int first_issued;
   int n_list;
   uint32_t red;
   uint32_t sel_T;
@@ -120,7 +119,7 @@ __device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
                                               unsigned long long* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
@@ -211,10 +210,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(unsigned long long* bar, u
   return ok != 0;
 }
 
-// Hardware barrier over every thread of the cluster; used once, at kernel
-// start, where every thread of every CTA reaches it.
-__device__ __forceinline__ void cluster_barrier_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// The hardware cluster barrier, split: every thread of every CTA arrives once
+// at kernel start (after the merge barriers are initialised); a thread that
+// will touch another CTA's shared memory waits first, which completes once
+// every thread of the cluster has arrived (threads that exited count as
+// arrived). Warp-uniform in both halves.
+__device__ __forceinline__ void cluster_arrive_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_all() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
@@ -791,30 +797,30 @@ __device__ __forceinline__ bool get_row(const Params& p, const Smem& s, int64_t 
   return true;
 }
 
-// The copy warp issues the first chunk of the CTA's first row at kernel start,
-// before the consumers have filled the length cache (in a cluster launch, right
-// after the cluster barrier). With whole rows per CTA
+// The copy warp issues the first chunk of the CTA's first row early. With whole
+// rows per CTA it does so at kernel start, before the length cache is filled:
 // the copy window is sized by the row stride, which covers the first chunk of
-// any length: it becomes that row's chunk 0, or a chunk the consumers discard
-// if the row needs no streaming. When a row is split, the copy thread reads the
-// row's length itself and issues chunk 0 of its part, if it has one. Returns
-// whether a copy was issued.
-__device__ __noinline__ bool producer_first(const Params& p, Smem& s, int g, int m) {
-  if (p.G == 1) {
-    const float* rowp = p.logits + static_cast<int64_t>(g) * p.stride;
-    const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
-    const int64_t ws = -mis;
-    const int64_t wend = ws + ((p.stride - ws + 3) & ~static_cast<int64_t>(3));
-    const int64_t we = min(ws + kChunk, wend);
-    const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
-    fence_proxy_async();
-    mbar_expect_tx(&s.full[0], bytes);
-    bulk_copy_g2s(s.stage[0], rowp + ws, bytes, &s.full[0]);
-    return true;
-  }
+// any length; it becomes that row's chunk 0, or a chunk the consumers discard
+// if the row needs no streaming.
+__device__ __noinline__ void producer_first_whole(const Params& p, Smem& s, int g) {
+  const float* rowp = p.logits + static_cast<int64_t>(g) * p.stride;
+  const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
+  const int64_t ws = -mis;
+  const int64_t wend = ws + ((p.stride - ws + 3) & ~static_cast<int64_t>(3));
+  const int64_t we = min(ws + kChunk, wend);
+  const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
+  fence_proxy_async();
+  mbar_expect_tx(&s.full[0], bytes);
+  bulk_copy_g2s(s.stage[0], rowp + ws, bytes, &s.full[0]);
+}
+
+// When rows are split, the copy thread reads the first row's length itself
+// (the read is in flight across the start-up barriers) and issues chunk 0 of
+// its part, if it has one. Returns whether a copy was issued.
+__device__ __noinline__ bool producer_first_split(const Params& p, Smem& s, int g, int m, int32_t raw_len) {
   if (g >= p.num_rows) return false;
   RowWin w;
-  row_window(p, g, clamp_len(p, __ldg(p.lengths + g)), m, w);
+  row_window(p, g, clamp_len(p, raw_len), m, w);
   if (w.nch == 0) return false;
   const int we = min(w.wstart + kChunk, w.wend);
   const uint32_t bytes = static_cast<uint32_t>(we - w.wstart) * 4u;
@@ -1541,9 +1547,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
   const int g = static_cast<int>(blockIdx.x) / p.G;
   const int m = static_cast<int>(blockIdx.x) % p.G;
 
+  int32_t len0 = 0;     // copy thread, split rows: the first row's length
+  bool first = false;   // copy thread: chunk 0 of the first row is issued
   if (tid == kThreads) {
     // the copy thread sets up the ring and, with whole rows per CTA, issues
     // the first copy right away; everyone else meets it at the barrier below
+    if (p.G > 1 && g < p.num_rows) len0 = __ldg(p.lengths + g);
     s.abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1u);
@@ -1554,8 +1563,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
       mbar_init(&s.xbar[1], static_cast<uint32_t>(p.G));
     }
     fence_mbar_init();
-    // a cluster launch issues no copy before every CTA of its cluster runs
-    s.first_issued = (!p.cluster && producer_first(p, s, g, m)) ? 1 : 0;
+    if (p.G == 1) {
+      producer_first_whole(p, s, g);
+      first = true;
+    }
   }
   if (tid < kThreads) {
     reset_row_state(s);
@@ -1564,15 +1575,16 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
       s.lens[k] = (r < p.num_rows) ? clamp_len(p, p.lengths[r]) : 0;
     }
   }
+  // the other CTAs of the cluster may reach into this one's shared memory only
+  // after every thread has arrived here (their wait comes before their first
+  // merge); the copies fill this CTA's own shared memory and need no wait
+  if (p.cluster) cluster_arrive_all();
   __syncthreads();
-  if (p.cluster) {
-    // every CTA of the cluster runs, and its merge barriers exist, before any
-    // CTA copies into cluster shared memory or arrives on another's barrier
-    cluster_barrier_all();
-    if (tid == kThreads) s.first_issued = producer_first(p, s, g, m) ? 1 : 0;
-  }
   if (tid >= kThreads) {
-    if (tid == kThreads) producer_loop(p, s, g, m, s.first_issued != 0);
+    if (tid == kThreads) {
+      if (p.G > 1) first = producer_first_split(p, s, g, m, len0);
+      producer_loop(p, s, g, m, first);
+    }
     return;
   }
 
@@ -1580,6 +1592,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
   uint32_t q = 0;  // chunks consumed
   uint32_t epoch = 0;
   uint32_t xph = 0;       // cluster merge syncs passed
+  bool cluster_ready = false;  // this thread passed the start-up cluster barrier
   bool used_ws = false;   // some row of a split group went through the workspace merge
   bool first_barrier = true;
   bool aborted = false;
@@ -1647,6 +1660,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
     if (p.G == 1) {
       finish_local(s, p, w.r);
     } else if (p.cluster) {
+      if (!cluster_ready) {
+        cluster_wait_all();
+        cluster_ready = true;
+      }
       const int mode = cluster_merge(s, p, m, xph);
       if (mode == 1) {
         finish_local(s, p, w.r);
@@ -1670,6 +1687,7 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
   }
   if (p.cluster) {
     // no CTA leaves while another may still reach into its shared memory
+    if (!cluster_ready) cluster_wait_all();
     if (!cluster_sync(s, p, xph)) return;
   }
   if (p.G > 1 && (!p.cluster || used_ws)) {
