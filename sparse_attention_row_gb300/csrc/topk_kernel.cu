@@ -7,7 +7,7 @@
 // slots through "empty" mbarriers), so each logit crosses HBM exactly once.
 //
 // Filtering: the first staged chunk of a row is histogrammed on the top 12 bits
-// of the keys and seeds a threshold aimed at about 1.5 K survivors over the
+// of the keys and seeds a threshold aimed at about 1.25 K survivors over the
 // whole row. Every later element costs one fp32 compare against that threshold;
 // only survivors become (key, index) candidates in shared memory. At the end of
 // the row the seed is verified: if fewer than K elements reached it, the row is
@@ -1621,13 +1621,13 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
         s.abort = 1;
         atomicOr(p.status, 0x4u);
       } else if (j == 0 && span > K) {
-        // seed: histogram the first chunk, aim the threshold at ~1.5 K survivors
+        // seed: histogram the first chunk, aim the threshold at ~1.25 K survivors
         // over the window (exactly K when the window is this one chunk)
         hist_chunk(s, s.stage[slot], ws, nvec, w.lo, w.hi);
         const int in_chunk = min(w.hi, we) - max(w.lo, ws);
         int target = K;
         if (w.nch > 1) {
-          const int64_t tt = (3ll * K * in_chunk + 2ll * span - 1) / (2ll * span);
+          const int64_t tt = (5ll * K * in_chunk + 4ll * span - 1) / (4ll * span);
           target = static_cast<int>(tt < 1 ? 1 : tt);
         }
         target = min(target, in_chunk);
