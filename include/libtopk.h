@@ -80,6 +80,9 @@ typedef struct {
    * 1 = through the workspace, with a grid-level barrier (any G); 2 = inside a
    * thread-block cluster, through its distributed shared memory (G <= 8). */
   int merge;
+  /* CTA shape. 0 = planner decides; 1 = one CTA of 24 consumer warps per SM;
+   * 2 = two CTAs of 12 consumer warps per SM (whole rows only). */
+  int shape;
 } topk_options;
 
 /* Properties of a device as the planner sees them. */
@@ -91,6 +94,8 @@ typedef struct {
   /* cluster_groups[c], c = 2..8: clusters of c CTAs of the kernel that can be
    * resident at once (0 = none; entries 0 and 1 are unused). */
   int cluster_groups[9];
+  int pair_smem_per_cta; /* the same for the paired shape (two CTAs per SM) */
+  int pair_ctas_per_sm;
 } topk_device_props;
 
 /* A launch configuration. */
@@ -102,6 +107,7 @@ typedef struct {
   int smem_bytes;     /* dynamic shared memory per CTA */
   int cooperative;    /* 1 when the CTAs of a group wait on one another through the workspace */
   int cluster;        /* 1 when the CTAs of a group form a cluster and merge in its shared memory */
+  int shape;          /* 1 = one CTA of 24 consumer warps per SM, 2 = two CTAs of 12 per SM */
 } topk_plan;
 
 /*
@@ -187,9 +193,10 @@ int topk_get_status(const void* workspace, void* stream, uint32_t* device_status
 const char* topk_status_string(int code);
 
 /*
- * Fills *props for `device`: SM count, opt-in shared memory per block, the
- * kernel's shared memory and its occupancy (queried for the exact kernel, as
- * the vLLM PR #41189 page's "Implementation breakdown" item 1 requires).
+ * Fills *props for `device`: SM count, opt-in shared memory per block, and for
+ * each CTA shape of the kernel its shared memory and occupancy (queried for
+ * the exact kernel, as the vLLM PR #41189 page's "Implementation breakdown"
+ * item 1 requires), plus the co-resident cluster counts.
  */
 int topk_query_device(int device, topk_device_props* props);
 

@@ -41,6 +41,10 @@ TOPK_MERGE_AUTO = 0
 TOPK_MERGE_WORKSPACE = 1
 TOPK_MERGE_CLUSTER = 2
 
+TOPK_SHAPE_AUTO = 0
+TOPK_SHAPE_WIDE = 1
+TOPK_SHAPE_PAIR = 2
+
 TOPK_DEV_LENGTH_CLAMPED = 0x1
 TOPK_DEV_BARRIER_TIMEOUT = 0x2
 TOPK_DEV_STAGE_TIMEOUT = 0x4
@@ -62,7 +66,8 @@ class TopkOptions(ctypes.Structure):
                 ("inject_skip_arrival", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t),
                 ("max_ctas", ctypes.c_int),
-                ("merge", ctypes.c_int)]
+                ("merge", ctypes.c_int),
+                ("shape", ctypes.c_int)]
 
 
 class TopkDeviceProps(ctypes.Structure):
@@ -70,7 +75,9 @@ class TopkDeviceProps(ctypes.Structure):
                 ("max_smem_optin", ctypes.c_int),
                 ("smem_per_cta", ctypes.c_int),
                 ("ctas_per_sm", ctypes.c_int),
-                ("cluster_groups", ctypes.c_int * 9)]
+                ("cluster_groups", ctypes.c_int * 9),
+                ("pair_smem_per_cta", ctypes.c_int),
+                ("pair_ctas_per_sm", ctypes.c_int)]
 
 
 class TopkPlan(ctypes.Structure):
@@ -80,7 +87,8 @@ class TopkPlan(ctypes.Structure):
                 ("threads", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int),
                 ("cooperative", ctypes.c_int),
-                ("cluster", ctypes.c_int)]
+                ("cluster", ctypes.c_int),
+                ("shape", ctypes.c_int)]
 
 
 def library_path() -> str:

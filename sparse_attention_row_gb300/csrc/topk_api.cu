@@ -58,18 +58,25 @@ int query_device_locked(int device, topk_device_props* out) {
             cudaSuccess) {
       rc = TOPK_ERR_CUDA;
     }
-    p.smem_per_cta = static_cast<int>(ltk::kernel_smem_bytes());
+    p.smem_per_cta = static_cast<int>(ltk::wide::kernel_smem_bytes());
+    p.pair_smem_per_cta = static_cast<int>(ltk::pair::kernel_smem_bytes());
     if (rc == TOPK_OK && p.smem_per_cta <= p.max_smem_optin) {
-      if (ltk::kernel_configure() != cudaSuccess || ltk::kernel_occupancy(&p.ctas_per_sm) != cudaSuccess)
+      if (ltk::wide::kernel_configure() != cudaSuccess ||
+          ltk::wide::kernel_occupancy(&p.ctas_per_sm) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
       for (int c = 2; rc == TOPK_OK && c <= ltk::kMaxCluster; ++c) {
-        if (ltk::kernel_max_clusters(c, &p.cluster_groups[c]) != cudaSuccess) {
+        if (ltk::wide::kernel_max_clusters(c, &p.cluster_groups[c]) != cudaSuccess) {
           cudaGetLastError();  // a device without clusters: no cluster merge is planned
           p.cluster_groups[c] = 0;
         }
       }
     } else if (rc == TOPK_OK) {
       p.ctas_per_sm = 0;  // the kernel cannot be resident; planning reports TOPK_ERR_PLAN
+    }
+    if (rc == TOPK_OK && p.pair_smem_per_cta <= p.max_smem_optin) {
+      if (ltk::pair::kernel_configure() != cudaSuccess ||
+          ltk::pair::kernel_occupancy(&p.pair_ctas_per_sm) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
     }
     if (prev != device) cudaSetDevice(prev);
     if (rc != TOPK_OK) {
@@ -201,7 +208,7 @@ int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengt
                                         : ltk::kDefaultTimeoutNs;
   p.inject = opt.inject_skip_arrival;
   p.cluster = plan.cluster;
-  if (ltk::launch_topk(p, plan.grid, plan.cooperative != 0, static_cast<cudaStream_t>(stream)) !=
+  if (ltk::launch_shape(plan.shape, p, plan.grid, plan.cooperative != 0, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess) {
     cudaGetLastError();
     return TOPK_ERR_CUDA;

@@ -6,14 +6,8 @@
 
 namespace ltk {
 
-// CTA shape and shared-memory staging.
-constexpr int kThreads = 768;          // consumer threads per CTA (24 warps)
-constexpr int kWarps = kThreads / 32;
-constexpr int kCtaThreads = kThreads + 32;  // plus one copy-issuing warp
-constexpr int kChunk = 6144;           // fp32 elements per staging slot (24 KB)
-constexpr int kStages = 4;             // staging slots in flight per CTA (96 KB)
+// Shared by both CTA shapes of the kernel (see topk_kernel.cu for the shapes).
 constexpr int kBins = 4096;            // 12-bit radix digits
-constexpr int kBufCap = 12288;         // candidate (key, index) pairs kept per CTA
 constexpr int kMaxTopK = 2048;
 constexpr int kMaxGroup = 16;          // CTAs that may split one row
 constexpr int kMaxCluster = 8;         // CTAs of a group that may form one thread-block cluster
@@ -23,10 +17,16 @@ constexpr int kMinSpan = 8192;         // fewest elements per CTA when a row is 
 constexpr int64_t kDefaultLongRowThreshold = 32768;
 constexpr int64_t kSplitGain = 90000;         // elements a workspace-merged split must save per CTA (measured)
 constexpr int64_t kSplitGainCluster = 24000;  // elements a cluster-merged split must save per CTA
+constexpr int64_t kPairRowsPerSm = 4;         // rows per SM from which the paired shape is planned
 constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
-static_assert(kMaxTopK + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");
-static_assert(kChunk % (4 * kThreads) == 0, "a chunk is a whole number of float4 per thread");
+// CTA shapes. kShapeWide: one CTA of 24 consumer warps per SM (any row split).
+// kShapePair: two CTAs of 12 consumer warps per SM, whole rows only; with many
+// rows per SM one CTA's row finish overlaps the other's streaming.
+constexpr int kShapeWide = 1;
+constexpr int kShapePair = 2;
+constexpr int kWideCtaThreads = 800;  // 24 consumer warps + the copy warp
+constexpr int kPairCtaThreads = 416;  // 12 consumer warps + the copy warp
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.
@@ -62,10 +62,23 @@ struct Params {
   int cluster;       // 1: the G CTAs of a group are one cluster and merge through its shared memory
 };
 
-size_t kernel_smem_bytes();
-cudaError_t kernel_configure();                 // sets the shared-memory opt-in (current device)
-cudaError_t kernel_occupancy(int* ctas_per_sm);  // occupancy of the exact kernel
-cudaError_t kernel_max_clusters(int cluster_size, int* clusters);  // co-resident clusters of that size
-cudaError_t launch_topk(const Params& p, int grid, bool cooperative, cudaStream_t stream);
+// Host side of one compiled shape of the kernel (namespace ltk::wide or ltk::pair).
+#define LTK_DECLARE_SHAPE(NS)                                                                  \
+  namespace NS {                                                                               \
+  int kernel_threads();                                                                        \
+  size_t kernel_smem_bytes();                                                                  \
+  cudaError_t kernel_configure();                  /* shared-memory opt-in (current device) */ \
+  cudaError_t kernel_occupancy(int* ctas_per_sm);  /* occupancy of the exact kernel */         \
+  cudaError_t kernel_max_clusters(int cluster_size, int* clusters);                            \
+  cudaError_t launch_topk(const Params& p, int grid, bool cooperative, cudaStream_t stream);   \
+  }
+LTK_DECLARE_SHAPE(wide)
+LTK_DECLARE_SHAPE(pair)
+#undef LTK_DECLARE_SHAPE
+
+inline cudaError_t launch_shape(int shape, const Params& p, int grid, bool cooperative, cudaStream_t stream) {
+  return shape == kShapePair ? pair::launch_topk(p, grid, cooperative, stream)
+                             : wide::launch_topk(p, grid, cooperative, stream);
+}
 
 }  // namespace ltk

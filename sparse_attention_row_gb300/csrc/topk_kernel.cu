@@ -43,7 +43,40 @@
 
 #include "topk_internal.h"
 
+// This file is compiled twice: as is (the wide CTA shape, namespace
+// ltk::wide) and from topk_kernel_pair.cu with LTK_SHAPE_PAIR set (two
+// narrower CTAs per SM, namespace ltk::pair).
+#ifndef LTK_SHAPE_PAIR
+#define LTK_SHAPE_PAIR 0
+#endif
+#if LTK_SHAPE_PAIR
+#define LTK_SHAPE_NS pair
+#else
+#define LTK_SHAPE_NS wide
+#endif
+
 namespace ltk {
+namespace LTK_SHAPE_NS {
+
+#if LTK_SHAPE_PAIR
+constexpr int kThreads = 384;   // consumer threads per CTA (12 warps)
+constexpr int kChunk = 3072;    // fp32 elements per staging slot (12 KB)
+constexpr int kStages = 3;      // staging slots per CTA (36 KB)
+constexpr int kBufCap = 6144;   // candidate (key, index) pairs kept per CTA
+constexpr int kMinBlocks = 2;   // CTAs per SM the shape is built for
+#else
+constexpr int kThreads = 768;   // consumer threads per CTA (24 warps)
+constexpr int kChunk = 6144;    // fp32 elements per staging slot (24 KB)
+constexpr int kStages = 4;      // staging slots per CTA (96 KB)
+constexpr int kBufCap = 12288;  // candidate (key, index) pairs kept per CTA
+constexpr int kMinBlocks = 1;
+#endif
+constexpr int kWarps = kThreads / 32;
+constexpr int kCtaThreads = kThreads + 32;  // plus one copy-issuing warp
+static_assert(kCtaThreads == (LTK_SHAPE_PAIR ? kPairCtaThreads : kWideCtaThreads), "shape constants agree");
+
+static_assert(kMaxTopK + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");
+static_assert(kChunk % (4 * kThreads) == 0, "a chunk is a whole number of float4 per thread");
 
 struct __align__(128) Smem {
   float stage[kStages][kChunk];   // staging ring (bulk-copy destination)
@@ -1540,7 +1573,7 @@ __device__ __noinline__ int cluster_merge(Smem& s, const Params& p, int m, uint3
 
 // ------------------------------------------------------------------- kernel
 
-__global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Params p) {
+__global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(const Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
@@ -1717,6 +1750,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1) topk_ragged_kernel(const Param
 
 // ---------------------------------------------------------------- host side
 
+int kernel_threads() { return kCtaThreads; }
+
 size_t kernel_smem_bytes() { return sizeof(Smem); }
 
 cudaError_t kernel_configure() {
@@ -1767,4 +1802,5 @@ cudaError_t launch_topk(const Params& p, int grid, bool cooperative, cudaStream_
   return cudaLaunchKernelEx(&cfg, topk_ragged_kernel, p);
 }
 
+}  // namespace LTK_SHAPE_NS
 }  // namespace ltk

@@ -106,7 +106,7 @@ extern "C" int topk_ragged_static(const float* logits, int64_t row_stride, const
   p.timeout_ns = ltk::kDefaultTimeoutNs;
   p.inject = 0;
   p.cluster = plan.cluster;
-  if (ltk::launch_topk(p, plan.grid, plan.cooperative != 0, s) != cudaSuccess) {
+  if (ltk::launch_shape(plan.shape, p, plan.grid, plan.cooperative != 0, s) != cudaSuccess) {
     cudaGetLastError();
     return TOPK_ERR_CUDA;
   }

@@ -26,6 +26,15 @@ def test_workloads_small_auto(rn, name, rows):
     assert rn.workspace_clean()
 
 
+@pytest.mark.parametrize("name,rows", SMALL)
+def test_workloads_small_paired_shape(rn, name, rows):
+    """The paired shape (two CTAs of 12 consumer warps per SM), forced on every workload."""
+    w = workloads.make(name, rows)
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=2))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} paired")
+    assert rn.workspace_clean()
+
+
 # merge 1: the CTAs of a row merge through the workspace (grid barrier);
 # merge 2: they form a thread-block cluster and merge in its shared memory
 SPLITS = [(1, 0), (2, 1), (2, 2), (3, 1), (3, 2), (5, 2), (8, 2), (9, 1), (16, 1)]
@@ -76,15 +85,15 @@ def _edge_rows(S: int, K: int, rng) -> tuple[np.ndarray, np.ndarray]:
 
 @pytest.mark.parametrize("topk", [512, 1024, 2048])
 @pytest.mark.parametrize("S", [4096, 9001, 40000])
-@pytest.mark.parametrize("G,merge", [(0, 0), (1, 0), (4, 1), (4, 2), (8, 2)])
-def test_edge_cases(rn, topk, S, G, merge):
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 0), (0, 0, 2), (4, 1, 0), (4, 2, 0), (8, 2, 0)])
+def test_edge_cases(rn, topk, S, G, merge, shape):
     # with G = 8 and K = 2048 the all-equal row keeps 8 x K candidates at one
     # key, more than the leader's buffer: the cluster merge hands over to the
     # workspace merge
     rng = np.random.default_rng(S + topk)
     x, lens = _edge_rows(S, topk, rng)
-    got = rn.run(x, lens, topk, options=rn.options(force_ctas_per_group=G, merge=merge))
-    assert_matches_oracle(x, lens, got, topk, label=f"edges S={S} K={topk} G={G} merge={merge}")
+    got = rn.run(x, lens, topk, options=rn.options(force_ctas_per_group=G, merge=merge, shape=shape))
+    assert_matches_oracle(x, lens, got, topk, label=f"edges S={S} K={topk} G={G} merge={merge} shape={shape}")
     assert rn.workspace_clean()
 
 
@@ -132,6 +141,9 @@ def test_many_rows_per_cta_and_per_group(rn):
     # 4 CTAs: 75 rows each, beyond the shared-memory length cache
     got = rn.run(x, lens, 1024, options=rn.options(max_ctas=4, force_ctas_per_group=1))
     assert_matches_oracle(x, lens, got, 1024, label="G=1 persistent")
+    # the paired shape, 3 CTAs: 100 rows each
+    got = rn.run(x, lens, 1024, options=rn.options(max_ctas=3, shape=2))
+    assert_matches_oracle(x, lens, got, 1024, label="paired persistent")
     # 2 groups of 4 CTAs: every group loops over 150 rows, reusing its workspace
     got = rn.run(x, lens, 1024, options=rn.options(max_ctas=8, force_ctas_per_group=4))
     assert_matches_oracle(x, lens, got, 1024, label="G=4 persistent")

@@ -13,13 +13,18 @@ def _built():
     build.build_library()
 
 
-def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None):
-    """A made-up device; clusters maps a cluster size to its co-resident count (none by default)."""
+def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, pair=(0, 0)):
+    """A made-up device; clusters maps a cluster size to its co-resident count (none by default);
+    pair is (shared memory, CTAs per SM) of the paired shape (absent by default)."""
     p = sar.TopkDeviceProps()
     p.num_sms, p.ctas_per_sm, p.smem_per_cta, p.max_smem_optin = num_sms, occ, smem, optin
     for c, n in (clusters or {}).items():
         p.cluster_groups[c] = n
+    p.pair_smem_per_cta, p.pair_ctas_per_sm = pair
     return p
+
+
+GB300_PAIR = (113536, 2)
 
 
 def gb300_clusters():
@@ -163,6 +168,31 @@ def test_cluster_invariants_on_random_shapes():
         elif G > 1:
             assert pl.cooperative and merge != 2 and pl.grid <= sms * occ
         assert pl.grid == pl.num_groups * G
+
+
+def test_paired_shape():
+    gb = props(clusters=gb300_clusters(), pair=GB300_PAIR)
+    rc, pl = plan(gb, 4096, 65536)  # prefill: 27 rows per SM
+    assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1 and pl.grid == 304 and pl.threads == 416
+    assert pl.smem_bytes == GB300_PAIR[0] and not pl.cooperative and not pl.cluster
+    rc, pl = plan(gb, 64, 32768)  # decode: one row per CTA, the wide shape
+    assert rc == 0 and pl.shape == 1 and pl.grid == 64 and pl.threads == 800
+    rc, pl = plan(gb, 4 * 152 - 1, 65536)
+    assert rc == 0 and pl.shape == 1
+    rc, pl = plan(gb, 4 * 152, 65536)
+    assert rc == 0 and pl.shape == 2 and pl.grid == 304
+    rc, pl = plan(gb, 8, 4096, topk=512, shape=2)  # forced
+    assert rc == 0 and pl.shape == 2 and pl.grid == 8
+    rc, pl = plan(gb, 4096, 65536, shape=1)
+    assert rc == 0 and pl.shape == 1 and pl.grid == 152
+    rc, pl = plan(gb, 4096, 65536, max_ctas=100)
+    assert rc == 0 and pl.shape == 2 and pl.grid == 100
+    # the paired shape never splits a row, and needs a device that holds two of it
+    assert plan(gb, 16, 131072, shape=2, force_ctas_per_group=4)[0] == sar.TOPK_ERR_INVALID_ARG
+    rc, pl = plan(gb, 16, 131072, shape=2)
+    assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1
+    assert plan(props(), 8, 4096, shape=2)[0] == sar.TOPK_ERR_PLAN
+    assert plan(gb, 8, 4096, shape=3)[0] == sar.TOPK_ERR_INVALID_ARG
 
 
 def test_rejections():
