@@ -6,8 +6,9 @@
  * serves DSA models in long-context inference). Every row r of a logits matrix
  * has its own valid length len_r. For every row, the library returns the
  * indices of its topk largest values among x[r, 0:len_r]. The per-row lengths
- * and the TopK template (512 / 1024 / 2048) follow the persistent_topk launcher
- * excerpt on the vLLM PR #41189 page ("Implementation breakdown"). MTP layouts,
+ * and the TopK values the pages' kernel is built for (512 / 1024 / 2048) follow
+ * the persistent_topk launcher excerpt on the vLLM PR #41189 page
+ * ("Implementation breakdown"); here any TopK from 1 to 4096 is accepted. MTP layouts,
  * where a request contributes next_n adjacent rows, each with its own length,
  * follow the vLLM PR #54110 page ("Implementation breakdown" item 2: next_n is
  * the second dimension of a 2-D lengths tensor).
@@ -46,7 +47,7 @@ extern "C" {
 typedef enum {
   TOPK_OK = 0,
   TOPK_ERR_INVALID_ARG = 1,         /* null pointer, negative size, next_n not dividing num_rows ... */
-  TOPK_ERR_UNSUPPORTED_TOPK = 2,    /* topk not in {512, 1024, 2048} */
+  TOPK_ERR_UNSUPPORTED_TOPK = 2,    /* topk outside [1, 4096] (or above 2048 with the paired shape) */
   TOPK_ERR_MISALIGNED = 3,          /* logits/lengths/out_idx not 4-byte, workspace not 16-byte aligned */
   TOPK_ERR_WORKSPACE_TOO_SMALL = 4, /* topk_options.workspace_bytes below topk_workspace_size */
   TOPK_ERR_CUDA = 5,                /* a CUDA runtime call failed (launch, query, copy) */
@@ -143,7 +144,8 @@ int topk_workspace_init(void* workspace, size_t bytes, void* stream);
  *              clamped and flagged with TOPK_DEV_LENGTH_CLAMPED.
  *   num_rows   rows; 0 is a no-op.
  *   next_n     rows per request (MTP); must divide num_rows.
- *   topk       512, 1024 or 2048.
+ *   topk       1..4096, any value (the pages' kernel is built for 512, 1024 and
+ *              2048; here TopK is a run-time argument of one kernel).
  *   out_idx    int32 [num_rows, topk], written in full.
  *   workspace  at least topk_workspace_size bytes, 16-byte aligned, zeroed once
  *              by topk_workspace_init. Calls that may run concurrently on the

@@ -41,7 +41,7 @@
 
 namespace {
 
-bool topk_supported(int topk) { return topk == 512 || topk == 1024 || topk == 2048; }
+bool topk_supported(int topk) { return topk >= 1 && topk <= ltk::kWideMaxTopK; }
 
 }  // namespace
 
@@ -105,10 +105,12 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   bool pair = false;
   if (G == 1) {
     if (shape == ltk::kShapePair) {
+      if (topk > ltk::kPairMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
       if (props->pair_ctas_per_sm < 1 || props->pair_smem_per_cta > props->max_smem_optin) return TOPK_ERR_PLAN;
       pair = true;
     } else if (shape == 0) {
-      pair = props->pair_ctas_per_sm >= 2 && props->pair_smem_per_cta <= props->max_smem_optin &&
+      pair = topk <= ltk::kPairMaxTopK && props->pair_ctas_per_sm >= 2 &&
+             props->pair_smem_per_cta <= props->max_smem_optin &&
              num_rows >= ltk::kPairRowsPerSm * props->num_sms;
     }
   }

@@ -111,7 +111,7 @@ const char* topk_status_string(int code) {
   switch (code) {
     case TOPK_OK: return "ok";
     case TOPK_ERR_INVALID_ARG: return "invalid argument";
-    case TOPK_ERR_UNSUPPORTED_TOPK: return "topk must be 512, 1024 or 2048";
+    case TOPK_ERR_UNSUPPORTED_TOPK: return "topk must be between 1 and 4096 (2048 for the paired shape)";
     case TOPK_ERR_MISALIGNED: return "misaligned pointer";
     case TOPK_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case TOPK_ERR_CUDA: return "CUDA runtime error";
@@ -166,7 +166,7 @@ int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengt
                    const topk_options* options) {
   if (num_rows < 0 || row_stride < 1 || next_n < 1 || (num_rows % next_n) != 0)
     return TOPK_ERR_INVALID_ARG;
-  if (!(topk == 512 || topk == 1024 || topk == 2048)) return TOPK_ERR_UNSUPPORTED_TOPK;
+  if (topk < 1 || topk > ltk::kWideMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
   if (num_rows == 0) return TOPK_OK;
   if (logits == nullptr || lengths == nullptr || out_idx == nullptr || workspace == nullptr)
     return TOPK_ERR_INVALID_ARG;

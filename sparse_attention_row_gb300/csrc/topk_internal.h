@@ -8,7 +8,9 @@ namespace ltk {
 
 // Shared by both CTA shapes of the kernel (see topk_kernel.cu for the shapes).
 constexpr int kBins = 4096;            // 12-bit radix digits
-constexpr int kMaxTopK = 2048;
+constexpr int kListCap = 2048;         // entries of the threshold bin listed by the row finish
+constexpr int kWideMaxTopK = 4096;     // largest TopK of the wide shape (buffer: TopK + a chunk)
+constexpr int kPairMaxTopK = 2048;     // largest TopK of the paired shape
 constexpr int kMaxGroup = 16;          // CTAs that may split one row
 constexpr int kMaxCluster = 8;         // CTAs of a group that may form one thread-block cluster
 constexpr int kLenCache = 64;          // row lengths cached in shared memory

@@ -59,12 +59,14 @@ namespace ltk {
 namespace LTK_SHAPE_NS {
 
 #if LTK_SHAPE_PAIR
+constexpr int kTopKMax = kPairMaxTopK;
 constexpr int kThreads = 384;   // consumer threads per CTA (12 warps)
 constexpr int kChunk = 3072;    // fp32 elements per staging slot (12 KB)
 constexpr int kStages = 3;      // staging slots per CTA (36 KB)
 constexpr int kBufCap = 6144;   // candidate (key, index) pairs kept per CTA
 constexpr int kMinBlocks = 2;   // CTAs per SM the shape is built for
 #else
+constexpr int kTopKMax = kWideMaxTopK;
 constexpr int kThreads = 768;   // consumer threads per CTA (24 warps)
 constexpr int kChunk = 6144;    // fp32 elements per staging slot (24 KB)
 constexpr int kStages = 4;      // staging slots per CTA (96 KB)
@@ -75,7 +77,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kCtaThreads = kThreads + 32;  // plus one copy-issuing warp
 static_assert(kCtaThreads == (LTK_SHAPE_PAIR ? kPairCtaThreads : kWideCtaThreads), "shape constants agree");
 
-static_assert(kMaxTopK + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");
+static_assert(kTopKMax + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");
 static_assert(kChunk % (4 * kThreads) == 0, "a chunk is a whole number of float4 per thread");
 
 struct __align__(128) Smem {
@@ -83,7 +85,7 @@ struct __align__(128) Smem {
   uint32_t hist[kBins];           // histogram of kept keys (also radix scratch)
   uint32_t bkey[kBufCap];         // candidate keys
   int32_t bidx[kBufCap];          // candidate indices (row-relative)
-  int32_t emit[kMaxTopK];         // selected indices of the row being finished
+  int32_t emit[kListCap];         // bin-t entries of the row being finished; staged survivors
   int32_t small[kSmallSet];       // candidate positions ranked by rank_small
   alignas(16) uint32_t rk[kSmallSet];  // their keys, copied for ranking
   alignas(16) int32_t ri[kSmallSet];   // their indices
@@ -586,9 +588,10 @@ __device__ __noinline__ void select_threshold(Smem& s, int K, uint32_t& T, int& 
   I = select_tied_indices(s, T, need);
 }
 
-// Puts the indices of the selected entries ({key > T} + {key == T, idx <= I})
-// into s.emit; returns how many.
-__device__ __noinline__ int emit_selected(Smem& s, uint32_t T, int I) {
+// Writes the indices of the selected entries ({key > T} + {key == T, idx <= I})
+// to dst[0, cap) (one shared reservation per warp; entries past cap are
+// dropped); returns how many were selected. Consumer-wide; ends with a barrier.
+__device__ __noinline__ int emit_selected(Smem& s, uint32_t T, int I, int32_t* dst, int cap) {
   csync();
   if (threadIdx.x == 0) s.n_emit = 0;
   csync();
@@ -603,7 +606,7 @@ __device__ __noinline__ int emit_selected(Smem& s, uint32_t T, int I) {
       x = s.bidx[i];
       sel = k > T || (k == T && x <= I);
     }
-    warp_push<int32_t>(s.emit, &s.n_emit, kMaxTopK, sel, x);
+    warp_push<int32_t>(dst, &s.n_emit, cap, sel, x);
   }
   csync();
   return s.n_emit;
@@ -941,7 +944,7 @@ __device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, 
   if (lane == 0) base = atomicAdd(&s.buf_n, tot);
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
   int o = __popc(q0 & lt) + 2 * __popc(q1 & lt) + 4 * __popc(q2 & lt) + 8 * __popc(q3 & lt);
-  constexpr int kStaged = (2 * kMaxTopK) / kWarps;  // 16-bit slots per warp in s.emit
+  constexpr int kStaged = (2 * kListCap) / kWarps;  // 16-bit slots per warp in s.emit
   if (tot <= kStaged) {
     // each lane only notes where its survivors are (a short divergent loop);
     // the whole warp then converts and stores them, 32 at a time. s.emit is
@@ -1099,7 +1102,7 @@ __device__ __forceinline__ void warp_find_top256(Smem& s, const uint32_t* h, int
 // they are ranked directly. Output slots come from one shared atomic per warp.
 // Starts right after close_window's barrier; five barriers in all.
 __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
-  constexpr int kListIt = (kMaxTopK + kThreads - 1) / kThreads;
+  constexpr int kListIt = (kListCap + kThreads - 1) / kThreads;
   const int K = p.topk;
   const int tid = threadIdx.x;
   const int lane = static_cast<int>(lane_id());
@@ -1110,7 +1113,7 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
   const int need = K - (s.cnt_ge - inbin);
   const int n = s.buf_n;
   bool done = false;
-  if (inbin <= kMaxTopK) {
+  if (inbin <= kListCap) {
     // pass 1 over the buffer, in two short loops (counts, then writes) so the
     // code stays small: one reservation per warp for winners and for the list
     int tw = 0, tc = 0;
@@ -1144,12 +1147,12 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
         const int q = ow + __popc(bw & lt);
         if (q < K) o[q] = s.bidx[i];
       }
-      if ((bc >> lane) & 1u) s.emit[min(oc + __popc(bc & lt), kMaxTopK - 1)] = i;
+      if ((bc >> lane) & 1u) s.emit[min(oc + __popc(bc & lt), kListCap - 1)] = i;
       ow += __popc(bw);
       oc += __popc(bc);
     }
     csync();
-    const int nL = min(s.n_list, kMaxTopK);
+    const int nL = min(s.n_list, kListCap);
     if (need >= nL) {
       const int base = s.n_emit;
       for (int j = tid; j < nL; j += kThreads)
@@ -1228,8 +1231,7 @@ __device__ void finish_local(Smem& s, const Params& p, int64_t r) {
     uint32_t T;
     int I;
     select_threshold(s, K, T, I);
-    const int ne = min(emit_selected(s, T, I), K);
-    for (int j = tid; j < ne; j += kThreads) o[j] = s.emit[j];
+    emit_selected(s, T, I, o, K);
   }
   csync();
   reset_row_state(s);
@@ -1364,11 +1366,8 @@ __device__ __noinline__ bool finish_group(Smem& s, const Params& p, int64_t r, i
       I = select_tied_indices(s, T, take);
     }
   }
-  const int ne = emit_selected(s, T, I);
   int32_t* o = p.out + r * static_cast<int64_t>(K);
-  for (int j = tid; j < ne; j += kThreads)
-    if (off + j < K) o[off + j] = s.emit[j];
-  csync();
+  emit_selected(s, T, I, o + off, max(0, K - off));
   reset_row_state(s);
   csync();
   return true;

@@ -46,7 +46,7 @@ extern "C" int topk_ragged_static(const float* logits, int64_t row_stride, const
                                   void* stream) {
   if (num_rows < 0 || row_stride < 1 || next_n < 1 || (num_rows % next_n) != 0)
     return TOPK_ERR_INVALID_ARG;
-  if (!(topk == 512 || topk == 1024 || topk == 2048)) return TOPK_ERR_UNSUPPORTED_TOPK;
+  if (topk < 1 || topk > ltk::kWideMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
   if (num_rows == 0) return TOPK_OK;
   if (logits == nullptr || lengths == nullptr || out_idx == nullptr) return TOPK_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(logits) & 3u) || (reinterpret_cast<uintptr_t>(lengths) & 3u) ||

@@ -41,7 +41,9 @@ def test_status_strings(lib):
 
 def test_host_validation_needs_no_gpu(lib):
     fake = 0x10000  # never dereferenced: validation fails before any CUDA call
-    assert sar.topk_ragged(fake, 4096, fake, 8, 1, 100, fake, fake, None) == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert sar.topk_ragged(fake, 4096, fake, 8, 1, 0, fake, fake, None) == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert sar.topk_ragged(fake, 4096, fake, 8, 1, 4097, fake, fake, None) == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert sar.topk_ragged_static(fake, 4096, fake, 8, 1, -5, fake, None) == sar.TOPK_ERR_UNSUPPORTED_TOPK
     assert sar.topk_ragged(fake, 4096, fake, -1, 1, 512, fake, fake, None) == sar.TOPK_ERR_INVALID_ARG
     assert sar.topk_ragged(fake, 0, fake, 8, 1, 512, fake, fake, None) == sar.TOPK_ERR_INVALID_ARG
     assert sar.topk_ragged(fake, 4096, fake, 9, 2, 512, fake, fake, None) == sar.TOPK_ERR_INVALID_ARG

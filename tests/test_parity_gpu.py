@@ -35,6 +35,22 @@ def test_workloads_small_paired_shape(rn, name, rows):
     assert rn.workspace_clean()
 
 
+@pytest.mark.parametrize("topk", [1, 7, 100, 1000, 2047, 2049, 3000, 4096])
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (0, 0, 2), (3, 1, 0), (4, 2, 0)])
+def test_runtime_topk(rn, topk, G, merge, shape):
+    """TopK outside the pages' 512 / 1024 / 2048, on every path (the paired shape up to 2048)."""
+    if shape == 2 and topk > 2048:
+        pytest.skip("the paired shape serves TopK up to 2048")
+    rng = np.random.default_rng(topk)
+    S = 40000
+    x = np.round(rng.standard_normal((12, S)) * 32).astype(np.float32) / 32  # heavy ties
+    lens = rng.integers(0, S, 12, endpoint=True).astype(np.int32)
+    lens[:4] = [0, topk - 1 if topk > 1 else 0, topk, S]
+    got = rn.run(x, lens, topk, options=rn.options(force_ctas_per_group=G, merge=merge, shape=shape))
+    assert_matches_oracle(x, lens, got, topk, label=f"K={topk} G={G} merge={merge} shape={shape}")
+    assert rn.workspace_clean()
+
+
 # merge 1: the CTAs of a row merge through the workspace (grid barrier);
 # merge 2: they form a thread-block cluster and merge in its shared memory
 SPLITS = [(1, 0), (2, 1), (2, 2), (3, 1), (3, 2), (5, 2), (8, 2), (9, 1), (16, 1)]

@@ -72,7 +72,7 @@ def test_invariants_on_random_shapes():
         nn = rng.choice([1, 2, 4])
         rows -= rows % nn
         stride = rng.choice([1, 17, 4096, 32768, 32769, 131072, rng.randint(1, 1 << 22)])
-        topk = rng.choice([512, 1024, 2048])
+        topk = rng.choice([512, 1024, 2048, 1, rng.randint(1, 4096)])
         force = rng.choice([0, 0, 0, 1, 2, 5, 16])
         maxc = rng.choice([0, 0, rng.randint(1, 400)])
         rc, pl = plan(props(num_sms=sms, occ=occ), rows, stride, next_n=nn, topk=topk,
@@ -193,11 +193,18 @@ def test_paired_shape():
     assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1
     assert plan(props(), 8, 4096, shape=2)[0] == sar.TOPK_ERR_PLAN
     assert plan(gb, 8, 4096, shape=3)[0] == sar.TOPK_ERR_INVALID_ARG
+    # TopK above 2048 runs on the wide shape only
+    rc, pl = plan(gb, 4096, 65536, topk=3000)
+    assert rc == 0 and pl.shape == 1
+    assert plan(gb, 8, 4096, topk=2049, shape=2)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    rc, pl = plan(gb, 4096, 65536, topk=777)
+    assert rc == 0 and pl.shape == 2
 
 
 def test_rejections():
     gb = props()
-    assert plan(gb, 8, 4096, topk=100)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert plan(gb, 8, 4096, topk=0)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert plan(gb, 8, 4096, topk=4097)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
     assert plan(gb, 9, 4096, next_n=2)[0] == sar.TOPK_ERR_INVALID_ARG
     assert plan(gb, 8, 0)[0] == sar.TOPK_ERR_INVALID_ARG
     assert plan(gb, 8, 4096, force_ctas_per_group=17)[0] == sar.TOPK_ERR_INVALID_ARG
