@@ -179,6 +179,26 @@ int topk_ragged(const float* logits, int64_t row_stride, const int32_t* lengths,
 int topk_ragged_static(const float* logits, int64_t row_stride, const int32_t* lengths,
                        int64_t num_rows, int next_n, int topk, int32_t* out_idx, void* stream);
 
+/*
+ * topk_ragged over a strided logits view: element (r, i) is
+ * logits[r * row_stride + i * col_stride], for 0 <= i < max_len. The pages'
+ * decode fallback receives both strides of the logits tensor (vLLM PR #54110
+ * page, "Implementation breakdown", the top_k_per_row_decode call with
+ * logits.stride(0) and logits.stride(1)); a transposed view has row_stride 1
+ * and col_stride equal to the number of rows.
+ *   row_stride  >= 0 elements between row starts.
+ *   col_stride  >= 1 elements between consecutive columns; 1 = contiguous rows
+ *               (then this is topk_ragged with max_len as the length bound).
+ *   max_len     1..2^31-1 columns per row: every length is clamped into
+ *               [0, max_len], and only elements i < max_len are ever read.
+ * Other arguments, ownership and errors as in topk_ragged; options may be
+ * NULL. With col_stride > 1 the rows are read element by element (no bulk
+ * copies): correct for any layout, but each element costs a memory sector.
+ */
+int topk_ragged_strided(const float* logits, int64_t row_stride, int64_t col_stride, int64_t max_len,
+                        const int32_t* lengths, int64_t num_rows, int next_n, int topk, int32_t* out_idx,
+                        void* workspace, void* stream, const topk_options* options);
+
 /* topk_ragged with options (NULL options = topk_ragged). */
 int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths,
                    int64_t num_rows, int next_n, int topk, int32_t* out_idx,

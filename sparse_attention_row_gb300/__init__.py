@@ -18,6 +18,7 @@ import threading
 __all__ = [
     "TOPK_OK", "TopkError", "TopkOptions", "TopkDeviceProps", "TopkPlan",
     "topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex", "topk_ragged_static",
+    "topk_ragged_strided",
     "topk_get_status", "topk_status_string", "topk_query_device", "topk_make_plan",
     "library_path", "Selector",
 ]
@@ -50,7 +51,8 @@ TOPK_DEV_BARRIER_TIMEOUT = 0x2
 TOPK_DEV_STAGE_TIMEOUT = 0x4
 
 EXPORTED = ("topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex", "topk_ragged_static",
-            "topk_get_status", "topk_status_string", "topk_query_device", "topk_make_plan")
+            "topk_ragged_strided", "topk_get_status", "topk_status_string", "topk_query_device",
+            "topk_make_plan")
 
 
 class TopkError(RuntimeError):
@@ -115,6 +117,9 @@ def _load():
         lib.topk_ragged_ex.restype = i32
         lib.topk_ragged_ex.argtypes = [vp, i64, vp, i64, i32, i32, vp, vp, vp,
                                        ctypes.POINTER(TopkOptions)]
+        lib.topk_ragged_strided.restype = i32
+        lib.topk_ragged_strided.argtypes = [vp, i64, i64, i64, vp, i64, i32, i32, vp, vp, vp,
+                                            ctypes.POINTER(TopkOptions)]
         lib.topk_ragged_static.restype = i32
         lib.topk_ragged_static.argtypes = [vp, i64, vp, i64, i32, i32, vp, vp]
         lib.topk_get_status.restype = i32
@@ -181,6 +186,16 @@ def topk_ragged_ex(logits, row_stride: int, lengths, num_rows: int, next_n: int,
                                       topk, _ptr(out_idx), _ptr(workspace), _stream(stream), opt))
 
 
+def topk_ragged_strided(logits, row_stride: int, col_stride: int, max_len: int, lengths, num_rows: int,
+                        next_n: int, topk: int, out_idx, workspace, stream=None,
+                        options: TopkOptions | None = None) -> int:
+    """topk_ragged over a strided view: element (r, i) at logits[r * row_stride + i * col_stride]."""
+    opt = ctypes.byref(options) if options is not None else None
+    return int(_load().topk_ragged_strided(_ptr(logits), row_stride, col_stride, max_len, _ptr(lengths),
+                                           num_rows, next_n, topk, _ptr(out_idx), _ptr(workspace),
+                                           _stream(stream), opt))
+
+
 def topk_ragged_static(logits, row_stride: int, lengths, num_rows: int, next_n: int, topk: int,
                        out_idx, stream=None) -> int:
     """topk_ragged for callers that cannot allocate: no workspace argument."""
@@ -231,19 +246,29 @@ class Selector:
         if rc != TOPK_OK:
             raise TopkError(rc, "topk_workspace_init")
 
-    def __call__(self, logits, lengths, topk: int, next_n: int = 1, out=None, stream=None,
+    def __call__(self, logits, lengths, topk: int, next_n: int | None = None, out=None, stream=None,
                  options: TopkOptions | None = None):
+        """Top-K indices of every row of a float32 [num_rows, max_len] tensor (any strides).
+
+        lengths: int32, [num_rows], or [num_rows / next_n, next_n] for MTP, in which
+        case next_n is taken from its second dimension (as the pages' launcher does).
+        """
         import torch
 
-        if logits.dtype != torch.float32 or logits.dim() != 2 or logits.stride(1) != 1:
-            raise ValueError("logits must be a float32 [num_rows, row_stride] tensor with unit column stride")
-        if lengths.dtype != torch.int32 or not lengths.is_contiguous():
-            raise ValueError("lengths must be a contiguous int32 tensor")
-        num_rows = logits.shape[0]
+        if logits.dtype != torch.float32 or logits.dim() != 2:
+            raise ValueError("logits must be a float32 [num_rows, max_len] tensor")
+        if lengths.dtype != torch.int32 or not lengths.is_contiguous() or lengths.dim() not in (1, 2):
+            raise ValueError("lengths must be a contiguous int32 tensor with 1 or 2 dimensions")
+        if next_n is None:
+            next_n = lengths.shape[1] if lengths.dim() == 2 else 1
+        num_rows, max_len = logits.shape
+        if lengths.numel() != num_rows:
+            raise ValueError("lengths must hold one length per row")
         if out is None:
             out = torch.empty((num_rows, topk), dtype=torch.int32, device=logits.device)
-        rc = topk_ragged_ex(logits, logits.stride(0), lengths, num_rows, next_n, topk, out,
-                            self.workspace, stream, options)
+        # contiguous rows (stride(1) == 1) take the bulk-copy path inside the library
+        rc = topk_ragged_strided(logits, logits.stride(0), logits.stride(1), max_len, lengths, num_rows,
+                                 next_n, topk, out, self.workspace, stream, options)
         if rc != TOPK_OK:
             raise TopkError(rc, "topk_ragged")
         return out

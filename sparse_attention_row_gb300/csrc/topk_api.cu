@@ -3,6 +3,7 @@
 // never throws.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <climits>
 #include <stdlib.h>
 
 #include <mutex>
@@ -161,10 +162,11 @@ int topk_get_status(const void* workspace, void* stream, uint32_t* device_status
   return TOPK_OK;
 }
 
-int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths, int64_t num_rows,
-                   int next_n, int topk, int32_t* out_idx, void* workspace, void* stream,
-                   const topk_options* options) {
-  if (num_rows < 0 || row_stride < 1 || next_n < 1 || (num_rows % next_n) != 0)
+int topk_ragged_strided(const float* logits, int64_t row_stride, int64_t col_stride, int64_t max_len,
+                        const int32_t* lengths, int64_t num_rows, int next_n, int topk, int32_t* out_idx,
+                        void* workspace, void* stream, const topk_options* options) {
+  if (num_rows < 0 || row_stride < 0 || col_stride < 1 || max_len < 1 || max_len > INT32_MAX || next_n < 1 ||
+      (num_rows % next_n) != 0)
     return TOPK_ERR_INVALID_ARG;
   if (topk < 1 || topk > ltk::kWideMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
   if (num_rows == 0) return TOPK_OK;
@@ -189,13 +191,15 @@ int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengt
   if (opt.merge == 0) opt.merge = env.merge;
 
   topk_plan plan{};
-  rc = topk_make_plan(&props, num_rows, row_stride, next_n, topk, &opt, &plan);
+  rc = topk_make_plan(&props, num_rows, max_len, next_n, topk, &opt, &plan);
   if (rc != TOPK_OK) return rc;
   if (plan.grid < 1) return TOPK_OK;
 
   ltk::Params p{};
   p.logits = logits;
   p.stride = row_stride;
+  p.col_stride = col_stride;
+  p.max_len = max_len;
   p.lengths = lengths;
   p.num_rows = num_rows;
   p.out = out_idx;
@@ -214,6 +218,15 @@ int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengt
     return TOPK_ERR_CUDA;
   }
   return TOPK_OK;
+}
+
+int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths, int64_t num_rows,
+                   int next_n, int topk, int32_t* out_idx, void* workspace, void* stream,
+                   const topk_options* options) {
+  if (row_stride < 1) return TOPK_ERR_INVALID_ARG;
+  const int64_t max_len = row_stride < INT32_MAX ? row_stride : INT32_MAX;  // lengths are int32
+  return topk_ragged_strided(logits, row_stride, 1, max_len, lengths, num_rows, next_n, topk, out_idx,
+                             workspace, stream, options);
 }
 
 int topk_ragged(const float* logits, int64_t row_stride, const int32_t* lengths, int64_t num_rows,

@@ -50,7 +50,9 @@ inline size_t workspace_bytes_for(int num_sms) {
 
 struct Params {
   const float* logits;
-  int64_t stride;
+  int64_t stride;      // elements between row starts
+  int64_t col_stride;  // elements between consecutive columns (1: contiguous rows, bulk copies)
+  int64_t max_len;     // columns of every row; lengths are clamped into [0, max_len]
   const int32_t* lengths;
   int64_t num_rows;
   int32_t* out;

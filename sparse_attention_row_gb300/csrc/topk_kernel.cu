@@ -786,9 +786,9 @@ struct RowWin {
 };
 
 __device__ __forceinline__ int clamp_len(const Params& p, int32_t raw) {
-  if (raw < 0 || static_cast<int64_t>(raw) > p.stride) {
+  if (raw < 0 || static_cast<int64_t>(raw) > p.max_len) {
     atomicOr(p.status, 0x1u);
-    return raw < 0 ? 0 : static_cast<int>(p.stride);
+    return raw < 0 ? 0 : static_cast<int>(p.max_len);
   }
   return raw;
 }
@@ -815,8 +815,10 @@ __device__ __forceinline__ void row_window(const Params& p, int64_t r, int len, 
     if (w.hi > w.lo) {
       // copies start on the 16-byte boundary at or below element lo and end on
       // the one at or above element hi; every 16-byte granule copied holds at
-      // least one element of [lo, hi), so no copy leaves the row's pages
-      const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(w.rowp + w.lo) & 15u) >> 2);
+      // least one element of [lo, hi), so no copy leaves the row's pages.
+      // Strided rows are read element by element from lo on.
+      const int mis = (p.col_stride != 1) ? 0
+                          : static_cast<int>((reinterpret_cast<uintptr_t>(w.rowp + w.lo) & 15u) >> 2);
       w.wstart = w.lo - mis;
       w.wend = w.wstart + ((w.hi - w.wstart + 3) & ~3);
       w.nch = (w.wend - w.wstart + kChunk - 1) / kChunk;
@@ -842,7 +844,7 @@ __device__ __noinline__ void producer_first_whole(const Params& p, Smem& s, int 
   const float* rowp = p.logits + static_cast<int64_t>(g) * p.stride;
   const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(rowp) & 15u) >> 2);
   const int64_t ws = -mis;
-  const int64_t wend = ws + ((p.stride - ws + 3) & ~static_cast<int64_t>(3));
+  const int64_t wend = ws + ((p.max_len - ws + 3) & ~static_cast<int64_t>(3));
   const int64_t we = min(ws + kChunk, wend);
   const uint32_t bytes = static_cast<uint32_t>(we - ws) * 4u;
   fence_proxy_async();
@@ -981,6 +983,54 @@ __device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, 
   }
 }
 
+// filter_chunk for strided rows read straight from global memory: element e
+// of the window is rowp[e * col_stride], loaded only inside [lo, hi).
+__device__ __forceinline__ void filter_chunk_strided(Smem& s, const float* rowp, int64_t cs, int ws, int nvec,
+                                                     int lo, int hi) {
+  constexpr int V = kChunk / (4 * kThreads);
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const float thr = s.thr_f;
+  uint32_t m = 0;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int vi = tid + v * kThreads;
+    if (vi < nvec) {
+      const int i0 = ws + 4 * vi;
+      uint32_t b = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i0 + e;
+        if (i >= lo && i < hi && __ldg(rowp + static_cast<int64_t>(i) * cs) >= thr) b |= 1u << e;
+      }
+      m |= b << (4 * v);
+    }
+  }
+  const uint32_t lt = lanemask_lt();
+  const int c = __popc(m);
+  const uint32_t q0 = __ballot_sync(0xFFFFFFFFu, c & 1);
+  const uint32_t q1 = __ballot_sync(0xFFFFFFFFu, c & 2);
+  const uint32_t q2 = __ballot_sync(0xFFFFFFFFu, c & 4);
+  const uint32_t q3 = __ballot_sync(0xFFFFFFFFu, c & 8);
+  const int tot = __popc(q0) + 2 * __popc(q1) + 4 * __popc(q2) + 8 * __popc(q3);
+  if (tot == 0) return;
+  int base = 0;
+  if (lane == 0) base = atomicAdd(&s.buf_n, tot);
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  int o = base + __popc(q0 & lt) + 2 * __popc(q1 & lt) + 4 * __popc(q2 & lt) + 8 * __popc(q3 & lt);
+  while (m) {
+    const int j = __ffs(m) - 1;
+    m &= m - 1;
+    const int idx = ws + 4 * (tid + (j >> 2) * kThreads) + (j & 3);
+    const uint32_t k = fkey(__ldg(rowp + static_cast<int64_t>(idx) * cs));
+    const int oo = min(o, kBufCap - 1);
+    s.bkey[oo] = k;
+    s.bidx[oo] = idx;
+    atomicAdd(&s.hist[k >> 20], 1u);
+    ++o;
+  }
+}
+
 // Histograms the keys of one staged chunk (elements inside [lo, hi)).
 __device__ __forceinline__ void hist_chunk(Smem& s, const float* src, int ws, int nvec, int lo, int hi) {
   constexpr int V = kChunk / (4 * kThreads);
@@ -1001,7 +1051,8 @@ __device__ __forceinline__ void hist_chunk(Smem& s, const float* src, int ws, in
 
 // Streams the window [lo, hi) of row w straight from global memory with no
 // seed: every element starts eligible and the threshold rises as candidates
-// accumulate. Used only when a seeded pass kept fewer than K elements.
+// accumulate. Used when a seeded pass kept fewer than K elements, and for
+// every row of strided logits (no bulk copies there).
 __device__ __noinline__ void restream_row(Smem& s, const Params& p, const RowWin w) {
   csync();
   reset_row_state(s);
@@ -1010,7 +1061,10 @@ __device__ __noinline__ void restream_row(Smem& s, const Params& p, const RowWin
     if (s.buf_n + kChunk > kBufCap) make_room(s, p.topk);
     const int ws = w.wstart + j * kChunk;
     const int we = min(ws + kChunk, w.wend);
-    filter_chunk<true, true>(s, w.rowp + ws, ws, (we - ws) >> 2, w.lo, w.hi);
+    if (p.col_stride == 1)
+      filter_chunk<true, true>(s, w.rowp + ws, ws, (we - ws) >> 2, w.lo, w.hi);
+    else
+      filter_chunk_strided(s, w.rowp, p.col_stride, ws, (we - ws) >> 2, w.lo, w.hi);
     csync();
     if (threadIdx.x < 32) advance_threshold(s, p.topk);
     csync();
@@ -1595,7 +1649,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
       mbar_init(&s.xbar[1], static_cast<uint32_t>(p.G));
     }
     fence_mbar_init();
-    if (p.G == 1) {
+    if (p.G == 1 && p.col_stride == 1) {
       producer_first_whole(p, s, g);
       first = true;
     }
@@ -1613,7 +1667,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
   if (p.cluster) cluster_arrive_all();
   __syncthreads();
   if (tid >= kThreads) {
-    if (tid == kThreads) {
+    if (tid == kThreads && p.col_stride == 1) {  // strided rows are read by the consumers
       if (p.G > 1) first = producer_first_split(p, s, g, m, len0);
       producer_loop(p, s, g, m, first);
     }
@@ -1632,7 +1686,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
   for (int64_t k = 0; !aborted && get_row(p, s, k, g, m, w); ++k) {
     if (w.len <= K) {
       if (m == 0) write_trivial_row(p, w.r, w.len);
-      if (p.G == 1 && k == 0) {
+      if (p.G == 1 && k == 0 && p.col_stride == 1) {
         // discard the early copy the copy warp issued for this row
         if (!mbar_wait_bounded(&s.full[0], 0u, p.timeout_ns, &s.abort)) atomicOr(p.status, 0x4u);
         __syncwarp();
@@ -1642,7 +1696,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
       continue;
     }
     const int span = w.hi - w.lo;
-    for (int j = 0; j < w.nch; ++j) {
+    if (p.col_stride != 1) restream_row(s, p, w);  // strided rows: no staging ring
+    for (int j = 0; p.col_stride == 1 && j < w.nch; ++j) {
       if (s.buf_n + kChunk > kBufCap) make_room(s, K);
       const int slot = static_cast<int>(q % kStages);
       const bool ok = mbar_wait_bounded(&s.full[slot], (q / kStages) & 1u, p.timeout_ns, &s.abort);

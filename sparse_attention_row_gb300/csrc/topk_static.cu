@@ -95,6 +95,8 @@ extern "C" int topk_ragged_static(const float* logits, int64_t row_stride, const
   ltk::Params p{};
   p.logits = logits;
   p.stride = row_stride;
+  p.col_stride = 1;
+  p.max_len = row_stride;
   p.lengths = lengths;
   p.num_rows = num_rows;
   p.out = out_idx;

@@ -52,6 +52,12 @@ def test_host_validation_needs_no_gpu(lib):
     assert sar.topk_ragged(fake + 2, 4096, fake, 8, 1, 512, fake, fake, None) == sar.TOPK_ERR_MISALIGNED
     assert sar.topk_ragged(fake, 4096, fake, 8, 1, 512, fake, fake + 4, None) == sar.TOPK_ERR_MISALIGNED
     assert sar.topk_workspace_init(None, 1024, None) == sar.TOPK_ERR_INVALID_ARG
+    # strided views: column stride and column count are checked before anything else
+    assert sar.topk_ragged_strided(fake, 4096, 0, 4096, fake, 8, 1, 512, fake, fake) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_ragged_strided(fake, 4096, 2, 0, fake, 8, 1, 512, fake, fake) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_ragged_strided(fake, -1, 2, 100, fake, 8, 1, 512, fake, fake) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_ragged_strided(fake, 1, 8, 100, fake, 8, 1, 0, fake, fake) == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert sar.topk_ragged_strided(fake, 1, 8, 100, fake, 0, 1, 512, fake, fake) == sar.TOPK_OK
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

@@ -51,6 +51,52 @@ def test_runtime_topk(rn, topk, G, merge, shape):
     assert rn.workspace_clean()
 
 
+@pytest.mark.parametrize("layout", ["transposed", "every_third_column", "padded_rows"])
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 2), (3, 1, 0), (4, 2, 0)])
+def test_strided_logits(rn, layout, G, merge, shape):
+    """Views with a row pitch and a column stride: transposed, column-strided, padded rows."""
+    torch = rn.torch
+    sar = rn.sar
+    rng = np.random.default_rng(hash(layout) % 1000 + G)
+    R, L, K = 10, 20000, 1024
+    x = (np.round(rng.standard_normal((R, L)) * 16) / 16).astype(np.float32)
+    lens = rng.integers(0, L, R, endpoint=True).astype(np.int32)
+    lens[:4] = [0, K - 1, K, L]
+    if layout == "transposed":
+        view = torch.from_numpy(np.ascontiguousarray(x.T)).to(rn.dev).t()
+    elif layout == "every_third_column":
+        big = np.full((R, 3 * L), np.nan, np.float32)
+        big[:, ::3] = x
+        view = torch.from_numpy(big).to(rn.dev)[:, ::3]
+    else:
+        big = np.full((R, L + 100), np.nan, np.float32)
+        big[:, :L] = x
+        view = torch.from_numpy(big).to(rn.dev)[:, :L]
+    ln = torch.from_numpy(lens).to(rn.dev)
+    out = torch.full((R, K), -7, dtype=torch.int32, device=rn.dev)
+    opts = rn.options(force_ctas_per_group=G, merge=merge, shape=shape)
+    rc = sar.topk_ragged_strided(view, view.stride(0), view.stride(1), L, ln, R, 1, K, out,
+                                 rn.sel.workspace, None, opts)
+    assert rc == sar.TOPK_OK, sar.topk_status_string(rc)
+    torch.cuda.synchronize()
+    assert rn.sel.status() == 0
+    assert_matches_oracle(x, lens, out.cpu().numpy(), K, label=f"{layout} G={G} merge={merge} shape={shape}")
+    assert rn.workspace_clean()
+
+
+def test_selector_takes_views_and_two_dimensional_lengths(rn):
+    """The binding's Selector: a strided view, and next_n from [requests, next_n] lengths."""
+    torch = rn.torch
+    w = workloads.make("mtp", 8)
+    ln2 = torch.from_numpy(w.lengths.reshape(-1, 2)).to(rn.dev)
+    x = torch.from_numpy(w.logits).to(rn.dev)
+    got = rn.sel(x, ln2, w.topk).cpu().numpy()
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, 2, label="selector mtp")
+    xt = torch.from_numpy(np.ascontiguousarray(w.logits.T)).to(rn.dev).t()
+    got = rn.sel(xt, ln2, w.topk).cpu().numpy()
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, 2, label="selector transposed")
+
+
 # merge 1: the CTAs of a row merge through the workspace (grid barrier);
 # merge 2: they form a thread-block cluster and merge in its shared memory
 SPLITS = [(1, 0), (2, 1), (2, 2), (3, 1), (3, 2), (5, 2), (8, 2), (9, 1), (16, 1)]
