@@ -82,7 +82,9 @@ typedef struct {
    * thread-block cluster, through its distributed shared memory (G <= 8). */
   int merge;
   /* CTA shape. 0 = planner decides; 1 = one CTA of 24 consumer warps per SM;
-   * 2 = two CTAs of 12 consumer warps per SM (whole rows only). */
+   * 2 = two CTAs of 12 consumer warps per SM (whole rows only); 3 = a CTA of 8
+   * consumer warps in about 83 KB of shared memory (whole rows only), the
+   * low-shared-memory mode for devices or partitions where 1 and 2 do not fit. */
   int shape;
 } topk_options;
 
@@ -97,6 +99,8 @@ typedef struct {
   int cluster_groups[9];
   int pair_smem_per_cta; /* the same for the paired shape (two CTAs per SM) */
   int pair_ctas_per_sm;
+  int small_smem_per_cta; /* the same for the small shape */
+  int small_ctas_per_sm;
 } topk_device_props;
 
 /* A launch configuration. */
@@ -108,7 +112,8 @@ typedef struct {
   int smem_bytes;     /* dynamic shared memory per CTA */
   int cooperative;    /* 1 when the CTAs of a group wait on one another through the workspace */
   int cluster;        /* 1 when the CTAs of a group form a cluster and merge in its shared memory */
-  int shape;          /* 1 = one CTA of 24 consumer warps per SM, 2 = two CTAs of 12 per SM */
+  int shape;          /* 1 = one CTA of 24 consumer warps per SM, 2 = two CTAs of 12 per SM,
+                         3 = the small shape (8 consumer warps, low shared memory) */
 } topk_plan;
 
 /*

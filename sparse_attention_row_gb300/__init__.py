@@ -45,6 +45,7 @@ TOPK_MERGE_CLUSTER = 2
 TOPK_SHAPE_AUTO = 0
 TOPK_SHAPE_WIDE = 1
 TOPK_SHAPE_PAIR = 2
+TOPK_SHAPE_SMALL = 3
 
 TOPK_DEV_LENGTH_CLAMPED = 0x1
 TOPK_DEV_BARRIER_TIMEOUT = 0x2
@@ -79,7 +80,9 @@ class TopkDeviceProps(ctypes.Structure):
                 ("ctas_per_sm", ctypes.c_int),
                 ("cluster_groups", ctypes.c_int * 9),
                 ("pair_smem_per_cta", ctypes.c_int),
-                ("pair_ctas_per_sm", ctypes.c_int)]
+                ("pair_ctas_per_sm", ctypes.c_int),
+                ("small_smem_per_cta", ctypes.c_int),
+                ("small_ctas_per_sm", ctypes.c_int)]
 
 
 class TopkPlan(ctypes.Structure):

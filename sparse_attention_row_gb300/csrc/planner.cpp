@@ -28,6 +28,9 @@
 //   - G = 1 launches min(num_rows, capacity) persistent CTAs, no waiting;
 //     with at least kPairRowsPerSm rows per SM it uses the paired shape (two
 //     CTAs of 12 consumer warps per SM), otherwise the wide one;
+//   - a device whose shared memory per block cannot hold the wide shape gets
+//     whole rows on the paired shape if it fits, else on the small shape
+//     (about 83 KB), else TOPK_ERR_PLAN;
 //   - a workspace merge launches num_groups = min(capacity / G, num_rows,
 //     num_sms) groups cooperatively, so grid = num_groups * G <= num_sms *
 //     ctas_per_sm always; a cluster merge launches at most cluster_groups[G]
@@ -52,73 +55,82 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     return TOPK_ERR_INVALID_ARG;
   if (!topk_supported(topk)) return TOPK_ERR_UNSUPPORTED_TOPK;
   *plan = topk_plan{};
-  plan->threads = ltk::kWideCtaThreads;
-  plan->smem_bytes = props->smem_per_cta;
-  plan->shape = ltk::kShapeWide;
-  if (props->num_sms < 1 || props->ctas_per_sm < 1 || props->smem_per_cta > props->max_smem_optin)
-    return TOPK_ERR_PLAN;
+  const int merge = (options != nullptr) ? options->merge : 0;
+  if (merge < 0 || merge > 2) return TOPK_ERR_INVALID_ARG;
+  const int shape = (options != nullptr) ? options->shape : 0;
+  if (shape < 0 || shape > 3) return TOPK_ERR_INVALID_ARG;
+  const int force = (options != nullptr) ? options->force_ctas_per_group : 0;
+  if (force < 0 || force > ltk::kMaxGroup) return TOPK_ERR_INVALID_ARG;
+  if (shape > ltk::kShapeWide && force > 1) return TOPK_ERR_INVALID_ARG;  // those shapes split no row
+  if (props->num_sms < 1) return TOPK_ERR_PLAN;
+  const bool wide_ok = props->ctas_per_sm >= 1 && props->smem_per_cta <= props->max_smem_optin;
+  const bool pair_ok = props->pair_ctas_per_sm >= 1 && props->pair_smem_per_cta <= props->max_smem_optin;
+  const bool small_ok = props->small_ctas_per_sm >= 1 && props->small_smem_per_cta <= props->max_smem_optin;
+
+  // the CTA shape when it is not the planner's to choose, or when the wide
+  // shape does not fit the device (then the largest whole-row shape that fits)
+  int chosen = shape;
+  if (chosen == 0 && !wide_ok) chosen = pair_ok ? ltk::kShapePair : ltk::kShapeSmall;
+  if (chosen == ltk::kShapeWide && !wide_ok) return TOPK_ERR_PLAN;
+  if (chosen == ltk::kShapePair && !pair_ok) return TOPK_ERR_PLAN;
+  if (chosen == ltk::kShapeSmall && !small_ok) return TOPK_ERR_PLAN;
+  if (chosen == ltk::kShapePair && topk > ltk::kPairMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
+  if (chosen == ltk::kShapeSmall && topk > ltk::kSmallMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
+
   int64_t cap = static_cast<int64_t>(props->num_sms) * props->ctas_per_sm;
   if (options != nullptr && options->max_ctas > 0) cap = std::min<int64_t>(cap, options->max_ctas);
   const int64_t threshold = (options != nullptr && options->long_row_threshold > 0)
                                 ? options->long_row_threshold
                                 : ltk::kDefaultLongRowThreshold;
-  const int merge = (options != nullptr) ? options->merge : 0;
-  if (merge < 0 || merge > 2) return TOPK_ERR_INVALID_ARG;
-  const int shape = (options != nullptr) ? options->shape : 0;
-  if (shape < 0 || shape > 2) return TOPK_ERR_INVALID_ARG;
-  const int force = (options != nullptr) ? options->force_ctas_per_group : 0;
-  if (shape == ltk::kShapePair && force > 1) return TOPK_ERR_INVALID_ARG;  // the paired shape splits no row
   auto clusters_of = [&](int64_t c) -> int64_t {
     return (c >= 2 && c <= ltk::kMaxCluster) ? props->cluster_groups[c] : 0;
   };
   int64_t G = 1;
   bool cluster = false;
-  if (options != nullptr && options->force_ctas_per_group != 0) {
-    G = options->force_ctas_per_group;
-    if (G < 1 || G > ltk::kMaxGroup) return TOPK_ERR_INVALID_ARG;
-    if (G > 1) {
-      if (merge == 2 && clusters_of(G) < 1) return TOPK_ERR_PLAN;
-      cluster = merge == 2 || (merge == 0 && clusters_of(G) >= 1);
+  if (chosen <= ltk::kShapeWide) {  // the wide shape, given or still open
+    if (force != 0) {
+      G = force;
+      if (G > 1) {
+        if (merge == 2 && clusters_of(G) < 1) return TOPK_ERR_PLAN;
+        cluster = merge == 2 || (merge == 0 && clusters_of(G) >= 1);
+      }
+    } else if (num_rows > 0 && row_stride > threshold && num_rows < cap) {
+      G = cap / num_rows;
+      G = std::min<int64_t>(G, ltk::kMaxGroup);
+      G = std::min<int64_t>(G, std::max<int64_t>(1, row_stride / ltk::kMinSpan));
+      // the largest cluster size whose clusters hold every row at once
+      int64_t gc = (merge != 1 && G >= 2) ? std::min<int64_t>(G, ltk::kMaxCluster) : 0;
+      while (gc >= 2 && clusters_of(gc) < num_rows) --gc;
+      if (gc >= 2) {
+        G = gc;
+        cluster = true;
+      } else if (merge == 2) {
+        G = 1;
+      }
+      const int64_t gain = cluster ? ltk::kSplitGainCluster : ltk::kSplitGain;
+      if (G < 2 || row_stride * (G - 1) / G < gain) {
+        G = 1;
+        cluster = false;
+      }
     }
-  } else if (shape != ltk::kShapePair && num_rows > 0 && row_stride > threshold && num_rows < cap) {
-    G = cap / num_rows;
-    G = std::min<int64_t>(G, ltk::kMaxGroup);
-    G = std::min<int64_t>(G, std::max<int64_t>(1, row_stride / ltk::kMinSpan));
-    // the largest cluster size whose clusters hold every row at once
-    int64_t gc = (merge != 1 && G >= 2) ? std::min<int64_t>(G, ltk::kMaxCluster) : 0;
-    while (gc >= 2 && clusters_of(gc) < num_rows) --gc;
-    if (gc >= 2) {
-      G = gc;
-      cluster = true;
-    } else if (merge == 2) {
-      G = 1;
-    }
-    const int64_t gain = cluster ? ltk::kSplitGainCluster : ltk::kSplitGain;
-    if (G < 2 || row_stride * (G - 1) / G < gain) {
-      G = 1;
-      cluster = false;
-    }
-  }
-  // whole rows: two narrower CTAs per SM when every SM gets several rows, so
-  // that one CTA's row finish overlaps the other's streaming (measured on a
-  // GB300 with 4096 rows of 61440+: 440 us against 509 us)
-  bool pair = false;
-  if (G == 1) {
-    if (shape == ltk::kShapePair) {
-      if (topk > ltk::kPairMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
-      if (props->pair_ctas_per_sm < 1 || props->pair_smem_per_cta > props->max_smem_optin) return TOPK_ERR_PLAN;
-      pair = true;
-    } else if (shape == 0) {
-      pair = topk <= ltk::kPairMaxTopK && props->pair_ctas_per_sm >= 2 &&
-             props->pair_smem_per_cta <= props->max_smem_optin &&
-             num_rows >= ltk::kPairRowsPerSm * props->num_sms;
+    // whole rows: two narrower CTAs per SM when every SM gets several rows, so
+    // that one CTA's row finish overlaps the other's streaming (measured on a
+    // GB300 with 4096 rows of 61440+: 440 us against 509 us)
+    if (chosen == 0) {
+      const bool pair = G == 1 && topk <= ltk::kPairMaxTopK && pair_ok && props->pair_ctas_per_sm >= 2 &&
+                        num_rows >= ltk::kPairRowsPerSm * props->num_sms;
+      chosen = pair ? ltk::kShapePair : ltk::kShapeWide;
     }
   }
-  if (pair) {
-    plan->shape = ltk::kShapePair;
-    plan->threads = ltk::kPairCtaThreads;
-    plan->smem_bytes = props->pair_smem_per_cta;
-    cap = static_cast<int64_t>(props->num_sms) * props->pair_ctas_per_sm;
+  plan->shape = chosen;
+  if (chosen == ltk::kShapeWide) {
+    plan->threads = ltk::kWideCtaThreads;
+    plan->smem_bytes = props->smem_per_cta;
+  } else {
+    const int per_sm = chosen == ltk::kShapePair ? props->pair_ctas_per_sm : props->small_ctas_per_sm;
+    plan->threads = chosen == ltk::kShapePair ? ltk::kPairCtaThreads : ltk::kSmallCtaThreads;
+    plan->smem_bytes = chosen == ltk::kShapePair ? props->pair_smem_per_cta : props->small_smem_per_cta;
+    cap = static_cast<int64_t>(props->num_sms) * per_sm;
     if (options != nullptr && options->max_ctas > 0) cap = std::min<int64_t>(cap, options->max_ctas);
   }
   plan->ctas_per_group = static_cast<int>(G);

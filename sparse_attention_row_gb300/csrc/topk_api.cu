@@ -79,6 +79,12 @@ int query_device_locked(int device, topk_device_props* out) {
           ltk::pair::kernel_occupancy(&p.pair_ctas_per_sm) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
     }
+    p.small_smem_per_cta = static_cast<int>(ltk::small::kernel_smem_bytes());
+    if (rc == TOPK_OK && p.small_smem_per_cta <= p.max_smem_optin) {
+      if (ltk::small::kernel_configure() != cudaSuccess ||
+          ltk::small::kernel_occupancy(&p.small_ctas_per_sm) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
+    }
     if (prev != device) cudaSetDevice(prev);
     if (rc != TOPK_OK) {
       cudaGetLastError();

@@ -11,6 +11,7 @@ constexpr int kBins = 4096;            // 12-bit radix digits
 constexpr int kListCap = 2048;         // entries of the threshold bin listed by the row finish
 constexpr int kWideMaxTopK = 4096;     // largest TopK of the wide shape (buffer: TopK + a chunk)
 constexpr int kPairMaxTopK = 2048;     // largest TopK of the paired shape
+constexpr int kSmallMaxTopK = 2048;    // largest TopK of the small shape
 constexpr int kMaxGroup = 16;          // CTAs that may split one row
 constexpr int kMaxCluster = 8;         // CTAs of a group that may form one thread-block cluster
 constexpr int kLenCache = 64;          // row lengths cached in shared memory
@@ -25,10 +26,14 @@ constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 // CTA shapes. kShapeWide: one CTA of 24 consumer warps per SM (any row split).
 // kShapePair: two CTAs of 12 consumer warps per SM, whole rows only; with many
 // rows per SM one CTA's row finish overlaps the other's streaming.
+// kShapeSmall: 8 consumer warps in about 83 KB of shared memory, whole rows
+// only, for devices or partitions with less shared memory per block.
 constexpr int kShapeWide = 1;
 constexpr int kShapePair = 2;
-constexpr int kWideCtaThreads = 800;  // 24 consumer warps + the copy warp
-constexpr int kPairCtaThreads = 416;  // 12 consumer warps + the copy warp
+constexpr int kShapeSmall = 3;
+constexpr int kWideCtaThreads = 800;   // 24 consumer warps + the copy warp
+constexpr int kPairCtaThreads = 416;   // 12 consumer warps + the copy warp
+constexpr int kSmallCtaThreads = 288;  // 8 consumer warps + the copy warp
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.
@@ -78,11 +83,13 @@ struct Params {
   }
 LTK_DECLARE_SHAPE(wide)
 LTK_DECLARE_SHAPE(pair)
+LTK_DECLARE_SHAPE(small)
 #undef LTK_DECLARE_SHAPE
 
 inline cudaError_t launch_shape(int shape, const Params& p, int grid, bool cooperative, cudaStream_t stream) {
-  return shape == kShapePair ? pair::launch_topk(p, grid, cooperative, stream)
-                             : wide::launch_topk(p, grid, cooperative, stream);
+  if (shape == kShapePair) return pair::launch_topk(p, grid, cooperative, stream);
+  if (shape == kShapeSmall) return small::launch_topk(p, grid, cooperative, stream);
+  return wide::launch_topk(p, grid, cooperative, stream);
 }
 
 }  // namespace ltk

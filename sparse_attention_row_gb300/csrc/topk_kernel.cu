@@ -43,14 +43,20 @@
 
 #include "topk_internal.h"
 
-// This file is compiled twice: as is (the wide CTA shape, namespace
-// ltk::wide) and from topk_kernel_pair.cu with LTK_SHAPE_PAIR set (two
-// narrower CTAs per SM, namespace ltk::pair).
+// This file is compiled three times: as is (the wide CTA shape, namespace
+// ltk::wide), from topk_kernel_pair.cu with LTK_SHAPE_PAIR set (two narrower
+// CTAs per SM, ltk::pair) and from topk_kernel_small.cu with LTK_SHAPE_SMALL
+// set (a CTA that fits in about 83 KB of shared memory, ltk::small).
 #ifndef LTK_SHAPE_PAIR
 #define LTK_SHAPE_PAIR 0
 #endif
+#ifndef LTK_SHAPE_SMALL
+#define LTK_SHAPE_SMALL 0
+#endif
 #if LTK_SHAPE_PAIR
 #define LTK_SHAPE_NS pair
+#elif LTK_SHAPE_SMALL
+#define LTK_SHAPE_NS small
 #else
 #define LTK_SHAPE_NS wide
 #endif
@@ -65,6 +71,13 @@ constexpr int kChunk = 3072;    // fp32 elements per staging slot (12 KB)
 constexpr int kStages = 3;      // staging slots per CTA (36 KB)
 constexpr int kBufCap = 6144;   // candidate (key, index) pairs kept per CTA
 constexpr int kMinBlocks = 2;   // CTAs per SM the shape is built for
+#elif LTK_SHAPE_SMALL
+constexpr int kTopKMax = kSmallMaxTopK;
+constexpr int kThreads = 256;   // consumer threads per CTA (8 warps)
+constexpr int kChunk = 2048;    // fp32 elements per staging slot (8 KB)
+constexpr int kStages = 3;      // staging slots per CTA (24 KB)
+constexpr int kBufCap = 4096;   // candidate (key, index) pairs kept per CTA
+constexpr int kMinBlocks = 1;
 #else
 constexpr int kTopKMax = kWideMaxTopK;
 constexpr int kThreads = 768;   // consumer threads per CTA (24 warps)
@@ -75,7 +88,9 @@ constexpr int kMinBlocks = 1;
 #endif
 constexpr int kWarps = kThreads / 32;
 constexpr int kCtaThreads = kThreads + 32;  // plus one copy-issuing warp
-static_assert(kCtaThreads == (LTK_SHAPE_PAIR ? kPairCtaThreads : kWideCtaThreads), "shape constants agree");
+static_assert(kCtaThreads == (LTK_SHAPE_PAIR ? kPairCtaThreads : LTK_SHAPE_SMALL ? kSmallCtaThreads : kWideCtaThreads),
+              "shape constants agree");
+static_assert(kThreads - 32 >= kSmallSet, "close_window pads the ranking slots with all but warp 0");
 
 static_assert(kTopKMax + kChunk <= kBufCap, "a chunk must fit next to topk kept candidates");
 static_assert(kChunk % (4 * kThreads) == 0, "a chunk is a whole number of float4 per thread");

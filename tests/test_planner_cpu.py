@@ -13,15 +13,19 @@ def _built():
     build.build_library()
 
 
-def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, pair=(0, 0)):
+def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, pair=(0, 0), small=(0, 0)):
     """A made-up device; clusters maps a cluster size to its co-resident count (none by default);
-    pair is (shared memory, CTAs per SM) of the paired shape (absent by default)."""
+    pair and small are (shared memory, CTAs per SM) of those shapes (absent by default)."""
     p = sar.TopkDeviceProps()
     p.num_sms, p.ctas_per_sm, p.smem_per_cta, p.max_smem_optin = num_sms, occ, smem, optin
     for c, n in (clusters or {}).items():
         p.cluster_groups[c] = n
     p.pair_smem_per_cta, p.pair_ctas_per_sm = pair
+    p.small_smem_per_cta, p.small_ctas_per_sm = small
     return p
+
+
+GB300_SMALL = (85000, 2)
 
 
 GB300_PAIR = (113536, 2)
@@ -192,13 +196,35 @@ def test_paired_shape():
     rc, pl = plan(gb, 16, 131072, shape=2)
     assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1
     assert plan(props(), 8, 4096, shape=2)[0] == sar.TOPK_ERR_PLAN
-    assert plan(gb, 8, 4096, shape=3)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 4096, shape=4)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 4096, shape=3)[0] == sar.TOPK_ERR_PLAN  # no small shape on this made-up device
     # TopK above 2048 runs on the wide shape only
     rc, pl = plan(gb, 4096, 65536, topk=3000)
     assert rc == 0 and pl.shape == 1
     assert plan(gb, 8, 4096, topk=2049, shape=2)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
     rc, pl = plan(gb, 4096, 65536, topk=777)
     assert rc == 0 and pl.shape == 2
+
+
+def test_low_shared_memory_devices():
+    # a GB10-class part: ~99 KB per block holds neither the wide nor the paired shape
+    gb10 = props(num_sms=48, smem=224 * 1024, optin=99 * 1024, pair=(113536, 0), small=(85000, 1))
+    gb10.ctas_per_sm = 0
+    rc, pl = plan(gb10, 64, 32768)
+    assert rc == 0 and pl.shape == 3 and pl.ctas_per_group == 1 and pl.grid == 48 and pl.threads == 288
+    rc, pl = plan(gb10, 16, 131072)  # long rows are not split on the small shape
+    assert rc == 0 and pl.shape == 3 and pl.ctas_per_group == 1 and not pl.cooperative
+    assert plan(gb10, 8, 4096, topk=3000)[0] == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert plan(gb10, 8, 4096, shape=1)[0] == sar.TOPK_ERR_PLAN
+    # a partition that holds the paired shape but not the wide one
+    mig = props(optin=120 * 1024, pair=GB300_PAIR, small=GB300_SMALL)
+    rc, pl = plan(mig, 64, 32768)
+    assert rc == 0 and pl.shape == 2
+    # the small shape forced on a full GB300
+    gb = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL)
+    rc, pl = plan(gb, 64, 32768, shape=3)
+    assert rc == 0 and pl.shape == 3 and pl.grid == 64
+    assert plan(gb, 64, 163840, shape=3, force_ctas_per_group=2)[0] == sar.TOPK_ERR_INVALID_ARG
 
 
 def test_rejections():
@@ -208,8 +234,8 @@ def test_rejections():
     assert plan(gb, 9, 4096, next_n=2)[0] == sar.TOPK_ERR_INVALID_ARG
     assert plan(gb, 8, 0)[0] == sar.TOPK_ERR_INVALID_ARG
     assert plan(gb, 8, 4096, force_ctas_per_group=17)[0] == sar.TOPK_ERR_INVALID_ARG
-    # a device whose opt-in shared memory cannot hold the kernel (a GB10-class ~99 KB part)
-    assert plan(props(optin=99 * 1024), 8, 200000)[0] == sar.TOPK_ERR_PLAN
+    # a device whose opt-in shared memory holds none of the shapes
+    assert plan(props(optin=64 * 1024, pair=GB300_PAIR, small=GB300_SMALL), 8, 200000)[0] == sar.TOPK_ERR_PLAN
     assert plan(props(occ=0), 8, 4096)[0] == sar.TOPK_ERR_PLAN
 
 
