@@ -204,6 +204,22 @@ int topk_ragged_strided(const float* logits, int64_t row_stride, int64_t col_str
                         const int32_t* lengths, int64_t num_rows, int next_n, int topk, int32_t* out_idx,
                         void* workspace, void* stream, const topk_options* options);
 
+/*
+ * Values and order of selected rows (one extra launch on `stream`). For every
+ * row r of out_idx (int32 [num_rows, topk], as written by topk_ragged or
+ * topk_ragged_strided on the same logits): if out_val is not NULL, writes the
+ * value of each selected index to out_val (fp32 [num_rows, topk]; -inf where
+ * the index is -1); if sort != 0, first reorders the row in place by value
+ * descending, then index ascending, -1 entries last (the order the pages' tie
+ * rule implies; the selection itself returns a set). Logits are addressed as
+ * in topk_ragged_strided; an index outside [0, max_len) is treated as -1 and
+ * never read. No workspace; the launch needs up to 32 KB of shared memory.
+ * Returns the topk_status codes of topk_ragged (TOPK_OK when num_rows is 0, or
+ * when sort is 0 and out_val is NULL: nothing to do).
+ */
+int topk_gather_sort(const float* logits, int64_t row_stride, int64_t col_stride, int64_t max_len,
+                     int64_t num_rows, int topk, int32_t* out_idx, float* out_val, int sort, void* stream);
+
 /* topk_ragged with options (NULL options = topk_ragged). */
 int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths,
                    int64_t num_rows, int next_n, int topk, int32_t* out_idx,

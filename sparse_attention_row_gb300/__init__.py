@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "TOPK_OK", "TopkError", "TopkOptions", "TopkDeviceProps", "TopkPlan",
     "topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex", "topk_ragged_static",
-    "topk_ragged_strided",
+    "topk_ragged_strided", "topk_gather_sort",
     "topk_get_status", "topk_status_string", "topk_query_device", "topk_make_plan",
     "library_path", "Selector",
 ]
@@ -52,8 +52,8 @@ TOPK_DEV_BARRIER_TIMEOUT = 0x2
 TOPK_DEV_STAGE_TIMEOUT = 0x4
 
 EXPORTED = ("topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex", "topk_ragged_static",
-            "topk_ragged_strided", "topk_get_status", "topk_status_string", "topk_query_device",
-            "topk_make_plan")
+            "topk_ragged_strided", "topk_gather_sort", "topk_get_status", "topk_status_string",
+            "topk_query_device", "topk_make_plan")
 
 
 class TopkError(RuntimeError):
@@ -123,6 +123,8 @@ def _load():
         lib.topk_ragged_strided.restype = i32
         lib.topk_ragged_strided.argtypes = [vp, i64, i64, i64, vp, i64, i32, i32, vp, vp, vp,
                                             ctypes.POINTER(TopkOptions)]
+        lib.topk_gather_sort.restype = i32
+        lib.topk_gather_sort.argtypes = [vp, i64, i64, i64, i64, i32, vp, vp, i32, vp]
         lib.topk_ragged_static.restype = i32
         lib.topk_ragged_static.argtypes = [vp, i64, vp, i64, i32, i32, vp, vp]
         lib.topk_get_status.restype = i32
@@ -199,6 +201,14 @@ def topk_ragged_strided(logits, row_stride: int, col_stride: int, max_len: int, 
                                            _stream(stream), opt))
 
 
+def topk_gather_sort(logits, row_stride: int, col_stride: int, max_len: int, num_rows: int, topk: int,
+                     out_idx, out_val=None, sort: bool = True, stream=None) -> int:
+    """Values of the selected indices (if out_val is given) and, with sort, rows ordered by
+    value descending then index ascending, -1 last."""
+    return int(_load().topk_gather_sort(_ptr(logits), row_stride, col_stride, max_len, num_rows, topk,
+                                        _ptr(out_idx), _ptr(out_val), 1 if sort else 0, _stream(stream)))
+
+
 def topk_ragged_static(logits, row_stride: int, lengths, num_rows: int, next_n: int, topk: int,
                        out_idx, stream=None) -> int:
     """topk_ragged for callers that cannot allocate: no workspace argument."""
@@ -250,8 +260,10 @@ class Selector:
             raise TopkError(rc, "topk_workspace_init")
 
     def __call__(self, logits, lengths, topk: int, next_n: int | None = None, out=None, stream=None,
-                 options: TopkOptions | None = None):
-        """Top-K indices of every row of a float32 [num_rows, max_len] tensor (any strides).
+                 options: TopkOptions | None = None, sort: bool = False, values: bool = False):
+        """Top-K indices of every row of a float32 [num_rows, max_len] tensor (any strides);
+        with values=True also their values (returns (indices, values)), with sort=True each row
+        ordered by value descending then index ascending, -1 last.
 
         lengths: int32, [num_rows], or [num_rows / next_n, next_n] for MTP, in which
         case next_n is taken from its second dimension (as the pages' launcher does).
@@ -274,7 +286,14 @@ class Selector:
                                  next_n, topk, out, self.workspace, stream, options)
         if rc != TOPK_OK:
             raise TopkError(rc, "topk_ragged")
-        return out
+        if not (sort or values):
+            return out
+        val = torch.empty((num_rows, topk), dtype=torch.float32, device=logits.device) if values else None
+        rc = topk_gather_sort(logits, logits.stride(0), logits.stride(1), max_len, num_rows, topk, out, val,
+                              sort, stream)
+        if rc != TOPK_OK:
+            raise TopkError(rc, "topk_gather_sort")
+        return (out, val) if values else out
 
     def status(self, stream=None) -> int:
         rc, word = topk_get_status(self.workspace, stream)

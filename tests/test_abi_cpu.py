@@ -58,6 +58,12 @@ def test_host_validation_needs_no_gpu(lib):
     assert sar.topk_ragged_strided(fake, -1, 2, 100, fake, 8, 1, 512, fake, fake) == sar.TOPK_ERR_INVALID_ARG
     assert sar.topk_ragged_strided(fake, 1, 8, 100, fake, 8, 1, 0, fake, fake) == sar.TOPK_ERR_UNSUPPORTED_TOPK
     assert sar.topk_ragged_strided(fake, 1, 8, 100, fake, 0, 1, 512, fake, fake) == sar.TOPK_OK
+    # values and order of selected rows
+    assert sar.topk_gather_sort(fake, 100, 0, 100, 8, 512, fake) == sar.TOPK_ERR_INVALID_ARG
+    assert sar.topk_gather_sort(fake, 100, 1, 100, 8, 0, fake) == sar.TOPK_ERR_UNSUPPORTED_TOPK
+    assert sar.topk_gather_sort(fake, 100, 1, 100, 0, 512, fake) == sar.TOPK_OK
+    assert sar.topk_gather_sort(fake, 100, 1, 100, 8, 512, fake, None, sort=False) == sar.TOPK_OK
+    assert sar.topk_gather_sort(fake + 1, 100, 1, 100, 8, 512, fake) == sar.TOPK_ERR_MISALIGNED
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

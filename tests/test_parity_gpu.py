@@ -4,6 +4,7 @@ from __future__ import annotations
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 from tests.gpu_util import Runner, assert_matches_oracle
 
@@ -97,6 +98,51 @@ def test_selector_takes_views_and_two_dimensional_lengths(rn):
     xt = torch.from_numpy(np.ascontiguousarray(w.logits.T)).to(rn.dev).t()
     got = rn.sel(xt, ln2, w.topk).cpu().numpy()
     assert_matches_oracle(w.logits, w.lengths, got, w.topk, 2, label="selector transposed")
+
+
+@pytest.mark.parametrize("name,rows,topk", [("decode_small", 8, 512), ("decode_batch", 6, 2048),
+                                            ("mtp", 4, 1024), ("prefill", 6, 2048), ("decode_batch", 6, 3000),
+                                            ("decode_small", 8, 1)])
+def test_values_and_sorted_rows(rn, name, rows, topk):
+    """topk_gather_sort: the selected values, and rows ordered exactly as the oracle orders them."""
+    torch = rn.torch
+    sar = rn.sar
+    w = workloads.make(name, rows)
+    x = torch.from_numpy(w.logits).to(rn.dev)
+    ln = torch.from_numpy(w.lengths).to(rn.dev)
+    R, S = w.logits.shape
+    out = torch.full((R, topk), -7, dtype=torch.int32, device=rn.dev)
+    assert sar.topk_ragged(x, S, ln, R, w.next_n, topk, out, rn.sel.workspace) == sar.TOPK_OK
+    unsorted = out.clone()
+    val = torch.zeros((R, topk), dtype=torch.float32, device=rn.dev)
+    # values only: indices untouched
+    assert sar.topk_gather_sort(x, S, 1, S, R, topk, out, val, sort=False) == sar.TOPK_OK
+    torch.cuda.synchronize()
+    assert torch.equal(out, unsorted)
+    idx, v = out.cpu().numpy(), val.cpu().numpy()
+    ok = idx >= 0
+    assert np.array_equal(v[ok], w.logits[np.nonzero(ok)[0], idx[ok]]) and np.all(np.isneginf(v[~ok]))
+    # sorted: element by element equal to the oracle's rows (value desc, index asc, -1 last)
+    assert sar.topk_gather_sort(x, S, 1, S, R, topk, out, val, sort=True) == sar.TOPK_OK
+    want, _ = oracle.topk_ragged(w.logits, w.lengths, topk, next_n=w.next_n)
+    got = out.cpu().numpy()
+    assert np.array_equal(got, want), f"{name}: first bad row {np.nonzero((got != want).any(1))[0][:3]}"
+    v = val.cpu().numpy()
+    ok = got >= 0
+    assert np.array_equal(v[ok], w.logits[np.nonzero(ok)[0], got[ok]]) and np.all(np.isneginf(v[~ok]))
+
+
+def test_sorted_rows_of_a_transposed_view_through_the_selector(rn):
+    torch = rn.torch
+    w = workloads.make("decode_batch", 6)
+    xt = torch.from_numpy(np.ascontiguousarray(w.logits.T)).to(rn.dev).t()
+    ln = torch.from_numpy(w.lengths).to(rn.dev)
+    idx, val = rn.sel(xt, ln, w.topk, sort=True, values=True)
+    want, _ = oracle.topk_ragged(w.logits, w.lengths, w.topk)
+    got = idx.cpu().numpy()
+    assert np.array_equal(got, want)
+    ok = got >= 0
+    assert np.array_equal(val.cpu().numpy()[ok], w.logits[np.nonzero(ok)[0], got[ok]])
 
 
 # merge 1: the CTAs of a row merge through the workspace (grid barrier);
