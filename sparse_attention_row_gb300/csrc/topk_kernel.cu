@@ -127,6 +127,8 @@ struct __align__(128) Smem {
   int x_n0;                       // cluster merge: this CTA's buffer size when the merge began
   int x_ln;                       // cluster merge: the leader's buffer size, as read here
   int x_push;                     // cluster merge: entries the other members appended (leader only)
+  int x_hi;                       // cluster merge: highest occupied bin of this CTA (-1: none)
+  int x_top;                      // cluster merge: highest occupied bin of any member
 };
 
 // ---------------------------------------------------------------- primitives
@@ -640,6 +642,7 @@ __device__ void reset_row_state(Smem& s) {
     s.thr_f = key_floor_value(0u);
     s.n_emit = 0;
     s.x_push = 0;  // other members append to a leader only after the next merge's first sync
+    s.x_hi = -1;
   }
 }
 
@@ -1108,9 +1111,21 @@ __device__ __forceinline__ void prepare_finish(Smem& s, int u, int nthreads) {
   }
 }
 
+// Highest bin with a buffered key, into s.x_hi (which starts at -1): thread
+// u of `nthreads` scans its share of the histogram. Bins below the threshold
+// may hold stale counts, but the highest occupied bin is the top key's bin.
+__device__ __forceinline__ void note_highest_bin(Smem& s, int u, int nthreads) {
+  int hi = -1;
+  for (int b = u; b < kBins; b += nthreads)
+    if (s.hist[b] != 0u) hi = b;
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  if (lane_id() == 0 && hi >= 0) atomicMax(&s.x_hi, hi);
+}
+
 // After the last chunk: settle the threshold bin and re-stream the window if
 // the seed kept fewer than K elements. While warp 0 moves the threshold, the
-// other warps prepare the finish. Consumer-wide; ends with a barrier.
+// other warps prepare the finish (and, in a cluster, note the highest occupied
+// bin for the merge). Consumer-wide; ends with a barrier.
 __device__ void close_window(Smem& s, const Params& p, const RowWin& w) {
   csync();
   const int tid = threadIdx.x;
@@ -1118,11 +1133,13 @@ __device__ void close_window(Smem& s, const Params& p, const RowWin& w) {
     advance_threshold(s, p.topk);
   } else {
     prepare_finish(s, tid - 32, kThreads - 32);
+    if (p.cluster) note_highest_bin(s, tid - 32, kThreads - 32);
   }
   csync();
   if (s.thr_lo != 0u && s.cnt_ge < p.topk) {
     restream_row(s, p, w);  // may use the ranking slots; prepare again
     prepare_finish(s, tid, kThreads);
+    if (p.cluster) note_highest_bin(s, tid, kThreads);
     csync();
   }
 }
@@ -1483,16 +1500,17 @@ __device__ __forceinline__ uint32_t merged_count(Smem& s, int b, int m, int G) {
   return c;
 }
 
-// block_find from the top over the members' merged counts of bins >= tmax
-// (those counts are exact; bins below are never reached because the suffix at
-// tmax already holds need). Writes the bin to s.find_b, the count above it to
-// s.find_gt and its own count to s.x_in. Consumer-wide; ends with a barrier.
-__device__ void cluster_find(Smem& s, int tmax, int need, int m, int G) {
+// block_find from the top over the members' merged counts of bins in
+// [tmax, top], top the highest occupied bin of any member (those counts are
+// exact; bins below tmax are never reached because the suffix at tmax already
+// holds need). Writes the bin to s.find_b, the count above it to s.find_gt and
+// its own count to s.x_in. Consumer-wide; ends with a barrier.
+__device__ void cluster_find(Smem& s, int tmax, int top, int need, int m, int G) {
   const int lane = static_cast<int>(lane_id());
   const int warp = threadIdx.x >> 5;
-  const int nblk = (kBins - tmax + 31) >> 5;
+  const int nblk = (top - tmax + 32) >> 5;
   for (int q = warp; q < nblk; q += kWarps) {
-    const int b = kBins - 1 - (32 * q + lane);
+    const int b = top - (32 * q + lane);
     const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, (b >= tmax) ? merged_count(s, b, m, G) : 0u);
     if (lane == 0) s.bsum[q] = sum;
   }
@@ -1528,7 +1546,7 @@ __device__ void cluster_find(Smem& s, int tmax, int need, int m, int G) {
     }
     qsel = __shfl_sync(0xFFFFFFFFu, qsel, L);
     run = __shfl_sync(0xFFFFFFFFu, run, L);
-    const int bin = kBins - 1 - (32 * qsel + lane);
+    const int bin = top - (32 * qsel + lane);
     const uint32_t h = (bin >= tmax) ? merged_count(s, bin, m, G) : 0u;
     uint32_t in2 = h;
 #pragma unroll
@@ -1599,15 +1617,21 @@ __device__ __noinline__ int cluster_merge(Smem& s, const Params& p, int m, uint3
   if (!cluster_sync(s, p, xph)) return -1;  // X1: every window is closed
   if (tid < 32) {
     uint32_t tm = 0;
-    if (tid < G) tm = (tid == m) ? static_cast<uint32_t>(s.t) : dsmem_ld(dsmem_addr(&s.t, static_cast<uint32_t>(tid)));
+    int hi = -1;
+    if (tid < G) {
+      tm = (tid == m) ? static_cast<uint32_t>(s.t) : dsmem_ld(dsmem_addr(&s.t, static_cast<uint32_t>(tid)));
+      hi = (tid == m) ? s.x_hi : static_cast<int>(dsmem_ld(dsmem_addr(&s.x_hi, static_cast<uint32_t>(tid))));
+    }
     tm = __reduce_max_sync(0xFFFFFFFFu, tm);
+    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
     if (tid == 0) {
+      s.x_top = max(hi, static_cast<int>(tm));
       s.x_t = static_cast<int>(tm);
       s.x_ln = (m == 0) ? s.x_n0 : static_cast<int>(dsmem_ld(dsmem_addr(&s.x_n0, 0u)));
     }
   }
   csync();
-  cluster_find(s, s.x_t, p.topk, m, G);
+  cluster_find(s, s.x_t, s.x_top, p.topk, m, G);
   const int ts = s.find_b;
   const int inbin = s.x_in;
   const int tot = s.find_gt + inbin;
