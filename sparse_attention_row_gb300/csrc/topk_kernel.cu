@@ -17,15 +17,26 @@
 //
 // Selection: an exact radix select on the composite key (value bits, then index)
 // finds the K-th candidate (T, I); the output is {key > T} + {key == T, index <=
-// I}, so equal values go to the smaller index. When G > 1 the CTAs of a group
-// merge their histograms through a workspace in global memory, meeting at a
-// group barrier after each radix pass; this replaces the per-row RadixRowState
-// of the persistent_topk kernel (vLLM PR #41444 page, "Executive summary":
-// arrival counter plus histogram per row group). Every workspace word a launch
-// touches is returned to zero before the launch ends, with the fencing that the
-// vLLM PR #41748 page's review asks for ("Code Review": zero in parallel, reset
-// the arrival counter only after the zeros are visible), so no per-call memset
-// is needed and graph replays start from a clean workspace.
+// I}, so equal values go to the smaller index.
+//
+// Split rows (G > 1 CTAs per row) merge in one of two ways. Where the G CTAs
+// form a thread-block cluster, each reads the others' bin counts through
+// distributed shared memory, all find the same threshold bin, and the members
+// append their candidates to the leader's buffer, which then finishes the row
+// as a whole-row CTA would (cluster_merge). Otherwise, or when that union
+// would not fit, the CTAs merge their histograms through a workspace in global
+// memory, meeting at a group barrier after each radix pass (finish_group);
+// this replaces the per-row RadixRowState of the persistent_topk kernel (vLLM
+// PR #41444 page, "Executive summary": arrival counter plus histogram per row
+// group). Every workspace word a launch touches is returned to zero before the
+// launch ends, with the fencing that the vLLM PR #41748 page's review asks for
+// ("Code Review": zero in parallel, reset the arrival counter only after the
+// zeros are visible), so no per-call memset is needed and graph replays start
+// from a clean workspace.
+//
+// Strided logits (a column stride above 1) have no contiguous run to copy: the
+// consumers then read each row from global memory element by element through
+// the unseeded streaming path, and the copy warp stays idle.
 //
 // Keys: an fp32 value x maps to a uint32 whose unsigned order is the order of
 // the values: -0.0 is first mapped to +0.0, then positive values get the sign
