@@ -104,14 +104,20 @@ def read_traffic(workload: str) -> float | None:
     return None
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(csrc: str | None = None) -> str:
+    """Hash of the library's code with comments and blank lines removed, so that
+    a comment edit does not void a DRAM traffic record taken on the same code."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "sparse_attention_row_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "sparse_attention_row_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".h", ".cpp", ".cuh")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+            text = open(os.path.join(csrc, name), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+            h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 
