@@ -130,6 +130,7 @@ struct __align__(128) Smem {
   float thr_f;
   int find_b, find_gt;
   int abort, last, off, take;
+  int full_row;  // the buffer reached its mark: this row is streamed again at its end
   int n_list;
   uint32_t red;
   uint32_t sel_T;
@@ -653,6 +654,7 @@ __device__ void reset_row_state(Smem& s) {
     s.thr_f = key_floor_value(0u);
     s.n_emit = 0;
     s.x_push = 0;  // other members append to a leader only after the next merge's first sync
+    s.full_row = 0;
     s.x_hi = -1;
   }
 }
@@ -974,6 +976,12 @@ __device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, 
   int base = 0;
   if (lane == 0) base = atomicAdd(&s.buf_n, tot);
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  if (base + tot > kBufCap) {
+    // no room: nothing of this reservation is stored and the row is marked
+    // to be streamed again at its end (the warps of a row filter unsynchronised)
+    if (lane == 0) *reinterpret_cast<volatile int*>(&s.full_row) = 1;
+    return;
+  }
   int o = __popc(q0 & lt) + 2 * __popc(q1 & lt) + 4 * __popc(q2 & lt) + 8 * __popc(q3 & lt);
   constexpr int kStaged = (2 * kListCap) / kWarps;  // 16-bit slots per warp in s.emit
   if (tot <= kStaged) {
@@ -1147,7 +1155,7 @@ __device__ void close_window(Smem& s, const Params& p, const RowWin& w) {
     if (p.cluster) note_highest_bin(s, tid - 32, kThreads - 32);
   }
   csync();
-  if (s.thr_lo != 0u && s.cnt_ge < p.topk) {
+  if (s.full_row || (s.thr_lo != 0u && s.cnt_ge < p.topk)) {
     restream_row(s, p, w);  // may use the ranking slots; prepare again
     prepare_finish(s, tid, kThreads);
     if (p.cluster) note_highest_bin(s, tid, kThreads);
@@ -1747,17 +1755,25 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
     }
     const int span = w.hi - w.lo;
     if (p.col_stride != 1) restream_row(s, p, w);  // strided rows: no staging ring
+    // The warps walk the chunks on their own. The only CTA-wide barriers of a
+    // row are the seed's (first chunk) and the row end's, and every warp
+    // reaches all of them whatever its waits returned. A reservation that
+    // would pass the end of the buffer stores nothing and marks the row full;
+    // the warps then skip its remaining chunks and the row is streamed again,
+    // exactly, at its end (the seed aims at 1.25 K survivors and the buffer
+    // holds at least 2 K, so mostly rows of heavy ties get there).
     for (int j = 0; p.col_stride == 1 && j < w.nch; ++j) {
-      if (s.buf_n + kChunk > kBufCap) make_room(s, K);
       const int slot = static_cast<int>(q % kStages);
-      const bool ok = mbar_wait_bounded(&s.full[slot], (q / kStages) & 1u, p.timeout_ns, &s.abort);
+      bool ok = mbar_wait_bounded(&s.full[slot], (q / kStages) & 1u, p.timeout_ns, &s.abort);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok && lane_id() == 0) {
+        s.abort = 1;
+        atomicOr(p.status, 0x4u);
+      }
       const int ws = w.wstart + j * kChunk;
       const int we = min(ws + kChunk, w.wend);
       const int nvec = (we - ws) >> 2;
-      if (!ok) {
-        s.abort = 1;
-        atomicOr(p.status, 0x4u);
-      } else if (j == 0 && span > K) {
+      if (j == 0 && span > K) {
         // seed: histogram the first chunk, aim the threshold at ~1.25 K survivors
         // over the window (exactly K when the window is this one chunk)
         hist_chunk(s, s.stage[slot], ws, nvec, w.lo, w.hi);
@@ -1779,18 +1795,20 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
           set_threshold(s, static_cast<uint32_t>(s.find_b) << 20);
         }
         csync();
-        filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
-      } else {
-        filter_chunk<true, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
+        if (ok) filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
+      } else if (ok) {
+        // warp-uniform: the filter's ballots need every lane
+        if (!__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s.full_row) != 0))
+          filter_chunk<true, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
       }
       __syncwarp();
       if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
       ++q;
-      csync();
-      if (s.abort) {
-        aborted = true;
-        break;
-      }
+    }
+    csync();
+    if (s.abort) {
+      aborted = true;
+      break;
     }
     if (aborted) break;
     close_window(s, p, w);
