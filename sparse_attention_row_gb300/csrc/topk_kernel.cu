@@ -98,6 +98,15 @@ constexpr int kBufCap = 12288;  // candidate (key, index) pairs kept per CTA
 constexpr int kMinBlocks = 1;
 #endif
 constexpr int kWarps = kThreads / 32;
+// Warp groups of the streaming loop: group g filters exactly the chunks staged
+// in ring slot g, so each group waits on its own slot's phases in order and a
+// warp filters a whole chunk's share of kChunk / (4 * kGroupThreads) float4 per
+// lane (every warp still reads the seed chunk of a row for its histogram).
+constexpr int kGroups = (kWarps % kStages == 0) ? kStages : 1;
+constexpr int kGroupWarps = kWarps / kGroups;
+constexpr int kGroupThreads = kGroupWarps * 32;
+static_assert(kChunk % (4 * kGroupThreads) == 0 && kChunk / (4 * kGroupThreads) <= 8,
+              "a group's share of a chunk fits one 32-bit survivor mask per lane");
 constexpr int kCtaThreads = kThreads + 32;  // plus one copy-issuing warp
 static_assert(kCtaThreads == (LTK_SHAPE_PAIR ? kPairCtaThreads : LTK_SHAPE_SMALL ? kSmallCtaThreads : kWideCtaThreads),
               "shape constants agree");
@@ -157,6 +166,22 @@ __device__ __forceinline__ uint64_t global_timer() {
 
 // Barrier among the consumer warps only (the copy warp never joins it).
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
+
+// Consumer barrier that also ORs a predicate over the consumer threads: every
+// thread gets the same answer, so a decision taken from it is uniform even when
+// the state it was computed from changes right after the barrier.
+__device__ __forceinline__ bool csync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(kThreads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
@@ -805,7 +830,7 @@ __device__ __noinline__ void make_room(Smem& s, int K) {
   csync();
   const uint32_t t = static_cast<uint32_t>(s.t);
   compact_buffer(s, [=](uint32_t k, int32_t) { return (k >> 20) >= t; });
-  if (s.buf_n + kChunk > kBufCap) compact_exact(s, K);
+  if (csync_or(threadIdx.x == 0 && s.buf_n + kChunk > kBufCap)) compact_exact(s, K);
 }
 
 // ----------------------------------------------------------------- row plans
@@ -936,43 +961,60 @@ __device__ __noinline__ void producer_loop(const Params& p, Smem& s, int g, int 
 
 // ------------------------------------------------------------- chunk filter
 
+// Bits of the elements of f (window elements i0 .. i0 + 3) at or above thr,
+// elements outside [lo, hi) cleared unless the whole chunk is inside.
+__device__ __forceinline__ uint32_t quad_bits(const float4 f, float thr, bool interior, int i0, int lo, int hi) {
+  uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) | (f.w >= thr ? 8u : 0u);
+  if (!interior) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (i0 + e < lo || i0 + e >= hi) b &= ~(1u << e);
+  }
+  return b;
+}
+
+template <bool kCount, bool kGlobal, int kT>
+__device__ __forceinline__ bool append_survivors(Smem& s, uint32_t m, const float* src, int ws, int tid);
+
 // Filters one chunk of a row window against the running threshold: one fp32
 // compare per element; a warp reserves buffer space once; only survivors are
 // converted to keys, stored and (with kCount) counted in the histogram.
-// src holds the window's elements [ws, ws + 4*nvec) (shared or global memory).
-template <bool kCount, bool kGlobal>
-__device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, int nvec, int lo, int hi) {
-  constexpr int V = kChunk / (4 * kThreads);
-  const int tid = threadIdx.x;
-  const int lane = static_cast<int>(lane_id());
+// src holds the window's elements [ws, ws + 4*nvec) (shared or global memory);
+// thread tid of kT takes float4 tid, tid + kT, ... Returns whether the warp
+// appended (or tried to append) any.
+template <bool kCount, bool kGlobal, int kT = kThreads>
+__device__ __forceinline__ bool filter_chunk(Smem& s, const float* src, int ws, int nvec, int lo, int hi,
+                                             int tid = threadIdx.x) {
   const float thr = s.thr_f;
   const float4* s4 = reinterpret_cast<const float4*>(src);
   const bool interior = ws >= lo && ws + 4 * nvec <= hi;
   uint32_t m = 0;
 #pragma unroll
-  for (int v = 0; v < V; ++v) {
-    const int vi = tid + v * kThreads;
-    if (vi < nvec) {
-      const float4 f = kGlobal ? __ldg(s4 + vi) : s4[vi];
-      uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
-                   (f.w >= thr ? 8u : 0u);
-      if (!interior) {
-        const int i0 = ws + 4 * vi;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (i0 + e < lo || i0 + e >= hi) b &= ~(1u << e);
-      }
-      m |= b << (4 * v);
-    }
+  for (int v = 0; v < kChunk / (4 * kT); ++v) {
+    const int vi = tid + v * kT;
+    if (vi < nvec)
+      m |= quad_bits(kGlobal ? __ldg(s4 + vi) : s4[vi], thr, interior, ws + 4 * vi, lo, hi) << (4 * v);
   }
+  return append_survivors<kCount, kGlobal, kT>(s, m, src, ws, tid);
+}
+
+// Appends the elements of a thread's share marked in m (bit 4v + e: element e
+// of float4 tid + v * kT) to the buffer.
+template <bool kCount, bool kGlobal, int kT>
+__device__ __forceinline__ bool append_survivors(Smem& s, uint32_t m, const float* src, int ws, int tid) {
+  constexpr int V = kChunk / (4 * kT);
+  // bits of a lane's survivor count (at most 4 V)
+  constexpr int kCB = (4 * V >= 32) ? 6 : (4 * V >= 16) ? 5 : (4 * V >= 8) ? 4 : (4 * V >= 4) ? 3 : 2;
+  const int lane = static_cast<int>(lane_id());
   const int c = __popc(m);
   const uint32_t lt = lanemask_lt();
-  const uint32_t q0 = __ballot_sync(0xFFFFFFFFu, c & 1);
-  const uint32_t q1 = __ballot_sync(0xFFFFFFFFu, c & 2);
-  const uint32_t q2 = __ballot_sync(0xFFFFFFFFu, c & 4);
-  const uint32_t q3 = __ballot_sync(0xFFFFFFFFu, c & 8);
-  const int tot = __popc(q0) + 2 * __popc(q1) + 4 * __popc(q2) + 8 * __popc(q3);
-  if (tot == 0) return;
+  uint32_t qb[kCB];
+#pragma unroll
+  for (int b = 0; b < kCB; ++b) qb[b] = __ballot_sync(0xFFFFFFFFu, (c >> b) & 1);
+  int tot = 0;
+#pragma unroll
+  for (int b = 0; b < kCB; ++b) tot += __popc(qb[b]) << b;
+  if (tot == 0) return false;
   int base = 0;
   if (lane == 0) base = atomicAdd(&s.buf_n, tot);
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
@@ -980,19 +1022,21 @@ __device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, 
     // no room: nothing of this reservation is stored and the row is marked
     // to be streamed again at its end (the warps of a row filter unsynchronised)
     if (lane == 0) *reinterpret_cast<volatile int*>(&s.full_row) = 1;
-    return;
+    return true;
   }
-  int o = __popc(q0 & lt) + 2 * __popc(q1 & lt) + 4 * __popc(q2 & lt) + 8 * __popc(q3 & lt);
+  int o = 0;
+#pragma unroll
+  for (int b = 0; b < kCB; ++b) o += __popc(qb[b] & lt) << b;
   constexpr int kStaged = (2 * kListCap) / kWarps;  // 16-bit slots per warp in s.emit
   if (tot <= kStaged) {
     // each lane only notes where its survivors are (a short divergent loop);
     // the whole warp then converts and stores them, 32 at a time. s.emit is
     // idle while a row streams, so it holds the per-warp lists.
-    uint16_t* stg = reinterpret_cast<uint16_t*>(s.emit) + (tid >> 5) * kStaged;
+    uint16_t* stg = reinterpret_cast<uint16_t*>(s.emit) + (threadIdx.x >> 5) * kStaged;
     while (m) {
       const int j = __ffs(m) - 1;
       m &= m - 1;
-      stg[o++] = static_cast<uint16_t>(4 * (tid + (j >> 2) * kThreads) + (j & 3));
+      stg[o++] = static_cast<uint16_t>(4 * (tid + (j >> 2) * kT) + (j & 3));
     }
     __syncwarp();
     for (int e = lane; e < tot; e += 32) {
@@ -1004,13 +1048,13 @@ __device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, 
       if (kCount) atomicAdd(&s.hist[k >> 20], 1u);
     }
     __syncwarp();
-    return;
+    return true;
   }
   o += base;
   while (m) {
     const int j = __ffs(m) - 1;
     m &= m - 1;
-    const int off = 4 * (tid + (j >> 2) * kThreads) + (j & 3);
+    const int off = 4 * (tid + (j >> 2) * kT) + (j & 3);
     const uint32_t k = fkey(kGlobal ? __ldg(src + off) : src[off]);
     const int oo = min(o, kBufCap - 1);
     s.bkey[oo] = k;
@@ -1018,11 +1062,12 @@ __device__ __forceinline__ void filter_chunk(Smem& s, const float* src, int ws, 
     if (kCount) atomicAdd(&s.hist[k >> 20], 1u);
     ++o;
   }
+  return true;
 }
 
 // filter_chunk for strided rows read straight from global memory: element e
 // of the window is rowp[e * col_stride], loaded only inside [lo, hi).
-__device__ __forceinline__ void filter_chunk_strided(Smem& s, const float* rowp, int64_t cs, int ws, int nvec,
+__device__ __forceinline__ bool filter_chunk_strided(Smem& s, const float* rowp, int64_t cs, int ws, int nvec,
                                                      int lo, int hi) {
   constexpr int V = kChunk / (4 * kThreads);
   const int tid = threadIdx.x;
@@ -1050,7 +1095,7 @@ __device__ __forceinline__ void filter_chunk_strided(Smem& s, const float* rowp,
   const uint32_t q2 = __ballot_sync(0xFFFFFFFFu, c & 4);
   const uint32_t q3 = __ballot_sync(0xFFFFFFFFu, c & 8);
   const int tot = __popc(q0) + 2 * __popc(q1) + 4 * __popc(q2) + 8 * __popc(q3);
-  if (tot == 0) return;
+  if (tot == 0) return false;
   int base = 0;
   if (lane == 0) base = atomicAdd(&s.buf_n, tot);
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
@@ -1066,6 +1111,7 @@ __device__ __forceinline__ void filter_chunk_strided(Smem& s, const float* rowp,
     atomicAdd(&s.hist[k >> 20], 1u);
     ++o;
   }
+  return true;
 }
 
 // Histograms the keys of one staged chunk (elements inside [lo, hi)).
@@ -1090,21 +1136,25 @@ __device__ __forceinline__ void hist_chunk(Smem& s, const float* src, int ws, in
 // seed: every element starts eligible and the threshold rises as candidates
 // accumulate. Used when a seeded pass kept fewer than K elements, and for
 // every row of strided logits (no bulk copies there).
+// The threshold moves only after a chunk that added candidates, and once at
+// the end.
 __device__ __noinline__ void restream_row(Smem& s, const Params& p, const RowWin w) {
   csync();
   reset_row_state(s);
   csync();
+  // Every chunk starts with room for a whole chunk (make_room keeps at most
+  // TopK + what a compaction leaves, and TopK + a chunk fits the buffer).
   for (int j = 0; j < w.nch; ++j) {
-    if (s.buf_n + kChunk > kBufCap) make_room(s, p.topk);
     const int ws = w.wstart + j * kChunk;
     const int we = min(ws + kChunk, w.wend);
-    if (p.col_stride == 1)
-      filter_chunk<true, true>(s, w.rowp + ws, ws, (we - ws) >> 2, w.lo, w.hi);
-    else
-      filter_chunk_strided(s, w.rowp, p.col_stride, ws, (we - ws) >> 2, w.lo, w.hi);
-    csync();
-    if (threadIdx.x < 32) advance_threshold(s, p.topk);
-    csync();
+    const bool added = p.col_stride == 1
+                           ? filter_chunk<true, true>(s, w.rowp + ws, ws, (we - ws) >> 2, w.lo, w.hi)
+                           : filter_chunk_strided(s, w.rowp, p.col_stride, ws, (we - ws) >> 2, w.lo, w.hi);
+    if (csync_or(added) || j + 1 == w.nch) {
+      if (threadIdx.x < 32) advance_threshold(s, p.topk);
+      // thread 0 reads the count while every other thread waits at the barrier
+      if (csync_or(threadIdx.x == 0 && s.buf_n + kChunk > kBufCap) && j + 1 < w.nch) make_room(s, p.topk);
+    }
   }
 }
 
@@ -1700,7 +1750,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
     s.abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&s.full[i], 1u);
-      mbar_init(&s.empty[i], kWarps);
+      mbar_init(&s.empty[i], kGroupWarps);
     }
     if (p.cluster) {
       mbar_init(&s.xbar[0], static_cast<uint32_t>(p.G));
@@ -1733,6 +1783,8 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
   }
 
   const int K = p.topk;
+  const int grp = (tid >> 5) / kGroupWarps;  // the ring slot this warp's group filters
+  const int gtid = tid - grp * kGroupThreads;
   uint32_t q = 0;  // chunks consumed
   uint32_t epoch = 0;
   uint32_t xph = 0;       // cluster merge syncs passed
@@ -1745,25 +1797,34 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
     if (w.len <= K) {
       if (m == 0) write_trivial_row(p, w.r, w.len);
       if (p.G == 1 && k == 0 && p.col_stride == 1) {
-        // discard the early copy the copy warp issued for this row
-        if (!mbar_wait_bounded(&s.full[0], 0u, p.timeout_ns, &s.abort)) atomicOr(p.status, 0x4u);
-        __syncwarp();
-        if (lane_id() == 0) mbar_arrive(&s.empty[0]);
+        // slot 0's group discards the early copy the copy warp issued for this row
+        if (grp == 0) {
+          if (!mbar_wait_bounded(&s.full[0], 0u, p.timeout_ns, &s.abort)) atomicOr(p.status, 0x4u);
+          __syncwarp();
+          if (lane_id() == 0) mbar_arrive(&s.empty[0]);
+        }
         q = 1;
       }
       continue;
     }
     const int span = w.hi - w.lo;
     if (p.col_stride != 1) restream_row(s, p, w);  // strided rows: no staging ring
-    // The warps walk the chunks on their own. The only CTA-wide barriers of a
-    // row are the seed's (first chunk) and the row end's, and every warp
-    // reaches all of them whatever its waits returned. A reservation that
-    // would pass the end of the buffer stores nothing and marks the row full;
-    // the warps then skip its remaining chunks and the row is streamed again,
-    // exactly, at its end (the seed aims at 1.25 K survivors and the buffer
-    // holds at least 2 K, so mostly rows of heavy ties get there).
-    for (int j = 0; p.col_stride == 1 && j < w.nch; ++j) {
+    // The warps walk the chunks on their own, each group the chunks of its
+    // ring slot. The only CTA-wide barriers of a row are the seed's (first
+    // chunk, read by every warp) and the row end's, and every warp reaches all
+    // of them whatever its waits returned. A warp waits on another group's
+    // slot only for a seed chunk, after the barrier that ended the previous
+    // row, when that slot's earlier phases have all completed. A reservation
+    // that would pass the end of the buffer stores nothing and marks the row
+    // full; the warps then skip its remaining chunks and the row is streamed
+    // again, exactly, at its end (the seed aims at 1.25 K survivors and the
+    // buffer holds at least 2 K, so mostly rows of heavy ties get there).
+    bool release_late = false;
+    for (int j = 0; p.col_stride == 1 && j < w.nch; ++j, ++q) {
       const int slot = static_cast<int>(q % kStages);
+      const bool seed = j == 0 && span > K;
+      const bool mine = kGroups == 1 || slot == grp;
+      if (!seed && !mine) continue;
       bool ok = mbar_wait_bounded(&s.full[slot], (q / kStages) & 1u, p.timeout_ns, &s.abort);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok && lane_id() == 0) {
@@ -1773,7 +1834,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
       const int ws = w.wstart + j * kChunk;
       const int we = min(ws + kChunk, w.wend);
       const int nvec = (we - ws) >> 2;
-      if (j == 0 && span > K) {
+      if (seed) {
         // seed: histogram the first chunk, aim the threshold at ~1.25 K survivors
         // over the window (exactly K when the window is this one chunk)
         hist_chunk(s, s.stage[slot], ws, nvec, w.lo, w.hi);
@@ -1795,18 +1856,34 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
           set_threshold(s, static_cast<uint32_t>(s.find_b) << 20);
         }
         csync();
-        if (ok) filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
+        if (w.nch == 1) {
+          // a one-chunk window: every warp filters it and the slot is released
+          // after the row-end barrier
+          if (ok) filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
+          release_late = mine;
+          continue;
+        }
+        if (ok && mine) filter_chunk<false, false, kGroupThreads>(s, s.stage[slot], ws, nvec, w.lo, w.hi, gtid);
       } else if (ok) {
         // warp-uniform: the filter's ballots need every lane
         if (!__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s.full_row) != 0))
-          filter_chunk<true, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
+          filter_chunk<true, false, kGroupThreads>(s, s.stage[slot], ws, nvec, w.lo, w.hi, gtid);
       }
-      __syncwarp();
-      if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
-      ++q;
+      if (mine) {
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
+      }
     }
     csync();
-    if (s.abort) {
+    // uniform: s.abort is next written in a later row's chunk loop, which a
+    // warp reaches only through close_window's first barrier, after every
+    // warp has read it here
+    const bool abort_row = s.abort != 0;
+    if (release_late) {
+      if (lane_id() == 0) mbar_arrive(&s.empty[static_cast<int>((q - 1) % kStages)]);
+      release_late = false;
+    }
+    if (abort_row) {
       aborted = true;
       break;
     }
