@@ -6,7 +6,7 @@
 // cooperative grid deadlocks (same page, "Feature and motivation": TopK=1024,
 // MTP=1). Here the plan is a pure function of the device properties, so the
 // bound can be checked on made-up devices, and the launch that waits across
-// CTAs is a cooperative launch, which the driver refuses rather than hangs if
+// CTAs is a cooperative launch, which the CUDA driver refuses rather than hangs if
 // the grid cannot be resident.
 //
 // Shape rules:
