@@ -1823,23 +1823,23 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
     // again, exactly, at its end (the seed aims at 1.25 K survivors and the
     // buffer holds at least 2 K, so mostly rows of heavy ties get there).
     bool release_late = false;
-    for (int j = 0; p.col_stride == 1 && j < w.nch; ++j, ++q) {
-      const int slot = static_cast<int>(q % kStages);
-      const bool seed = j == 0 && span > K;
-      const bool mine = kGroups == 1 || slot == grp;
-      if (!seed && !mine) continue;
-      bool ok = mbar_wait_bounded(&s.full[slot], (q / kStages) & 1u, p.timeout_ns, &s.abort);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok && lane_id() == 0) {
-        s.abort = 1;
-        atomicOr(p.status, 0x4u);
-      }
-      const int ws = w.wstart + j * kChunk;
-      const int we = min(ws + kChunk, w.wend);
-      const int nvec = (we - ws) >> 2;
-      if (seed) {
-        // seed: histogram the first chunk, aim the threshold at ~1.25 K survivors
-        // over the window (exactly K when the window is this one chunk)
+    if (p.col_stride == 1 && w.nch > 0) {
+      const uint32_t q0 = q;  // ring position of the window's chunk 0
+      int j = 0;
+      if (span > K) {
+        // seed: every warp histograms the first chunk, and the threshold aims at
+        // ~1.25 K survivors over the window (exactly K when it is this one chunk)
+        const int slot = static_cast<int>(q0 % kStages);
+        const bool mine = kGroups == 1 || slot == grp;
+        bool ok = mbar_wait_bounded(&s.full[slot], (q0 / kStages) & 1u, p.timeout_ns, &s.abort);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok && lane_id() == 0) {
+          s.abort = 1;
+          atomicOr(p.status, 0x4u);
+        }
+        const int ws = w.wstart;
+        const int we = min(ws + kChunk, w.wend);
+        const int nvec = (we - ws) >> 2;
         hist_chunk(s, s.stage[slot], ws, nvec, w.lo, w.hi);
         const int in_chunk = min(w.hi, we) - max(w.lo, ws);
         int target = K;
@@ -1864,18 +1864,42 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
           // after the row-end barrier
           if (ok) filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
           release_late = mine;
-          continue;
+        } else if (mine) {
+          if (ok) filter_chunk<false, false, kGroupThreads>(s, s.stage[slot], ws, nvec, w.lo, w.hi, gtid);
+          __syncwarp();
+          if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
         }
-        if (ok && mine) filter_chunk<false, false, kGroupThreads>(s, s.stage[slot], ws, nvec, w.lo, w.hi, gtid);
-      } else if (ok) {
-        // warp-uniform: the filter's ballots need every lane
-        if (!__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s.full_row) != 0))
-          filter_chunk<true, false, kGroupThreads>(s, s.stage[slot], ws, nvec, w.lo, w.hi, gtid);
+        j = 1;
       }
-      if (mine) {
+      // then the group's own chunks: ring positions q0 + j stepping by kGroups,
+      // all in slot grp when the groups own the slots
+      if (kGroups > 1)
+        j += static_cast<int>((static_cast<uint32_t>(grp) + kStages - (q0 + j) % kStages) % kStages);
+      int slot = static_cast<int>((q0 + j) % kStages);
+      uint32_t par = ((q0 + j) / kStages) & 1u;
+      for (; j < w.nch; j += kGroups) {
+        bool ok = mbar_wait_bounded(&s.full[slot], par, p.timeout_ns, &s.abort);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok && lane_id() == 0) {
+          s.abort = 1;
+          atomicOr(p.status, 0x4u);
+        }
+        // warp-uniform: the filter's ballots need every lane
+        if (ok && !__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s.full_row) != 0)) {
+          const int ws = w.wstart + j * kChunk;
+          const int we = min(ws + kChunk, w.wend);
+          filter_chunk<true, false, kGroupThreads>(s, s.stage[slot], ws, (we - ws) >> 2, w.lo, w.hi, gtid);
+        }
         __syncwarp();
         if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
+        if (kGroups == kStages) {
+          par ^= 1u;  // the next own chunk is one lap later in the same slot
+        } else if (++slot == kStages) {
+          slot = 0;
+          par ^= 1u;
+        }
       }
+      q = q0 + static_cast<uint32_t>(w.nch);
     }
     csync();
     // uniform: s.abort is next written in a later row's chunk loop, which a
