@@ -102,10 +102,16 @@ constexpr int kMinBlocks = 1;
 #endif
 constexpr int kWarps = kThreads / 32;
 // Warp groups of the streaming loop: group g filters exactly the chunks staged
-// in ring slot g, so each group waits on its own slot's phases in order and a
-// warp filters a whole chunk's share of kChunk / (4 * kGroupThreads) float4 per
-// lane (every warp still reads the seed chunk of a row for its histogram).
-constexpr int kGroups = (kWarps % kStages == 0) ? kStages : 1;
+// in the ring slots s with s % kGroups == g, so each group waits on its own
+// slots' phases in order and a warp filters a whole chunk's share of
+// kChunk / (4 * kGroupThreads) float4 per lane (every warp still reads the
+// seed chunk of a row for its histogram).
+// Paired shape: 3 groups of 4 warps, one slot each. Wide shape: 2 groups of
+// 12 warps, two slots each, so a group's next chunk is in flight while it
+// filters one (measured faster than 4 groups of 6 on split rows). Small
+// shape: one group (8 warps do not divide into its 3 slots).
+constexpr int kGroups = LTK_SHAPE_PAIR ? kStages : (LTK_SHAPE_SMALL ? 1 : 2);
+static_assert(kStages % kGroups == 0 && kWarps % kGroups == 0, "groups own whole slots and whole warps");
 constexpr int kGroupWarps = kWarps / kGroups;
 constexpr int kGroupThreads = kGroupWarps * 32;
 static_assert(kChunk % (4 * kGroupThreads) == 0 && kChunk / (4 * kGroupThreads) <= 8,
@@ -1786,7 +1792,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
   }
 
   const int K = p.topk;
-  const int grp = (tid >> 5) / kGroupWarps;  // the ring slot this warp's group filters
+  const int grp = (tid >> 5) / kGroupWarps;  // this warp's group: it filters the slots s with s % kGroups == grp
   const int gtid = tid - grp * kGroupThreads;
   uint32_t q = 0;  // chunks consumed
   uint32_t epoch = 0;
@@ -1830,7 +1836,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
         // seed: every warp histograms the first chunk, and the threshold aims at
         // ~1.25 K survivors over the window (exactly K when it is this one chunk)
         const int slot = static_cast<int>(q0 % kStages);
-        const bool mine = kGroups == 1 || slot == grp;
+        const bool mine = slot % kGroups == grp;
         bool ok = mbar_wait_bounded(&s.full[slot], (q0 / kStages) & 1u, p.timeout_ns, &s.abort);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok && lane_id() == 0) {
@@ -1871,10 +1877,10 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
         }
         j = 1;
       }
-      // then the group's own chunks: ring positions q0 + j stepping by kGroups,
-      // all in slot grp when the groups own the slots
+      // then the group's own chunks: ring positions q0 + j stepping by kGroups
+      // (slot % kGroups == grp; kGroups divides kStages)
       if (kGroups > 1)
-        j += static_cast<int>((static_cast<uint32_t>(grp) + kStages - (q0 + j) % kStages) % kStages);
+        j += static_cast<int>((static_cast<uint32_t>(grp) + kGroups - (q0 + j) % kGroups) % kGroups);
       int slot = static_cast<int>((q0 + j) % kStages);
       uint32_t par = ((q0 + j) / kStages) & 1u;
       for (; j < w.nch; j += kGroups) {
@@ -1892,10 +1898,9 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
         }
         __syncwarp();
         if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
-        if (kGroups == kStages) {
-          par ^= 1u;  // the next own chunk is one lap later in the same slot
-        } else if (++slot == kStages) {
-          slot = 0;
+        slot += kGroups;  // the next own chunk; past the last slot it is the next lap
+        if (slot >= kStages) {
+          slot -= kStages;
           par ^= 1u;
         }
       }
