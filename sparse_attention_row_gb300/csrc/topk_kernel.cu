@@ -10,8 +10,8 @@
 // of the keys and seeds a threshold aimed at about 1.25 K survivors over the
 // whole row. Every later element costs one fp32 compare against that threshold;
 // only survivors become (key, index) candidates in shared memory. The consumer
-// warps form one group per ring slot and each group filters the chunks of its
-// slot on its own, with no CTA-wide barrier between chunks. At the end of the
+// warps form groups that own ring slots, and each group filters the chunks of
+// its slots on its own, with no CTA-wide barrier between chunks. At the end of the
 // row the seed is verified: if fewer than K elements reached it, or the
 // candidates outgrew the buffer (heavy ties at the seed's bin), the row is
 // streamed again in index order with no seed (exact whatever the data); there a
