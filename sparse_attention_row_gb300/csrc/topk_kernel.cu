@@ -153,6 +153,8 @@ struct __align__(128) Smem {
   uint32_t red;
   uint32_t sel_T;
   int sel_I;
+  uint32_t run_kmin, run_kmax;  // tied_run's extremes
+  int run_imin, run_imax;
   int x_t, x_in;                  // cluster merge: t_max, then the count in bin t*
   int x_n0;                       // cluster merge: this CTA's buffer size when the merge began
   int x_ln;                       // cluster merge: the leader's buffer size, as read here
@@ -812,15 +814,63 @@ __device__ void compact_buffer(Smem& s, Keep keep) {
 // Keeps exactly the K best buffered candidates and raises the filter to
 // (K-th key) + 1: a later element equal to that key has a larger index than
 // every kept one, so it can never be selected.
+// A buffer whose keys are all equal and whose n indices form the contiguous run
+// [i0, i0 + n) (n distinct indices spanning n values) holds ties only, and by
+// the tie rule its K best are i0 .. i0 + K - 1. One pass finds the key and
+// index extremes; returns whether that holds (then T, I describe the K best).
+// Consumer-wide; every thread gets the same answer.
+__device__ bool tied_run(Smem& s, int K, uint32_t& T, int& I) {
+  const int tid = threadIdx.x;
+  csync();
+  if (tid == 0) {
+    s.run_kmin = 0xFFFFFFFFu;
+    s.run_kmax = 0u;
+    s.run_imin = 0x7FFFFFFF;
+    s.run_imax = -1;
+  }
+  csync();
+  const int n = s.buf_n;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  int imin = 0x7FFFFFFF, imax = -1;
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t k = s.bkey[i];
+    const int x = s.bidx[i];
+    kmin = min(kmin, k);
+    kmax = max(kmax, k);
+    imin = min(imin, x);
+    imax = max(imax, x);
+  }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  imin = __reduce_min_sync(0xFFFFFFFFu, imin);
+  imax = __reduce_max_sync(0xFFFFFFFFu, imax);
+  if (lane_id() == 0) {
+    atomicMin(&s.run_kmin, kmin);
+    atomicMax(&s.run_kmax, kmax);
+    atomicMin(&s.run_imin, imin);
+    atomicMax(&s.run_imax, imax);
+  }
+  csync();
+  T = s.run_kmin;
+  I = s.run_imin + K - 1;
+  return n >= K && s.run_kmin == s.run_kmax &&
+         static_cast<int64_t>(s.run_imax) - static_cast<int64_t>(s.run_imin) + 1 == n;
+}
+
 __device__ __noinline__ void compact_exact(Smem& s, int K) {
   uint32_t T;
   int I;
-  select_threshold(s, K, T, I);
+  const bool run = tied_run(s, K, T, I);
+  if (!run) select_threshold(s, K, T, I);
   compact_buffer(s, [=](uint32_t k, int32_t i) { return k > T || (k == T && i <= I); });
   for (int b = threadIdx.x; b < kBins; b += kThreads) s.hist[b] = 0;
   csync();
   const int n = s.buf_n;
-  for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&s.hist[s.bkey[i] >> 20], 1u);
+  if (run) {
+    if (threadIdx.x == 0) s.hist[T >> 20] = static_cast<uint32_t>(n);  // all kept keys are T
+  } else {
+    for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&s.hist[s.bkey[i] >> 20], 1u);
+  }
   csync();
   if (threadIdx.x == 0) {
     s.buf_mark = n;
