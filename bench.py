@@ -2,6 +2,14 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workloads a,b]
 
+Multi-GPU: rows are independent, so every rank runs the whole workload as a
+replica on its own GPU (weak scaling: per-GPU work is fixed as N grows) and no
+collective touches the data path; ``value`` is the rows of all ranks divided by
+the slowest rank's time. Under torchrun the ranks come from the environment;
+``--gpus N`` without a launcher spawns the N ranks itself (one process per
+GPU, NCCL for the timing barrier and the max over ranks). ``--dry-run`` runs
+that launch and aggregation with zero-work steps and no GPU (gloo), for tests.
+
 A step is one topk_ragged call over one batch of the workload (all of the
 hot path: load + key + filter + radix select + gather in one kernel launch).
 The headline workload is the decode batch: 64 rows, lengths uniform in
@@ -54,6 +62,52 @@ DESCR = {
 
 
 # --------------------------------------------------------------------- helpers
+
+def free_port() -> int:
+    import socket
+
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    return port
+
+
+def _rank_entry(rank: int, world: int, port: int, argv: list[str]) -> None:
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world), LOCAL_WORLD_SIZE=str(world),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    main(argv)
+
+
+def launch_ranks(world: int, argv: list[str]) -> int:
+    """Spawns `world` ranks of this benchmark on this node (one process per GPU) and returns
+    the worst exit code; rank 0 prints the JSON line."""
+    import multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    port = free_port()
+    procs = [ctx.Process(target=_rank_entry, args=(r, world, port, argv)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    for pr in procs:
+        pr.join()
+    return max(abs(pr.exitcode or 0) for pr in procs)
+
+
+def init_dist(world: int, local: int) -> None:
+    """One process group for the timing barrier and the max over ranks: NCCL between GPUs,
+    gloo where there is no GPU (the dry run)."""
+    if world <= 1:
+        return
+    import torch
+    import torch.distributed as dist
+
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        dist.init_process_group("gloo")
+
 
 def dist_env() -> tuple[int, int, int]:
     rank = int(os.environ.get("RANK", "0"))
@@ -361,15 +415,33 @@ def run_only(args) -> None:
                       "frac_of_hbm_peak": gbs / peak, "steps": args.steps}), flush=True)
 
 
+def run_dry(args) -> None:
+    """The multi-rank launch and aggregation with zero-work steps (no GPU needed)."""
+    rank, world, local = dist_env()
+    init_dist(world, local)
+    import torch
+
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    barrier(world)
+    t0 = time.perf_counter()
+    barrier(world)
+    el = max_over_ranks(time.perf_counter() - t0, world, dev)
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "metric": METRIC, "value": None, "unit": "rows/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "scaling": "weak",
+                          "max_rank_wall_s": el, "config": {"parallelism": f"replica per GPU x{world}"}}),
+              flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def run_ours(args) -> None:
     rank, world, local = dist_env()
     import torch
 
-    if world > 1:
-        import torch.distributed as dist
-
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+    init_dist(world, local)
     gb = GpuBench(local)
     peak, peak_src = read_peaks()
 
@@ -466,9 +538,15 @@ def main(argv=None) -> None:
     ap.add_argument("--cpu-budget", type=float, default=3.0, help="seconds of oracle wall time")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timings")
     ap.add_argument("--only", default="", help="time only this workload's kernel (profiling runs)")
-    args = ap.parse_args(argv)
+    ap.add_argument("--dry-run", action="store_true", help="launch and aggregate with zero-work steps, no GPU")
+    raw = list(sys.argv[1:] if argv is None else argv)
+    args = ap.parse_args(raw)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.impl == "ours":
+        sys.exit(launch_ranks(args.gpus, raw))  # no launcher: spawn one rank per GPU
+    if args.dry_run:
+        run_dry(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.only:
         run_only(args)

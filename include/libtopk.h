@@ -60,6 +60,11 @@ typedef enum {
 #define TOPK_DEV_LENGTH_CLAMPED 0x1u  /* a length < 0 was read as 0, or > row_stride as row_stride */
 #define TOPK_DEV_BARRIER_TIMEOUT 0x2u /* a CTA of a row group waited longer than the barrier limit */
 #define TOPK_DEV_STAGE_TIMEOUT 0x4u   /* a staging copy did not land within the limit */
+/* A launch that splits rows found TOPK_DEV_BARRIER_TIMEOUT or TOPK_DEV_STAGE_TIMEOUT
+ * already set: the timed-out launch left the workspace's group words as they were,
+ * so this launch wrote rows of -1 instead of merging through them. Every such
+ * launch does the same until topk_workspace_init clears the workspace. */
+#define TOPK_DEV_WORKSPACE_DIRTY 0x8u
 
 /* Tuning and test knobs for topk_ragged_ex. Zero-initialise, then set fields. */
 typedef struct {
@@ -69,9 +74,13 @@ typedef struct {
   int64_t long_row_threshold;
   /* 0 = default (1 s); limit of every device-side wait, in microseconds. */
   uint32_t barrier_timeout_us;
-  /* Test only. 1 = CTA 1 of row group 0 leaves before its first group barrier,
-   * so the other CTAs' waits run out and set TOPK_DEV_BARRIER_TIMEOUT. The
-   * workspace must then be re-initialised with topk_workspace_init. */
+  /* Test only. 1 = CTA 1 of row group 0 leaves before its first group barrier
+   * (workspace merge), so the other CTAs' waits run out and set
+   * TOPK_DEV_BARRIER_TIMEOUT; 2 = CTA 1 of cluster 0 withholds its arrivals at
+   * the launch's first cluster merge sync, so every member's bounded wait runs
+   * out (TOPK_DEV_BARRIER_TIMEOUT) and all of them leave through the cluster's
+   * exit barrier. Either way the workspace must then be re-initialised with
+   * topk_workspace_init (see TOPK_DEV_WORKSPACE_DIRTY). */
   int inject_skip_arrival;
   /* 0 = unchecked; otherwise the workspace's size, checked against topk_workspace_size. */
   size_t workspace_bytes;
@@ -84,7 +93,9 @@ typedef struct {
   /* CTA shape. 0 = planner decides; 1 = one CTA of 24 consumer warps per SM;
    * 2 = two CTAs of 12 consumer warps per SM (whole rows only); 3 = a CTA of 8
    * consumer warps in about 83 KB of shared memory (whole rows only), the
-   * low-shared-memory mode for devices or partitions where 1 and 2 do not fit. */
+   * low-shared-memory mode for devices or partitions where 1 and 2 do not fit;
+   * 4 = the short-row kernel: one CTA of 32 warps holds a whole row in shared
+   * memory (rows of at most 32768 elements, whole rows only). */
   int shape;
 } topk_options;
 
@@ -101,6 +112,8 @@ typedef struct {
   int pair_ctas_per_sm;
   int small_smem_per_cta; /* the same for the small shape */
   int small_ctas_per_sm;
+  int short_smem_per_cta; /* the same for the short-row kernel (whole rows held in shared memory) */
+  int short_ctas_per_sm;
 } topk_device_props;
 
 /* A launch configuration. */
@@ -113,7 +126,8 @@ typedef struct {
   int cooperative;    /* 1 when the CTAs of a group wait on one another through the workspace */
   int cluster;        /* 1 when the CTAs of a group form a cluster and merge in its shared memory */
   int shape;          /* 1 = one CTA of 24 consumer warps per SM, 2 = two CTAs of 12 per SM,
-                         3 = the small shape (8 consumer warps, low shared memory) */
+                         3 = the small shape (8 consumer warps, low shared memory),
+                         4 = the short-row kernel (a whole row in shared memory) */
 } topk_plan;
 
 /*
@@ -132,7 +146,9 @@ size_t topk_workspace_size(int device, int64_t num_rows, int64_t row_stride, int
  * workspace zeroed again, apart from the sticky status word, which this call
  * also clears (the per-call memset it replaces is the one the vLLM PR #41748
  * page, "Motivation", removes for a 3-5 us saving per decode step).
- * After a TOPK_DEV_BARRIER_TIMEOUT the workspace must be re-initialised.
+ * After a TOPK_DEV_BARRIER_TIMEOUT or TOPK_DEV_STAGE_TIMEOUT the workspace must
+ * be re-initialised: until then, launches that split rows refuse to merge
+ * through it and write rows of -1 (TOPK_DEV_WORKSPACE_DIRTY).
  */
 int topk_workspace_init(void* workspace, size_t bytes, void* stream);
 
@@ -177,9 +193,12 @@ int topk_ragged(const float* logits, int64_t row_stride, const int32_t* lengths,
  *     make that first call before any stream capture.
  *   - All calls on a device share the one array: calls that may overlap on
  *     the GPU (different streams without ordering) race and must not be made.
- *   - The device status word is not readable through this entry point; after a
- *     device-side time-out the shared array is left dirty until the process
- *     restarts (use topk_ragged with a workspace where that matters).
+ *   - The device status word is not readable through this entry point. A
+ *     device-side time-out (a wait of a second, which a working GPU never
+ *     reaches) leaves the array marked: from then on, calls whose plan splits
+ *     rows write rows of -1 instead of merging through stale words, until the
+ *     process restarts (use topk_ragged with a workspace where that matters).
+ *   - The LIBTOPK_* environment knobs apply as they do to topk_ragged.
  */
 int topk_ragged_static(const float* logits, int64_t row_stride, const int32_t* lengths,
                        int64_t num_rows, int next_n, int topk, int32_t* out_idx, void* stream);

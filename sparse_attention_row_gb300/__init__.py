@@ -46,10 +46,12 @@ TOPK_SHAPE_AUTO = 0
 TOPK_SHAPE_WIDE = 1
 TOPK_SHAPE_PAIR = 2
 TOPK_SHAPE_SMALL = 3
+TOPK_SHAPE_SHORT = 4
 
 TOPK_DEV_LENGTH_CLAMPED = 0x1
 TOPK_DEV_BARRIER_TIMEOUT = 0x2
 TOPK_DEV_STAGE_TIMEOUT = 0x4
+TOPK_DEV_WORKSPACE_DIRTY = 0x8
 
 EXPORTED = ("topk_workspace_size", "topk_workspace_init", "topk_ragged", "topk_ragged_ex", "topk_ragged_static",
             "topk_ragged_strided", "topk_gather_sort", "topk_get_status", "topk_status_string",
@@ -82,7 +84,9 @@ class TopkDeviceProps(ctypes.Structure):
                 ("pair_smem_per_cta", ctypes.c_int),
                 ("pair_ctas_per_sm", ctypes.c_int),
                 ("small_smem_per_cta", ctypes.c_int),
-                ("small_ctas_per_sm", ctypes.c_int)]
+                ("small_ctas_per_sm", ctypes.c_int),
+                ("short_smem_per_cta", ctypes.c_int),
+                ("short_ctas_per_sm", ctypes.c_int)]
 
 
 class TopkPlan(ctypes.Structure):

@@ -28,6 +28,9 @@
 //   - G = 1 launches min(num_rows, capacity) persistent CTAs, no waiting;
 //     with at least kPairRowsPerSm rows per SM it uses the paired shape (two
 //     CTAs of 12 consumer warps per SM), otherwise the wide one;
+//   - whole rows of at most kShortMaxLen elements (row_stride) take the
+//     short-row kernel, one CTA of 32 warps per row holding the row in shared
+//     memory, where the device can hold it;
 //   - a device whose shared memory per block cannot hold the wide shape gets
 //     whole rows on the paired shape if it fits, else on the small shape
 //     (about 83 KB), else TOPK_ERR_PLAN;
@@ -58,7 +61,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   const int merge = (options != nullptr) ? options->merge : 0;
   if (merge < 0 || merge > 2) return TOPK_ERR_INVALID_ARG;
   const int shape = (options != nullptr) ? options->shape : 0;
-  if (shape < 0 || shape > 3) return TOPK_ERR_INVALID_ARG;
+  if (shape < 0 || shape > 4) return TOPK_ERR_INVALID_ARG;
   const int force = (options != nullptr) ? options->force_ctas_per_group : 0;
   if (force < 0 || force > ltk::kMaxGroup) return TOPK_ERR_INVALID_ARG;
   if (shape > ltk::kShapeWide && force > 1) return TOPK_ERR_INVALID_ARG;  // those shapes split no row
@@ -66,6 +69,8 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   const bool wide_ok = props->ctas_per_sm >= 1 && props->smem_per_cta <= props->max_smem_optin;
   const bool pair_ok = props->pair_ctas_per_sm >= 1 && props->pair_smem_per_cta <= props->max_smem_optin;
   const bool small_ok = props->small_ctas_per_sm >= 1 && props->small_smem_per_cta <= props->max_smem_optin;
+  const bool short_ok = props->short_ctas_per_sm >= 1 && props->short_smem_per_cta <= props->max_smem_optin &&
+                        row_stride <= ltk::kShortMaxLen;
 
   // the CTA shape when it is not the planner's to choose, or when the wide
   // shape does not fit the device (then the largest whole-row shape that fits)
@@ -74,6 +79,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   if (chosen == ltk::kShapeWide && !wide_ok) return TOPK_ERR_PLAN;
   if (chosen == ltk::kShapePair && !pair_ok) return TOPK_ERR_PLAN;
   if (chosen == ltk::kShapeSmall && !small_ok) return TOPK_ERR_PLAN;
+  if (chosen == ltk::kShapeShort && !short_ok) return TOPK_ERR_PLAN;
   if (chosen == ltk::kShapePair && topk > ltk::kPairMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
   if (chosen == ltk::kShapeSmall && topk > ltk::kSmallMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
 
@@ -119,7 +125,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     if (chosen == 0) {
       const bool pair = G == 1 && topk <= ltk::kPairMaxTopK && pair_ok && props->pair_ctas_per_sm >= 2 &&
                         num_rows >= ltk::kPairRowsPerSm * props->num_sms;
-      chosen = pair ? ltk::kShapePair : ltk::kShapeWide;
+      chosen = (G == 1 && short_ok) ? ltk::kShapeShort : pair ? ltk::kShapePair : ltk::kShapeWide;
     }
   }
   plan->shape = chosen;
@@ -127,9 +133,15 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     plan->threads = ltk::kWideCtaThreads;
     plan->smem_bytes = props->smem_per_cta;
   } else {
-    const int per_sm = chosen == ltk::kShapePair ? props->pair_ctas_per_sm : props->small_ctas_per_sm;
-    plan->threads = chosen == ltk::kShapePair ? ltk::kPairCtaThreads : ltk::kSmallCtaThreads;
-    plan->smem_bytes = chosen == ltk::kShapePair ? props->pair_smem_per_cta : props->small_smem_per_cta;
+    const int per_sm = chosen == ltk::kShapePair    ? props->pair_ctas_per_sm
+                       : chosen == ltk::kShapeSmall ? props->small_ctas_per_sm
+                                                    : props->short_ctas_per_sm;
+    plan->threads = chosen == ltk::kShapePair    ? ltk::kPairCtaThreads
+                    : chosen == ltk::kShapeSmall ? ltk::kSmallCtaThreads
+                                                 : ltk::kShortCtaThreads;
+    plan->smem_bytes = chosen == ltk::kShapePair    ? props->pair_smem_per_cta
+                       : chosen == ltk::kShapeSmall ? props->small_smem_per_cta
+                                                    : props->short_smem_per_cta;
     cap = static_cast<int64_t>(props->num_sms) * per_sm;
     if (options != nullptr && options->max_ctas > 0) cap = std::min<int64_t>(cap, options->max_ctas);
   }

@@ -85,6 +85,12 @@ int query_device_locked(int device, topk_device_props* out) {
           ltk::small::kernel_occupancy(&p.small_ctas_per_sm) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
     }
+    p.short_smem_per_cta = static_cast<int>(ltk::shortrow::kernel_smem_bytes());
+    if (rc == TOPK_OK && p.short_smem_per_cta <= p.max_smem_optin) {
+      if (ltk::shortrow::kernel_configure() != cudaSuccess ||
+          ltk::shortrow::kernel_occupancy(&p.short_ctas_per_sm) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
+    }
     if (prev != device) cudaSetDevice(prev);
     if (rc != TOPK_OK) {
       cudaGetLastError();
@@ -111,6 +117,66 @@ int current_props(topk_device_props* out, int* device) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
+
+namespace ltk {
+
+int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t stream, const topk_options* options) {
+  if (c.num_rows < 0 || c.row_stride < 0 || c.col_stride < 1 || c.max_len < 1 || c.max_len > INT32_MAX ||
+      c.next_n < 1 || (c.num_rows % c.next_n) != 0)
+    return TOPK_ERR_INVALID_ARG;
+  if (c.topk < 1 || c.topk > kWideMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
+  if (c.num_rows == 0) return TOPK_OK;
+  if (c.logits == nullptr || c.lengths == nullptr || c.out == nullptr || scratch == nullptr)
+    return TOPK_ERR_INVALID_ARG;
+  if (!aligned(c.logits, 4) || !aligned(c.lengths, 4) || !aligned(c.out, 4) || !aligned(scratch, 16))
+    return TOPK_ERR_MISALIGNED;
+
+  topk_device_props props{};
+  int rc = current_props(&props, nullptr);
+  if (rc != TOPK_OK) return rc;
+  if (options != nullptr && options->workspace_bytes != 0 &&
+      options->workspace_bytes < workspace_bytes_for(props.num_sms))
+    return TOPK_ERR_WORKSPACE_TOO_SMALL;
+
+  const EnvKnobs& env = env_knobs();
+  topk_options opt{};
+  if (options != nullptr) opt = *options;
+  if (opt.long_row_threshold == 0) opt.long_row_threshold = env.long_row_threshold;
+  if (opt.force_ctas_per_group == 0) opt.force_ctas_per_group = env.force_ctas_per_group;
+  if (opt.barrier_timeout_us == 0) opt.barrier_timeout_us = env.timeout_us;
+  if (opt.merge == 0) opt.merge = env.merge;
+
+  topk_plan plan{};
+  rc = topk_make_plan(&props, c.num_rows, c.max_len, c.next_n, c.topk, &opt, &plan);
+  if (rc != TOPK_OK) return rc;
+  if (plan.grid < 1) return TOPK_OK;
+  // a caller-provided workspace holds num_sms row groups, as many as the planner ever uses
+  if (max_groups >= 0 && plan.ctas_per_group > 1 && plan.num_groups > max_groups) return TOPK_ERR_WORKSPACE_TOO_SMALL;
+
+  Params p{};
+  p.logits = c.logits;
+  p.stride = c.row_stride;
+  p.col_stride = c.col_stride;
+  p.max_len = c.max_len;
+  p.lengths = c.lengths;
+  p.num_rows = c.num_rows;
+  p.out = c.out;
+  p.topk = c.topk;
+  p.G = plan.ctas_per_group;
+  p.num_groups = plan.num_groups;
+  p.status = static_cast<uint32_t*>(scratch);
+  p.groups = reinterpret_cast<GroupWs*>(static_cast<char*>(scratch) + kWsHeaderBytes);
+  p.timeout_ns = opt.barrier_timeout_us ? static_cast<uint64_t>(opt.barrier_timeout_us) * 1000ull : kDefaultTimeoutNs;
+  p.inject = opt.inject_skip_arrival;
+  p.cluster = plan.cluster;
+  if (launch_shape(plan.shape, p, plan.grid, plan.cooperative != 0, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return TOPK_ERR_CUDA;
+  }
+  return TOPK_OK;
+}
+
+}  // namespace ltk
 
 extern "C" {
 
@@ -171,59 +237,8 @@ int topk_get_status(const void* workspace, void* stream, uint32_t* device_status
 int topk_ragged_strided(const float* logits, int64_t row_stride, int64_t col_stride, int64_t max_len,
                         const int32_t* lengths, int64_t num_rows, int next_n, int topk, int32_t* out_idx,
                         void* workspace, void* stream, const topk_options* options) {
-  if (num_rows < 0 || row_stride < 0 || col_stride < 1 || max_len < 1 || max_len > INT32_MAX || next_n < 1 ||
-      (num_rows % next_n) != 0)
-    return TOPK_ERR_INVALID_ARG;
-  if (topk < 1 || topk > ltk::kWideMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
-  if (num_rows == 0) return TOPK_OK;
-  if (logits == nullptr || lengths == nullptr || out_idx == nullptr || workspace == nullptr)
-    return TOPK_ERR_INVALID_ARG;
-  if (!aligned(logits, 4) || !aligned(lengths, 4) || !aligned(out_idx, 4) || !aligned(workspace, 16))
-    return TOPK_ERR_MISALIGNED;
-
-  topk_device_props props{};
-  int rc = current_props(&props, nullptr);
-  if (rc != TOPK_OK) return rc;
-  if (options != nullptr && options->workspace_bytes != 0 &&
-      options->workspace_bytes < ltk::workspace_bytes_for(props.num_sms))
-    return TOPK_ERR_WORKSPACE_TOO_SMALL;
-
-  const EnvKnobs& env = env_knobs();
-  topk_options opt{};
-  if (options != nullptr) opt = *options;
-  if (opt.long_row_threshold == 0) opt.long_row_threshold = env.long_row_threshold;
-  if (opt.force_ctas_per_group == 0) opt.force_ctas_per_group = env.force_ctas_per_group;
-  if (opt.barrier_timeout_us == 0) opt.barrier_timeout_us = env.timeout_us;
-  if (opt.merge == 0) opt.merge = env.merge;
-
-  topk_plan plan{};
-  rc = topk_make_plan(&props, num_rows, max_len, next_n, topk, &opt, &plan);
-  if (rc != TOPK_OK) return rc;
-  if (plan.grid < 1) return TOPK_OK;
-
-  ltk::Params p{};
-  p.logits = logits;
-  p.stride = row_stride;
-  p.col_stride = col_stride;
-  p.max_len = max_len;
-  p.lengths = lengths;
-  p.num_rows = num_rows;
-  p.out = out_idx;
-  p.topk = topk;
-  p.G = plan.ctas_per_group;
-  p.num_groups = plan.num_groups;
-  p.status = static_cast<uint32_t*>(workspace);
-  p.groups = reinterpret_cast<ltk::GroupWs*>(static_cast<char*>(workspace) + ltk::kWsHeaderBytes);
-  p.timeout_ns = opt.barrier_timeout_us ? static_cast<uint64_t>(opt.barrier_timeout_us) * 1000ull
-                                        : ltk::kDefaultTimeoutNs;
-  p.inject = opt.inject_skip_arrival;
-  p.cluster = plan.cluster;
-  if (ltk::launch_shape(plan.shape, p, plan.grid, plan.cooperative != 0, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return TOPK_ERR_CUDA;
-  }
-  return TOPK_OK;
+  const ltk::Call c{logits, row_stride, col_stride, max_len, lengths, num_rows, next_n, topk, out_idx};
+  return ltk::run_selection(c, workspace, -1, static_cast<cudaStream_t>(stream), options);
 }
 
 int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths, int64_t num_rows,

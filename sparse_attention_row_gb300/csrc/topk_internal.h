@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "libtopk.h"
+
 namespace ltk {
 
 // Shared by both CTA shapes of the kernel (see topk_kernel.cu for the shapes).
@@ -28,12 +30,17 @@ constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 // rows per SM one CTA's row finish overlaps the other's streaming.
 // kShapeSmall: 8 consumer warps in about 83 KB of shared memory, whole rows
 // only, for devices or partitions with less shared memory per block.
+// kShapeShort: the short-row kernel (topk_short.cu), one CTA of 32 warps that
+// holds a whole row of at most kShortMaxLen elements in shared memory.
 constexpr int kShapeWide = 1;
 constexpr int kShapePair = 2;
 constexpr int kShapeSmall = 3;
+constexpr int kShapeShort = 4;
 constexpr int kWideCtaThreads = 800;   // 24 consumer warps + the copy warp
 constexpr int kPairCtaThreads = 416;   // 12 consumer warps + the copy warp
 constexpr int kSmallCtaThreads = 288;  // 8 consumer warps + the copy warp
+constexpr int kShortCtaThreads = 1024;
+constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.
@@ -71,7 +78,7 @@ struct Params {
   int cluster;       // 1: the G CTAs of a group are one cluster and merge through its shared memory
 };
 
-// Host side of one compiled shape of the kernel (namespace ltk::wide or ltk::pair).
+// Host side of one compiled kernel shape (ltk::wide, ltk::pair, ltk::small, ltk::shortrow).
 #define LTK_DECLARE_SHAPE(NS)                                                                  \
   namespace NS {                                                                               \
   int kernel_threads();                                                                        \
@@ -84,11 +91,35 @@ struct Params {
 LTK_DECLARE_SHAPE(wide)
 LTK_DECLARE_SHAPE(pair)
 LTK_DECLARE_SHAPE(small)
+LTK_DECLARE_SHAPE(shortrow)
 #undef LTK_DECLARE_SHAPE
+
+// One selection as the entry points receive it (device pointers, caller-owned).
+struct Call {
+  const float* logits;
+  int64_t row_stride;
+  int64_t col_stride;
+  int64_t max_len;
+  const int32_t* lengths;
+  int64_t num_rows;
+  int next_n;
+  int topk;
+  int32_t* out;
+};
+
+
+// Checks the arguments, plans and enqueues one selection on `stream`, with
+// `scratch` laid out as a workspace (status word, then row-group areas) that
+// holds `max_groups` row groups; a plan needing more returns
+// TOPK_ERR_WORKSPACE_TOO_SMALL. `options` may be null; the LIBTOPK_*
+// environment knobs fill the fields it leaves at zero. Used by every entry
+// point that selects (topk_api.cu, topk_static.cu).
+int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t stream, const topk_options* options);
 
 inline cudaError_t launch_shape(int shape, const Params& p, int grid, bool cooperative, cudaStream_t stream) {
   if (shape == kShapePair) return pair::launch_topk(p, grid, cooperative, stream);
   if (shape == kShapeSmall) return small::launch_topk(p, grid, cooperative, stream);
+  if (shape == kShapeShort) return shortrow::launch_topk(p, grid, cooperative, stream);
   return wide::launch_topk(p, grid, cooperative, stream);
 }
 

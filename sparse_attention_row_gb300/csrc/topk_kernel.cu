@@ -325,6 +325,12 @@ __device__ __forceinline__ void cluster_wait_all() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// The CTA's abort flag. It is set by this CTA's own threads and, in a cluster
+// launch, by a member CTA that gave up, at any time: every CTA-wide decision
+// taken from it goes through a reducing barrier (csync_or), so that all
+// consumer warps take the same branch.
+__device__ __forceinline__ bool abort_set(const int* flag) { return *reinterpret_cast<const volatile int*>(flag) != 0; }
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -1018,6 +1024,13 @@ __device__ __noinline__ void producer_loop(const Params& p, Smem& s, int g, int 
     mbar_wait_bounded(&s.full[i % kStages], (i / kStages) & 1u, p.timeout_ns, nullptr);
 }
 
+// A consumer's wait for a staged chunk ended without the chunk: flag a
+// time-out unless the CTA was already giving up (then the cause is elsewhere).
+__device__ __noinline__ void stage_gave_up(Smem& s, const Params& p) {
+  if (!abort_set(&s.abort)) atomicOr(p.status, 0x4u);
+  *reinterpret_cast<volatile int*>(&s.abort) = 1;
+}
+
 // ------------------------------------------------------------- chunk filter
 
 // Bits of the elements of f (window elements i0 .. i0 + 3) at or above thr,
@@ -1459,15 +1472,17 @@ __device__ bool group_sync(Smem& s, uint32_t* ctr, uint32_t target, const Params
   csync();
   if (threadIdx.x == 0) {
     if (skip) {
-      s.abort = 1;
+      *reinterpret_cast<volatile int*>(&s.abort) = 1;
     } else {
       __threadfence();
       atom_add_release_gpu(ctr, 1u);
       const uint64_t t0 = global_timer();
       uint32_t spins = 0;
       while (ld_acquire_gpu(ctr) < target) {
-        if ((++spins & 63u) == 0 && global_timer() - t0 > p.timeout_ns) {
-          s.abort = 1;
+        if ((++spins & 63u) != 0) continue;
+        if (abort_set(&s.abort)) break;  // a member of this cluster gave up
+        if (global_timer() - t0 > p.timeout_ns) {
+          *reinterpret_cast<volatile int*>(&s.abort) = 1;
           atomicOr(p.status, 0x2u);
           break;
         }
@@ -1475,8 +1490,7 @@ __device__ bool group_sync(Smem& s, uint32_t* ctr, uint32_t target, const Params
       __threadfence();
     }
   }
-  csync();
-  return s.abort == 0;
+  return !csync_or(abort_set(&s.abort));
 }
 
 __device__ __forceinline__ void clear_slice(uint32_t* a, int n, int m, int G) {
@@ -1596,27 +1610,33 @@ __device__ __noinline__ bool finish_group(Smem& s, const Params& p, int64_t r, i
 // land its next arrival on a phase another CTA is still waiting for. The copy
 // warp takes no part (a hardware cluster barrier would wait for it). Returns
 // false, with TOPK_DEV_BARRIER_TIMEOUT set, if the wait ran out. Consumer-wide.
-__device__ bool cluster_sync(Smem& s, const Params& p, uint32_t& xph) {
+__device__ bool cluster_sync(Smem& s, const Params& p, uint32_t& xph, int g, int m) {
   csync();  // this CTA's writes, local and remote, come before its arrivals
   const int b = static_cast<int>(xph & 1u);
   const uint32_t parity = (xph >> 1) & 1u;
+  // test only: CTA 1 of cluster 0 withholds its arrivals at the launch's first merge sync
+  const bool skip = p.inject == 2 && g == 0 && m == 1 && xph == 0;
   ++xph;
-  if (threadIdx.x < static_cast<unsigned>(p.G)) mbar_arrive_remote(dsmem_addr(&s.xbar[b], threadIdx.x));
+  if (!skip && threadIdx.x < static_cast<unsigned>(p.G)) mbar_arrive_remote(dsmem_addr(&s.xbar[b], threadIdx.x));
   bool ok = mbar_try_wait_cluster(&s.xbar[b], parity);
   if (!ok) {
     const uint64_t t0 = global_timer();
+    bool gave_up = false;
     while (!ok) {
 #pragma unroll 1
       for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait_cluster(&s.xbar[b], parity);
-      if (!ok && global_timer() - t0 > p.timeout_ns) break;
+      if (ok || abort_set(&s.abort)) break;  // a member gave up: it will not arrive
+      if (global_timer() - t0 > p.timeout_ns) {
+        gave_up = true;
+        break;
+      }
     }
-    if (!ok) {
+    if (gave_up) {
       atomicOr(p.status, 0x2u);
-      s.abort = 1;
+      *reinterpret_cast<volatile int*>(&s.abort) = 1;
     }
   }
-  csync();
-  return s.abort == 0;
+  return !csync_or(abort_set(&s.abort));
 }
 
 // Count of bin b over the members of the cluster: this CTA's own count plus
@@ -1738,11 +1758,11 @@ __device__ void push_to_leader(Smem& s, uint32_t ts, int n0) {
 // bins >= t* (one more sync); if even the union does not fit, every member
 // goes to the workspace merge. Returns 1 on the leader, 0 on the members, 2
 // for the workspace merge (everywhere), -1 on a time-out.
-__device__ __noinline__ int cluster_merge(Smem& s, const Params& p, int m, uint32_t& xph) {
+__device__ __noinline__ int cluster_merge(Smem& s, const Params& p, int g, int m, uint32_t& xph) {
   const int tid = threadIdx.x;
   const int G = p.G;
   if (tid == 0) s.x_n0 = s.buf_n;  // what the others read as this CTA's size until X3
-  if (!cluster_sync(s, p, xph)) return -1;  // X1: every window is closed
+  if (!cluster_sync(s, p, xph, g, m)) return -1;  // X1: every window is closed
   if (tid < 32) {
     uint32_t tm = 0;
     int hi = -1;
@@ -1767,13 +1787,13 @@ __device__ __noinline__ int cluster_merge(Smem& s, const Params& p, int m, uint3
   if (n0 + tot > kBufCap) {
     if (tot > kBufCap) return 2;  // heavy ties at t*: same decision in every member
     if (m == 0) compact_buffer(s, [=](uint32_t k, int32_t) { return (k >> 20) >= static_cast<uint32_t>(ts); });
-    if (!cluster_sync(s, p, xph)) return -1;  // X2: the leader kept only its bins >= t*
+    if (!cluster_sync(s, p, xph, g, m)) return -1;  // X2: the leader kept only its bins >= t*
     if (tid == 0) s.x_ln = (m == 0) ? s.buf_n : static_cast<int>(dsmem_ld(dsmem_addr(&s.buf_n, 0u)));
     csync();
     n0 = s.x_ln;
   }
   if (m != 0) push_to_leader(s, static_cast<uint32_t>(ts), n0);
-  if (!cluster_sync(s, p, xph)) return -1;  // X3: the union is in the leader's buffer
+  if (!cluster_sync(s, p, xph, g, m)) return -1;  // X3: the union is in the leader's buffer
   if (m != 0) return 0;
   if (tid == 0) {
     s.t = ts;
@@ -1821,7 +1841,9 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
       first = true;
     }
   }
+  uint32_t status0 = 0;  // split rows: the status word as this launch found it
   if (tid < kThreads) {
+    if (p.G > 1 && tid == 0) status0 = *reinterpret_cast<const volatile uint32_t*>(p.status);
     reset_row_state(s);
     for (int k = tid; k < kLenCache; k += kThreads) {
       const int64_t r = g + static_cast<int64_t>(k) * p.num_groups;
@@ -1830,13 +1852,24 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
   }
   // the other CTAs of the cluster may reach into this one's shared memory only
   // after every thread has arrived here (their wait comes before their first
-  // merge); the copies fill this CTA's own shared memory and need no wait
+  // merge); the copies fill this CTA's own shared memory and need no wait.
+  // The barrier is .aligned: the copy warp, whose lane 0 alone ran the set-up
+  // above, reconverges first.
+  __syncwarp();
   if (p.cluster) cluster_arrive_all();
   __syncthreads();
   if (tid >= kThreads) {
     if (tid == kThreads && p.col_stride == 1) {  // strided rows are read by the consumers
       if (p.G > 1) first = producer_first_split(p, s, g, m, len0);
       producer_loop(p, s, g, m, first);
+    }
+    if (p.cluster) {
+      // the copy warp also meets the rest of the cluster before leaving: it
+      // waits out the start-up phase, then arrives at the exit phase
+      __syncwarp();
+      cluster_wait_all();
+      cluster_arrive_all();
+      cluster_wait_all();
     }
     return;
   }
@@ -1851,6 +1884,18 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
   bool used_ws = false;   // some row of a split group went through the workspace merge
   bool first_barrier = true;
   bool aborted = false;
+  if (p.G > 1 && csync_or(tid == 0 && (status0 & (0x2u | 0x4u)) != 0)) {
+    // An earlier launch on this workspace timed out and left its group words
+    // as they were; merging through them could give wrong rows. Write rows of
+    // -1 instead, flag the refusal, and let topk_workspace_init restore service.
+    if (tid == 0) {
+      atomicOr(p.status, 0x8u);
+      *reinterpret_cast<volatile int*>(&s.abort) = 1;  // the copy warp stops issuing
+    }
+    if (m == 0)
+      for (int64_t r = g; r < p.num_rows; r += p.num_groups) write_trivial_row(p, r, 0);
+    aborted = true;
+  }
   RowWin w;
   for (int64_t k = 0; !aborted && get_row(p, s, k, g, m, w); ++k) {
     if (w.len <= K) {
@@ -1858,7 +1903,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
       if (p.G == 1 && k == 0 && p.col_stride == 1) {
         // slot 0's group discards the early copy the copy warp issued for this row
         if (grp == 0) {
-          if (!mbar_wait_bounded(&s.full[0], 0u, p.timeout_ns, &s.abort)) atomicOr(p.status, 0x4u);
+          if (!mbar_wait_bounded(&s.full[0], 0u, p.timeout_ns, &s.abort) && lane_id() == 0) stage_gave_up(s, p);
           __syncwarp();
           if (lane_id() == 0) mbar_arrive(&s.empty[0]);
         }
@@ -1889,10 +1934,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
         const bool mine = slot % kGroups == grp;
         bool ok = mbar_wait_bounded(&s.full[slot], (q0 / kStages) & 1u, p.timeout_ns, &s.abort);
         ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok && lane_id() == 0) {
-          s.abort = 1;
-          atomicOr(p.status, 0x4u);
-        }
+        if (!ok && lane_id() == 0) stage_gave_up(s, p);
         const int ws = w.wstart;
         const int we = min(ws + kChunk, w.wend);
         const int nvec = (we - ws) >> 2;
@@ -1914,8 +1956,32 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
           s.buf_mark = 0;
           set_threshold(s, static_cast<uint32_t>(s.find_b) << 20);
         }
+        // Crowded seed bin (heavy ties, e.g. a constant row): the chunk holds
+        // at least K elements at or above it and the projection overflows the
+        // buffer. Then the chunk's own K best (by value, then index) are
+        // kept and the filter rises to their K-th key + 1: every later element
+        // of this window has a larger index than all of them, so one equal to
+        // that key can never be selected (exact for any data).
+        const int at_or_above = s.find_gt + static_cast<int>(s.hist[s.find_b]);
+        const bool crowded = w.nch > 1 && at_or_above >= K &&
+                             static_cast<int64_t>(at_or_above) * span > static_cast<int64_t>(kBufCap) * in_chunk;
         csync();
-        if (w.nch == 1) {
+        if (crowded) {
+          const bool staged = !csync_or(!ok);  // the same answer in every warp
+          if (staged) {
+            filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
+            csync();
+          }
+          if (mine) {
+            __syncwarp();
+            if (lane_id() == 0) mbar_arrive(&s.empty[slot]);
+          }
+          if (staged) {
+            if (tid < 32) advance_threshold(s, K);
+            csync();
+            compact_exact(s, K);
+          }
+        } else if (w.nch == 1) {
           // a one-chunk window: every warp filters it and the slot is released
           // after the row-end barrier
           if (ok) filter_chunk<false, false>(s, s.stage[slot], ws, nvec, w.lo, w.hi);
@@ -1936,10 +2002,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
       for (; j < w.nch; j += kGroups) {
         bool ok = mbar_wait_bounded(&s.full[slot], par, p.timeout_ns, &s.abort);
         ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok && lane_id() == 0) {
-          s.abort = 1;
-          atomicOr(p.status, 0x4u);
-        }
+        if (!ok && lane_id() == 0) stage_gave_up(s, p);
         // warp-uniform: the filter's ballots need every lane
         if (ok && !__any_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int*>(&s.full_row) != 0)) {
           const int ws = w.wstart + j * kChunk;
@@ -1956,11 +2019,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
       }
       q = q0 + static_cast<uint32_t>(w.nch);
     }
-    csync();
-    // uniform: s.abort is next written in a later row's chunk loop, which a
-    // warp reaches only through close_window's first barrier, after every
-    // warp has read it here
-    const bool abort_row = s.abort != 0;
+    const bool abort_row = csync_or(abort_set(&s.abort));  // the same answer in every warp
     if (release_late) {
       if (lane_id() == 0) mbar_arrive(&s.empty[static_cast<int>((q - 1) % kStages)]);
       release_late = false;
@@ -1978,7 +2037,7 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
         cluster_wait_all();
         cluster_ready = true;
       }
-      const int mode = cluster_merge(s, p, m, xph);
+      const int mode = cluster_merge(s, p, g, m, xph);
       if (mode == 1) {
         finish_local(s, p, w.r);
       } else if (mode == 0) {
@@ -1995,15 +2054,20 @@ __global__ void __launch_bounds__(kCtaThreads, kMinBlocks) topk_ragged_kernel(co
     }
   }
 
-  if (aborted) {
-    s.abort = 1;
-    return;
-  }
+  if (aborted) *reinterpret_cast<volatile int*>(&s.abort) = 1;  // the copy warp stops issuing
   if (p.cluster) {
-    // no CTA leaves while another may still reach into its shared memory
+    // No CTA leaves while another may still reach into its shared memory:
+    // every thread of the cluster, the copy warps included, meets at the exit
+    // phase of the hardware cluster barrier. Every wait before it is bounded,
+    // so every thread gets there. A CTA that gave up first tells the others,
+    // whose bounded waits then end at once instead of at their own limits.
     if (!cluster_ready) cluster_wait_all();
-    if (!cluster_sync(s, p, xph)) return;
+    if (aborted && tid < p.G) dsmem_st(dsmem_addr(&s.abort, static_cast<uint32_t>(tid)), 1u);
+    __syncwarp();
+    cluster_arrive_all();
+    cluster_wait_all();
   }
+  if (aborted) return;
   if (p.G > 1 && (!p.cluster || used_ws)) {
     // last CTA of the group to finish clears the per-member words and counters
     GroupWs* gw = p.groups + g;

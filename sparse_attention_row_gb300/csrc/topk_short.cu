@@ -1,0 +1,809 @@
+// Short rows: one CTA holds a whole row in shared memory (rows of at most
+// kShortMaxLen elements, one CTA per row).
+//
+// This is the single-CTA path of the method: a shared-memory histogram seeds a
+// threshold, a filter keeps the elements at or above it as candidates with
+// warp-level compaction, and a radix select on the candidates finishes the row
+// (the "decode / medium" path that rows below the cooperative radix threshold
+// take in the persistent_topk launcher of the vLLM PR #41189 page,
+// "Implementation breakdown"; the single-CTA FilteredTopK there keeps rows in
+// at least 128 KB of shared memory, vLLM PR #54110 page, "Feature and
+// motivation").
+//
+// Latency is what counts for these rows (a decode step runs one call over a
+// few dozen rows), so the kernel is built around the arrival of the data:
+//   - thread 0 issues bulk copies (cp.async.bulk) of the row's window in 8 KB
+//     pieces, each completing on its own mbarrier; for a CTA's first row it
+//     does so at kernel start, before the row's length is known (the window
+//     is sized by the row stride, so every piece a length can need is in
+//     flight from the first cycle);
+//   - the first 4096 window elements are histogrammed (top 12 key bits) as
+//     soon as they land and seed a threshold aimed at about 1.25 K survivors;
+//   - every warp then filters its float4s of each piece as the piece lands
+//     (one fp32 compare per element); survivors go, as (key, index), into the
+//     warp's own region of the candidate buffer, so no atomic reserves space,
+//     and a histogram of their top 12 key bits is kept;
+//   - the K-th key's bin t, then its 8-bit sub-bin, are found by one warp
+//     each; candidates above them are written out directly, the few left in
+//     the sub-bin are ranked by (key desc, index asc).
+// Anything the seed misjudged (fewer than K survivors, a full warp region, a
+// crowded threshold bin) falls back to an exact radix select over the resident
+// row, whose ties are taken in index order by a block-wide scan.
+//
+// Strided logits (a column stride above 1) are loaded into the same buffer by
+// every thread with plain loads; the rest is the same.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "topk_internal.h"
+
+namespace ltk {
+namespace shortrow {
+
+constexpr int kThreads = kShortCtaThreads;  // 32 warps
+constexpr int kWarps = kThreads / 32;
+constexpr int kPiece = 2048;                        // elements per bulk copy (8 KB), one mbarrier each
+constexpr int kRowCap = kShortMaxLen + 4;           // window: the row plus up to 3 elements before it
+constexpr int kPieces = (kRowCap + kPiece - 1) / kPiece;
+constexpr int kSeed = kPiece;                       // window elements histogrammed for the seed (piece 0)
+constexpr int kRegion = 256;                        // candidate slots per warp
+constexpr int kCand = kWarps * kRegion;
+constexpr int kList = 2048;                         // candidates of the threshold bin, listed
+constexpr int kRank = 128;                          // sub-bin entries ranked directly
+static_assert(kShortMaxLen < 65536, "candidate indices are 16-bit");
+static_assert(kPieces <= 32, "piece phases fit one 32-bit mask");
+static_assert(kWarps == 32, "a warp reads every warp's survivor count with one lane each");
+static_assert(kPiece % (4 * 32) == 0 && (kThreads * 4) % kPiece == 0, "a warp's float4s lie in one piece");
+
+struct __align__(128) Smem {
+  float row[(kRowCap + 3) & ~3];  // the row's window (bulk-copy destination)
+  uint32_t ckey[kCand];           // candidate keys, warp w in [w * kRegion, (w + 1) * kRegion)
+  uint16_t cidx[kCand];           // candidate indices
+  uint32_t hseed[kBins];          // seed histogram; scratch of the fallback
+  uint32_t hcand[kBins];          // histogram of the candidates' top 12 key bits
+  uint16_t list[kList];           // candidate positions in the threshold bin
+  alignas(16) uint32_t sub[256];  // 8-bit sub-histogram of the threshold bin
+  uint32_t bsum[kBins / 32];      // 32-bin block sums (find_top)
+  alignas(16) uint32_t rk[kRank];
+  alignas(16) int32_t ri[kRank];
+  unsigned long long bar[kPieces];
+  int wcnt[kWarps];               // survivors per warp (may exceed kRegion: overflow)
+  int tcnt[kWarps];               // fallback: ties per warp before the scan
+  int abort;
+  int len_next;
+  int fb, fgt;                    // find_top result
+  int n_out, n_list, n_rank;
+  uint32_t thr_bits;
+  uint32_t key_max;
+};
+
+// ---------------------------------------------------------------- primitives
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for a piece, at most timeout_ns; false if it gave up (or, with an
+// abort flag given, once the CTA is giving up).
+__device__ __noinline__ bool wait_piece(unsigned long long* bar, uint32_t parity, uint64_t timeout_ns,
+                                        const int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *reinterpret_cast<const volatile int*>(abort)) return false;
+    if (global_timer() - t0 > timeout_ns) return false;
+  }
+}
+
+// Block barrier that ORs a predicate: every thread gets the same answer.
+__device__ __forceinline__ bool sync_or(bool pred) { return __syncthreads_or(pred ? 1 : 0) != 0; }
+
+__device__ __forceinline__ uint32_t fkey(float x) {
+  uint32_t u = __float_as_uint(x);
+  u = (u == 0x80000000u) ? 0u : u;
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
+
+// fp32 value whose ">=" test is equivalent to "key >= k" for every non-NaN input.
+__device__ __forceinline__ float key_floor_value(uint32_t k) {
+  if (k <= 0x007FFFFFu) return -__int_as_float(0x7F800000);
+  if (k > 0xFF800000u) return __int_as_float(0x7FC00000);
+  const uint32_t u = (k & 0x80000000u) ? (k ^ 0x80000000u) : ~k;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ float pick(const float4 f, int j) {
+  return j == 0 ? f.x : j == 1 ? f.y : j == 2 ? f.z : f.w;
+}
+
+// Appends val at out[*counter ...] for every lane with pred: one shared atomic per warp.
+__device__ __forceinline__ void warp_emit(int32_t* out, int* counter, int cap, bool pred, int32_t val) {
+  const uint32_t m = __ballot_sync(0xFFFFFFFFu, pred);
+  if (m == 0) return;
+  int base = 0;
+  if (lane_id() == 0) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  const int o = base + __popc(m & lanemask_lt());
+  if (pred && o < cap) out[o] = val;
+}
+
+// Over h[0, kBins): the largest bin b whose suffix sum (bins >= b) reaches
+// need, into s.fb, and the count above b into s.fgt. Requires 1 <= need <=
+// total. Every warp sums whole 32-bin blocks; warp 0 scans the block sums and
+// then the block holding the crossing. Two barriers.
+__device__ __noinline__ void find_top(Smem& s, const uint32_t* h, int need) {
+  const int lane = static_cast<int>(lane_id());
+  const int warp = threadIdx.x >> 5;
+  for (int q = warp; q < kBins / 32; q += kWarps)  // block q: bins kBins-1-32q down to kBins-32-32q
+    s.bsum[q] = __reduce_add_sync(0xFFFFFFFFu, h[kBins - 1 - (32 * q + lane)]);
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t b4[4], own = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      b4[k] = s.bsum[4 * lane + k];
+      own += b4[k];
+    }
+    uint32_t incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
+    const int L = hit ? __ffs(hit) - 1 : 31;
+    uint32_t run = incl - own;
+    int qsel = 4 * L + 3;
+    if (lane == L) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (run + b4[k] >= static_cast<uint32_t>(need)) {
+          qsel = 4 * lane + k;
+          break;
+        }
+        run += b4[k];
+      }
+    }
+    qsel = __shfl_sync(0xFFFFFFFFu, qsel, L);
+    run = __shfl_sync(0xFFFFFFFFu, run, L);
+    const int bin = kBins - 1 - (32 * qsel + lane);
+    const uint32_t hv = h[bin];
+    uint32_t in2 = hv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, in2, o);
+      if (lane >= o) in2 += v;
+    }
+    const uint32_t hit2 = __ballot_sync(0xFFFFFFFFu, run + in2 >= static_cast<uint32_t>(need));
+    const int L2 = hit2 ? __ffs(hit2) - 1 : 31;
+    if (lane == L2) {
+      s.fb = bin;
+      s.fgt = static_cast<int>(run + in2 - hv);
+    }
+  }
+  __syncthreads();
+}
+
+// One warp, over h[0, 256): the largest bin b whose suffix sum reaches need
+// (1 <= need <= total); b into s.fb, the count above it into s.fgt.
+__device__ __forceinline__ void warp_find_top256(Smem& s, const uint32_t* h, int need) {
+  const int lane = static_cast<int>(lane_id());
+  const uint4 lo4 = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
+  const uint4 hi4 = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
+  const uint32_t v[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};  // bins 255-8l down
+  uint32_t own = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) own += v[k];
+  uint32_t incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
+  const int L = hit ? __ffs(hit) - 1 : 31;
+  if (lane == L) {
+    uint32_t run = incl - own;
+    int b = 255 - 8 * lane - 7;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (run + v[k] >= static_cast<uint32_t>(need)) {
+        b = 255 - 8 * lane - k;
+        break;
+      }
+      run += v[k];
+    }
+    s.fb = b;
+    s.fgt = static_cast<int>(run);
+  }
+}
+
+// ------------------------------------------------------------------ copies
+
+struct Win {
+  const float* rowp;  // element 0 of the row
+  int len;            // valid length (clamped)
+  int mis;            // window elements before element 0 (16-byte alignment of the copies)
+  int nwin;           // window elements, a multiple of 4 (0: nothing to read)
+  int np;             // pieces of the window
+};
+
+__device__ __forceinline__ int clamp_len(const Params& p, int32_t raw, bool flag) {
+  if (raw < 0 || static_cast<int64_t>(raw) > p.max_len) {
+    if (flag) atomicOr(p.status, 0x1u);
+    return raw < 0 ? 0 : static_cast<int>(p.max_len);
+  }
+  return raw;
+}
+
+// The window of row r for a length of n elements (n = max_len: the blind window).
+__device__ __forceinline__ Win make_win(const Params& p, int64_t r, int n) {
+  Win w;
+  w.rowp = p.logits + r * p.stride;
+  w.len = n;
+  w.mis = (p.col_stride == 1) ? static_cast<int>((reinterpret_cast<uintptr_t>(w.rowp) & 15u) >> 2) : 0;
+  w.nwin = (n > p.topk) ? ((n + w.mis + 3) & ~3) : 0;
+  w.np = (w.nwin + kPiece - 1) / kPiece;
+  return w;
+}
+
+// Issues the bulk copies of pieces [0, np) of window w: lane q of the calling
+// warp issues piece q, so the copies leave together. Each 16-byte granule
+// copied holds at least one element of the row, so no copy leaves the row's
+// pages.
+__device__ __forceinline__ void issue_pieces(Smem& s, const Win& w, int np) {
+  const int q = static_cast<int>(lane_id());
+  if (q < np) {
+    fence_proxy_async();
+    const int e0 = q * kPiece;
+    const int e1 = min(e0 + kPiece, w.nwin);
+    bulk_copy(&s.row[e0], w.rowp - w.mis + e0, static_cast<uint32_t>(e1 - e0) * 4u, &s.bar[q]);
+  }
+}
+
+// ---------------------------------------------------------------- fallback
+
+// Exact selection over the resident row, whatever the data: three radix levels
+// over the full key (12, 12 and 8 bits) find the K-th key T and how many of the
+// keys equal to T are taken; then the keys above T are written out, and the
+// ties in index order (each thread owns a contiguous segment of the row; a
+// block-wide scan of the segments' tie counts ranks them). Histograms count runs
+// of equal digits within a segment with one atomic, so tie-heavy rows cost few
+// atomics. Rewrites the whole output row.
+__device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r, const Win& w) {
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const int warp = tid >> 5;
+  const int K = p.topk;
+  const int seg = (((w.len + kThreads - 1) / kThreads) + 3) & ~3;
+  const int e_lo = min(tid * seg, w.len);
+  const int e_hi = min(e_lo + seg, w.len);
+  const float* x = s.row + w.mis;
+  uint32_t prefix = 0;
+  int need = K;
+  // levels: bits 31..20, 19..8 (within prefix), 7..0 (within prefix)
+#pragma unroll 1
+  for (int lv = 0; lv < 3; ++lv) {
+    const int shift = lv == 0 ? 20 : lv == 1 ? 8 : 0;
+    const int pshift = lv == 0 ? 32 : lv == 1 ? 20 : 8;
+    const uint32_t mask = lv == 2 ? 0xFFu : 0xFFFu;
+    for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
+    __syncthreads();
+    uint32_t cur = 0xFFFFFFFFu, run = 0;
+    for (int e = e_lo; e < e_hi; ++e) {
+      const uint32_t k = fkey(x[e]);
+      if (pshift < 32 && (k >> pshift) != prefix) continue;
+      const uint32_t d = (k >> shift) & mask;
+      if (d != cur) {
+        if (run) atomicAdd(&s.hseed[cur], run);
+        cur = d;
+        run = 0;
+      }
+      ++run;
+    }
+    if (run) atomicAdd(&s.hseed[cur], run);
+    __syncthreads();
+    find_top(s, s.hseed, need);  // digits above 255 stay empty at level 2
+    need -= s.fgt;
+    prefix = (prefix << (lv == 2 ? 8 : 12)) | static_cast<uint32_t>(s.fb);
+  }
+  const uint32_t T = prefix;  // the K-th key; `need` of the keys equal to T are taken
+  // ties per thread segment, then an exclusive scan over the threads in order
+  int ties = 0;
+  for (int e = e_lo; e < e_hi; ++e) ties += (fkey(x[e]) == T) ? 1 : 0;
+  int incl = ties;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s.tcnt[warp] = incl;
+  if (tid == 0) s.n_out = 0;
+  __syncthreads();
+  int before = incl - ties;
+  for (int q = 0; q < warp; ++q) before += s.tcnt[q];
+  int32_t* o = p.out + r * static_cast<int64_t>(K);
+  // keys above T, and the first `need` ties in index order: one reservation
+  // per warp and step (every warp takes seg steps)
+  for (int j = 0; j < seg; ++j) {
+    const int e = e_lo + j;
+    bool sel = false;
+    if (e < e_hi) {
+      const uint32_t k = fkey(x[e]);
+      if (k > T) {
+        sel = true;
+      } else if (k == T) {
+        sel = before < need;  // the tie's rank in index order
+        ++before;
+      }
+    }
+    warp_emit(o, &s.n_out, K, sel, e);
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ kernel
+
+// One warp, every lane with the same answer: scanning h down from bin `top`
+// (counts above it are zero), the bin b where the suffix sum (bins >= b)
+// reaches need; `above` = the count in bins > b. Requires 1 <= need <= total.
+__device__ __forceinline__ void warp_scan_down(const uint32_t* h, int top, int need, int& bin, int& above) {
+  const int lane = static_cast<int>(lane_id());
+  uint32_t carry = 0;
+#pragma unroll 1
+  for (int b0 = top; b0 >= 0; b0 -= 32) {
+    const int b = b0 - lane;
+    const uint32_t v = (b >= 0) ? h[b] : 0u;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, carry + incl >= static_cast<uint32_t>(need));
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      const uint32_t il = __shfl_sync(0xFFFFFFFFu, incl, L);
+      const uint32_t vl = __shfl_sync(0xFFFFFFFFu, v, L);
+      bin = b0 - L;
+      above = static_cast<int>(carry + il - vl);
+      return;
+    }
+    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  bin = 0;
+  above = static_cast<int>(carry);  // unreachable when the total reaches need
+}
+
+// One warp, every lane with the same answer: scanning h up from bin lo (bins
+// below it are empty), the smallest bin t whose prefix sum (lo..t) exceeds
+// skip; `upto` = that prefix sum. Requires skip < total.
+__device__ __forceinline__ void warp_scan_up(const uint32_t* h, int lo, int skip, int& t, int& upto) {
+  const int lane = static_cast<int>(lane_id());
+  uint32_t carry = 0;
+#pragma unroll 1
+  for (int b0 = lo; b0 < kBins; b0 += 32) {
+    const int b = b0 + lane;
+    const uint32_t v = (b < kBins) ? h[b] : 0u;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, carry + incl > static_cast<uint32_t>(skip));
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      t = b0 + L;
+      upto = static_cast<int>(carry + __shfl_sync(0xFFFFFFFFu, incl, L));
+      return;
+    }
+    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  t = kBins - 1;
+  upto = static_cast<int>(carry);  // unreachable when skip < total
+}
+
+// One warp, every lane with the same answer: over h[0, 256), the largest bin b
+// whose suffix sum reaches need (1 <= need <= total); `above` = the count in
+// bins > b.
+__device__ __forceinline__ void warp_find256(const uint32_t* h, int need, int& bin, int& above) {
+  const int lane = static_cast<int>(lane_id());
+  const uint4 lo4 = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
+  const uint4 hi4 = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
+  const uint32_t v[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};  // bins 255-8l down
+  uint32_t own = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) own += v[k];
+  uint32_t incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
+  const int L = hit ? __ffs(hit) - 1 : 31;
+  // lane L's eight bins, walked down from its top by every lane alike
+  uint32_t run = __shfl_sync(0xFFFFFFFFu, incl - own, L);
+  int b = 255 - 8 * L - 7;
+  bool found = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t vk = __shfl_sync(0xFFFFFFFFu, v[k], L);
+    if (!found && run + vk >= static_cast<uint32_t>(need)) {
+      b = 255 - 8 * L - k;
+      found = true;
+    }
+    if (!found) run += vk;
+  }
+  bin = b;
+  above = static_cast<int>(run);
+}
+
+// Waits for piece q's phase `parity`: the common case (landed) inline, the
+// bounded wait out of line. Warp-uniform answer.
+__device__ __forceinline__ bool piece_ready(Smem& s, int q, uint32_t parity, uint64_t timeout_ns) {
+  bool ok = mbar_try_wait(&s.bar[q], parity);
+  if (!__all_sync(0xFFFFFFFFu, ok)) ok = wait_piece(&s.bar[q], parity, timeout_ns, &s.abort);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const int warp = tid >> 5;
+  const int K = p.topk;
+  const bool bulk = p.col_stride == 1;
+  int64_t r = blockIdx.x;
+  if (r >= p.num_rows) return;
+
+  // Set-up: thread 0 initialises the piece barriers and, with contiguous rows,
+  // issues the first row's blind window (sized by max_len) before anything
+  // else; the first length is loaded now and waited for only after the data.
+  const int32_t len_raw0 = __ldg(p.lengths + r);
+  int blind = 0;  // pieces of the first row in flight before its length is known
+  if (bulk) blind = make_win(p, r, static_cast<int>(p.max_len)).np;  // the same in every thread
+  if (warp == 0) {
+    // lane q initialises piece q's barrier and issues its copy
+    if (lane < kPieces) {
+      mbar_init(&s.bar[lane], 1u);
+      fence_mbar_init();
+    }
+    if (lane == 0) s.abort = 0;
+    if (bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), blind);
+  }
+  for (int b = tid; b < kBins; b += kThreads) {
+    s.hseed[b] = 0;
+    s.hcand[b] = 0;
+  }
+  if (tid < 256) s.sub[tid] = 0;
+  if (tid == 0) {
+    s.key_max = 0;
+    s.n_out = 0;
+    s.n_list = 0;
+    s.n_rank = 0;
+  }
+  __syncthreads();
+  int len = clamp_len(p, len_raw0, tid == 0);
+
+  uint32_t par = 0;  // bit q: parity of the next phase of piece q's barrier
+  bool aborted = false;
+#pragma unroll 1
+  for (int64_t k = 0; r < p.num_rows; ++k) {
+    const int64_t rn = r + gridDim.x;
+    int32_t len_n_raw = 0;
+    if (tid == 0 && rn < p.num_rows) len_n_raw = __ldg(p.lengths + rn);  // consumed at the row's end
+    const Win w = make_win(p, r, len);
+    int32_t* o = p.out + r * static_cast<int64_t>(K);
+    const uint32_t issued = (k == 0) ? ((1u << blind) - 1u) : ((1u << w.np) - 1u);
+    if (w.nwin == 0) {
+      for (int j = tid; j < K; j += kThreads) o[j] = (j < len) ? j : -1;
+    } else {
+      if (!bulk) {
+        // strided rows: every thread loads its elements into the window
+        const int64_t cs = p.col_stride;
+        for (int e = tid; e < len; e += kThreads) s.row[e] = __ldg(w.rowp + static_cast<int64_t>(e) * cs);
+        __syncthreads();
+      }
+      // seed: the top 12 key bits of the first piece (kSeed window elements),
+      // and their largest key
+      bool ok = !bulk || piece_ready(s, 0, par & 1u, p.timeout_ns);
+      const int seed_hi = min(kSeed, w.nwin);
+      uint32_t kmax = 0;
+      for (int i = tid; i < seed_hi; i += kThreads) {
+        const int e = i - w.mis;
+        if (e >= 0 && e < len) {
+          const uint32_t key = fkey(s.row[i]);
+          kmax = max(kmax, key);
+          atomicAdd(&s.hseed[key >> 20], 1u);
+        }
+      }
+      kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+      if (lane == 0 && kmax) atomicMax(&s.key_max, kmax);
+      const int n_seed = min(len, kSeed - w.mis);
+      int target = K;
+      if (n_seed < len) {
+        const int64_t tt = (5ll * K * n_seed + 4ll * len - 1) / (4ll * len);
+        target = static_cast<int>(tt < 1 ? 1 : tt);
+      }
+      target = min(target, n_seed);
+      if (sync_or(!ok)) {
+        aborted = true;
+      } else {
+        // every warp finds the seed bin itself (no second barrier)
+        int t0, above0;
+        warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
+        const float thr = key_floor_value(static_cast<uint32_t>(t0) << 20);
+        // filter: warp w takes float4s v = 32 w + lane + j * kThreads, all in
+        // piece (4 v) / kPiece; survivors go to the warp's own region
+        const int nvec = w.nwin >> 2;
+        const int base = warp * kRegion;
+        int wc = 0;
+#pragma unroll 1
+        for (int v0 = warp * 32; v0 < nvec; v0 += kThreads) {
+          const int q = (4 * v0) / kPiece;
+          if (bulk && q >= 1 && !piece_ready(s, q, (par >> q) & 1u, p.timeout_ns)) {
+            ok = false;  // the whole warp leaves the filter; the barrier below decides for the CTA
+            break;
+          }
+          const int v = v0 + lane;
+          uint32_t m = 0;
+          float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+          const int e0 = 4 * v - w.mis;
+          if (v < nvec) {
+            f = *reinterpret_cast<const float4*>(&s.row[4 * v]);
+            m = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) | (f.w >= thr ? 8u : 0u);
+            if (e0 < 0 || e0 + 3 >= len) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (e0 + j < 0 || e0 + j >= len) m &= ~(1u << j);
+            }
+          }
+          const int c = __popc(m);
+          const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, c & 1);
+          const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, c & 2);
+          const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, c & 4);
+          const int tot = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
+          if (tot == 0) continue;
+          const uint32_t lt = lanemask_lt();
+          int oo = wc + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
+          wc += tot;
+          while (m) {
+            const int j = __ffs(m) - 1;
+            m &= m - 1;
+            if (oo < kRegion) {
+              const uint32_t key = fkey(pick(f, j));
+              s.ckey[base + oo] = key;
+              s.cidx[base + oo] = static_cast<uint16_t>(e0 + j);
+              atomicAdd(&s.hcand[key >> 20], 1u);
+            }
+            ++oo;
+          }
+        }
+        if (lane == 0) s.wcnt[warp] = wc;
+        if (sync_or(!ok)) {
+          aborted = true;
+        } else {
+          // every piece has landed and been read. Every warp sums the counts
+          // and finds the K-th key's bin t itself, scanning up from t0.
+          const int wcl = s.wcnt[lane];
+          const int n_c = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(wcl));
+          const bool over = __any_sync(0xFFFFFFFFu, wcl > kRegion);
+          bool done = false;
+          if (!over && n_c >= K) {
+            int t, upto;
+            warp_scan_up(s.hcand, t0, n_c - K, t, upto);
+            const int in_t = static_cast<int>(s.hcand[t]);
+            const int need = K - (n_c - upto);  // of bin t's candidates, the best `need` are taken
+            const bool all_t = need == in_t;
+            // candidate pass: winners above t out; bin t counted by its next 8 bits and listed
+            const int cnt = min(wcl, kRegion);  // lane-held; the warp's own count is lane `warp`'s
+            const int mine = __shfl_sync(0xFFFFFFFFu, cnt, warp);
+#pragma unroll 1
+            for (int i0 = 0; i0 < mine; i0 += 32) {
+              const int i = i0 + lane;
+              uint32_t key = 0;
+              int d = -1;
+              if (i < mine) {
+                key = s.ckey[base + i];
+                d = static_cast<int>(key >> 20);
+              }
+              warp_emit(o, &s.n_out, K, d > t || (all_t && d == t), i < mine ? static_cast<int32_t>(s.cidx[base + i]) : 0);
+              const bool inbin = !all_t && d == t;
+              const uint32_t bm = __ballot_sync(0xFFFFFFFFu, inbin);
+              if (bm) {
+                if (inbin) atomicAdd(&s.sub[(key >> 12) & 0xFFu], 1u);
+                int lb = 0;
+                if (lane == 0) lb = atomicAdd(&s.n_list, __popc(bm));
+                lb = __shfl_sync(0xFFFFFFFFu, lb, 0) + __popc(bm & lanemask_lt());
+                if (inbin && lb < kList) s.list[lb] = static_cast<uint16_t>(base + i);
+              }
+            }
+            __syncthreads();
+            if (all_t) {
+              done = true;
+            } else if (s.n_list <= kList) {
+              // the sub-bin of the K-th key (every warp finds it), its entries ranked
+              int b2, above2;
+              warp_find256(s.sub, need, b2, above2);
+              const int need2 = need - above2;
+              const int c2 = static_cast<int>(s.sub[b2]);
+              if (c2 <= kRank) {
+                const int nl = s.n_list;
+                const bool all2 = need2 == c2;
+                for (int e0 = warp * 32; e0 < nl; e0 += kThreads) {
+                  const int e = e0 + lane;
+                  int pos = 0, sd = -1;
+                  uint32_t key = 0;
+                  if (e < nl) {
+                    pos = s.list[e];
+                    key = s.ckey[pos];
+                    sd = static_cast<int>((key >> 12) & 0xFFu);
+                  }
+                  warp_emit(o, &s.n_out, K, sd > b2 || (all2 && sd == b2), e < nl ? s.cidx[pos] : 0);
+                  const bool stage = !all2 && sd == b2;
+                  const uint32_t bm = __ballot_sync(0xFFFFFFFFu, stage);
+                  if (bm) {
+                    int lb = 0;
+                    if (lane == 0) lb = atomicAdd(&s.n_rank, __popc(bm));
+                    lb = __shfl_sync(0xFFFFFFFFu, lb, 0) + __popc(bm & lanemask_lt());
+                    if (stage && lb < kRank) {
+                      s.rk[lb] = key;
+                      s.ri[lb] = s.cidx[pos];
+                    }
+                  }
+                }
+                const int c4 = (c2 + 3) & ~3;
+                if (tid >= c2 && tid < c4) {  // padding never beats a real entry
+                  s.rk[tid] = 0u;
+                  s.ri[tid] = 0x7FFFFFFF;
+                }
+                __syncthreads();
+                if (!all2 && tid < c2) {
+                  const uint32_t kj = s.rk[tid];
+                  const int32_t ij = s.ri[tid];
+                  int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+                  for (int i0 = 0; i0 < c2; i0 += 4) {
+                    const uint4 k4 = *reinterpret_cast<const uint4*>(&s.rk[i0]);
+                    const int4 x4 = *reinterpret_cast<const int4*>(&s.ri[i0]);
+                    r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
+                    r1 += (k4.y > kj || (k4.y == kj && x4.y < ij)) ? 1 : 0;
+                    r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
+                    r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
+                  }
+                  const int rank = r0 + r1 + r2 + r3;
+                  const int at = s.n_out + rank;
+                  if (rank < need2 && at < K) o[at] = ij;
+                }
+                done = true;
+              }
+            }
+          }
+          if (!done) fallback_select(s, p, r, w);
+        }
+      }
+    }
+    // the row's end: clear the histograms and counters, learn the next length,
+    // issue its window
+    if (aborted) break;
+    __syncthreads();
+    for (int b = tid; b < kBins; b += kThreads) {
+      s.hseed[b] = 0;
+      s.hcand[b] = 0;
+    }
+    if (tid < 256) s.sub[tid] = 0;
+    if (warp == 0) {
+      // blind pieces past this row's window may still be landing: wait for
+      // them before the buffer takes the next window (lane q, piece q)
+      if (lane < kPieces && lane >= w.np && ((issued >> lane) & 1u))
+        wait_piece(&s.bar[lane], (par >> lane) & 1u, p.timeout_ns, &s.abort);
+      __syncwarp();
+      const int ln = (rn < p.num_rows) ? clamp_len(p, __shfl_sync(0xFFFFFFFFu, len_n_raw, 0), lane == 0) : 0;
+      if (lane == 0) {
+        s.key_max = 0;
+        s.n_out = 0;
+        s.n_list = 0;
+        s.n_rank = 0;
+        s.len_next = ln;
+      }
+      if (rn < p.num_rows && bulk) {
+        const Win wn = make_win(p, rn, ln);
+        issue_pieces(s, wn, wn.np);
+      }
+    }
+    par ^= issued;
+    __syncthreads();
+    r = rn;
+    if (r < p.num_rows) len = s.len_next;
+  }
+  if (aborted && tid == 0) {
+    // a piece did not land in time: flag it, and wait (bounded) for every
+    // copy of the row still in flight before the CTA leaves
+    atomicOr(p.status, 0x4u);
+    const uint32_t issued = (r == static_cast<int64_t>(blockIdx.x)) ? ((1u << blind) - 1u)
+                                                                   : ((1u << make_win(p, r, len).np) - 1u);
+    for (int q = 0; q < 32; ++q)
+      if ((issued >> q) & 1u) wait_piece(&s.bar[q], (par >> q) & 1u, p.timeout_ns, nullptr);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+int kernel_threads() { return kThreads; }
+
+size_t kernel_smem_bytes() { return sizeof(Smem); }
+
+cudaError_t kernel_configure() {
+  return cudaFuncSetAttribute(topk_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sizeof(Smem)));
+}
+
+cudaError_t kernel_occupancy(int* ctas_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, topk_short_kernel, kThreads, sizeof(Smem));
+}
+
+cudaError_t kernel_max_clusters(int, int* clusters) {
+  *clusters = 0;
+  return cudaSuccess;
+}
+
+cudaError_t launch_topk(const Params& p, int grid, bool, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, topk_short_kernel, p);
+}
+
+}  // namespace shortrow
+}  // namespace ltk

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
 #include <mutex>
 
 #include "libtopk.h"
@@ -44,6 +45,8 @@ StaticDevice g_static_dev[kMaxDevices];
 extern "C" int topk_ragged_static(const float* logits, int64_t row_stride, const int32_t* lengths,
                                   int64_t num_rows, int next_n, int topk, int32_t* out_idx,
                                   void* stream) {
+  // the host-side checks come first, as in topk_ragged: nothing is set up or
+  // enqueued for a call that returns an error
   if (num_rows < 0 || row_stride < 1 || next_n < 1 || (num_rows % next_n) != 0)
     return TOPK_ERR_INVALID_ARG;
   if (topk < 1 || topk > ltk::kWideMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
@@ -59,10 +62,6 @@ extern "C" int topk_ragged_static(const float* logits, int64_t row_stride, const
     cudaGetLastError();
     return TOPK_ERR_CUDA;
   }
-  topk_device_props props{};
-  int rc = topk_query_device(dev, &props);
-  if (rc != TOPK_OK) return rc;
-
   void* scratch = nullptr;
   {
     // First call on this device (the device is current here): look up the
@@ -85,32 +84,10 @@ extern "C" int topk_ragged_static(const float* logits, int64_t row_stride, const
     }
     scratch = d.scratch;
   }
-
-  topk_plan plan{};
-  rc = topk_make_plan(&props, num_rows, row_stride, next_n, topk, nullptr, &plan);
-  if (rc != TOPK_OK) return rc;
-  if (plan.grid < 1) return TOPK_OK;
-  if (plan.ctas_per_group > 1 && plan.num_groups > kStaticGroups) return TOPK_ERR_WORKSPACE_TOO_SMALL;
-
-  ltk::Params p{};
-  p.logits = logits;
-  p.stride = row_stride;
-  p.col_stride = 1;
-  p.max_len = row_stride;
-  p.lengths = lengths;
-  p.num_rows = num_rows;
-  p.out = out_idx;
-  p.topk = topk;
-  p.G = plan.ctas_per_group;
-  p.num_groups = plan.num_groups;
-  p.status = static_cast<uint32_t*>(scratch);
-  p.groups = reinterpret_cast<ltk::GroupWs*>(static_cast<char*>(scratch) + ltk::kWsHeaderBytes);
-  p.timeout_ns = ltk::kDefaultTimeoutNs;
-  p.inject = 0;
-  p.cluster = plan.cluster;
-  if (ltk::launch_shape(plan.shape, p, plan.grid, plan.cooperative != 0, s) != cudaSuccess) {
-    cudaGetLastError();
-    return TOPK_ERR_CUDA;
-  }
-  return TOPK_OK;
+  // the same checks, planning (LIBTOPK_* knobs included) and launch as
+  // topk_ragged, on the fixed array; a plan needing more row groups than the
+  // array holds is refused
+  const int64_t max_len = row_stride < INT32_MAX ? row_stride : INT32_MAX;  // lengths are int32
+  const ltk::Call c{logits, row_stride, 1, max_len, lengths, num_rows, next_n, topk, out_idx};
+  return ltk::run_selection(c, scratch, kStaticGroups, s, nullptr);
 }

@@ -56,3 +56,21 @@ def test_peaks_and_traffic_records():
     # the committed traffic record matches the current kernel sources or is dropped
     t = bench.read_traffic("decode_batch")
     assert t is None or t > 5e6
+
+
+def test_gpus_flag_spawns_the_ranks_itself():
+    """`bench.py --gpus 2` without a launcher starts two ranks (gloo here, no GPU) and rank 0
+    reports the aggregate over both."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--dry-run", "--steps", "3"],
+                         capture_output=True, text=True, timeout=300, env=env, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["dry_run"] and line["scaling"] == "weak"

@@ -85,3 +85,28 @@ def test_random_case_matches_oracle(rn, seed):
     assert_matches_oracle(x, lengths, got, topk, next_n=next_n,
                           label=f"seed {seed}: {x.shape[0]} rows x {x.shape[1]}, K {topk}, next_n {next_n}, {opts}")
     assert rn.workspace_clean()
+
+
+SHORT_CASES = 40
+
+
+def _short_case(seed: int):
+    """Batches for the short-row kernel: rows of at most 32768 elements, one CTA per row (or
+    several rows per CTA), every value mix, TopK up to 4096."""
+    rng = np.random.default_rng(2_000_029 * seed + 5)
+    topk = int(rng.choice([int(rng.integers(1, 65)), 512, 1024, 2048, int(rng.integers(1, 4097))]))
+    stride = int(rng.choice([int(rng.integers(1, 5000)), int(rng.integers(5000, 32769)), 32768]))
+    num_rows = int(rng.integers(1, min(200, MAX_ELEMENTS // stride) + 1))
+    x = np.stack([_row(rng, stride) for _ in range(num_rows)])
+    lengths = rng.integers(0, stride + 1, size=num_rows)
+    lengths[rng.random(num_rows) < 0.3] = stride
+    max_ctas = int(rng.choice([0, 0, 1, 3, 17]))
+    return x, lengths.astype(np.int32), topk, dict(shape=4, max_ctas=max_ctas)
+
+
+@pytest.mark.parametrize("seed", range(SHORT_CASES))
+def test_random_short_rows_match_oracle(rn, seed):
+    x, lengths, topk, opts = _short_case(seed)
+    got = rn.run(x, lengths, topk, options=rn.options(**opts))
+    assert_matches_oracle(x, lengths, got, topk,
+                          label=f"short seed {seed}: {x.shape[0]} rows x {x.shape[1]}, K {topk}, {opts}")

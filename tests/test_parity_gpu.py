@@ -27,25 +27,28 @@ def test_workloads_small_auto(rn, name, rows):
     assert rn.workspace_clean()
 
 
-@pytest.mark.parametrize("shape", [2, 3])
+@pytest.mark.parametrize("shape", [1, 2, 3, 4])
 @pytest.mark.parametrize("name,rows", SMALL)
 def test_workloads_small_other_shapes(rn, name, rows, shape):
-    """The paired shape (two CTAs of 12 consumer warps per SM) and the small, low-shared-memory
-    shape (8 consumer warps), forced on every workload."""
+    """Every CTA shape forced on every workload it can hold: the wide one (24 consumer warps), the
+    paired one (two CTAs of 12 consumer warps per SM), the small, low-shared-memory one (8 consumer
+    warps), and the short-row kernel (a whole row of at most 32768 elements in shared memory)."""
     w = workloads.make(name, rows)
+    if shape == 4 and w.row_stride > 32768:
+        pytest.skip("the short-row kernel holds rows of at most 32768 elements")
     got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=shape))
     assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} shape={shape}")
     assert rn.workspace_clean()
 
 
 @pytest.mark.parametrize("topk", [1, 7, 100, 1000, 2047, 2049, 3000, 4096])
-@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (0, 0, 2), (0, 0, 3), (3, 1, 0), (4, 2, 0)])
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (0, 0, 2), (0, 0, 3), (3, 1, 0), (4, 2, 0), (0, 0, 4)])
 def test_runtime_topk(rn, topk, G, merge, shape):
     """TopK outside the pages' 512 / 1024 / 2048, on every path (paired and small shapes up to 2048)."""
     if shape in (2, 3) and topk > 2048:
         pytest.skip("the paired and small shapes serve TopK up to 2048")
     rng = np.random.default_rng(topk)
-    S = 40000
+    S = 40000 if shape != 4 else 32768
     x = np.round(rng.standard_normal((12, S)) * 32).astype(np.float32) / 32  # heavy ties
     lens = rng.integers(0, S, 12, endpoint=True).astype(np.int32)
     lens[:4] = [0, topk - 1 if topk > 1 else 0, topk, S]
@@ -55,7 +58,7 @@ def test_runtime_topk(rn, topk, G, merge, shape):
 
 
 @pytest.mark.parametrize("layout", ["transposed", "every_third_column", "padded_rows"])
-@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 2), (1, 0, 3), (3, 1, 0), (4, 2, 0)])
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 1), (1, 0, 2), (1, 0, 3), (3, 1, 0), (4, 2, 0)])
 def test_strided_logits(rn, layout, G, merge, shape):
     """Views with a row pitch and a column stride: transposed, column-strided, padded rows."""
     torch = rn.torch
@@ -195,8 +198,11 @@ def _edge_rows(S: int, K: int, rng) -> tuple[np.ndarray, np.ndarray]:
 
 @pytest.mark.parametrize("topk", [512, 1024, 2048])
 @pytest.mark.parametrize("S", [4096, 9001, 40000])
-@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 0), (0, 0, 2), (0, 0, 3), (4, 1, 0), (4, 2, 0), (8, 2, 0)])
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 1), (0, 0, 2), (0, 0, 3), (4, 1, 0), (4, 2, 0), (8, 2, 0),
+                                           (0, 0, 4)])
 def test_edge_cases(rn, topk, S, G, merge, shape):
+    if shape == 4 and S > 32768:
+        pytest.skip("the short-row kernel holds rows of at most 32768 elements")
     # with G = 8 and K = 2048 the all-equal row keeps 8 x K candidates at one
     # key, more than the leader's buffer: the cluster merge hands over to the
     # workspace merge
@@ -257,6 +263,12 @@ def test_many_rows_per_cta_and_per_group(rn):
     # the small shape, 5 CTAs: 60 rows each
     got = rn.run(x, lens, 1024, options=rn.options(max_ctas=5, shape=3))
     assert_matches_oracle(x, lens, got, 1024, label="small persistent")
+    # the short-row kernel, 7 CTAs: 42 or 43 rows each
+    got = rn.run(x, lens, 1024, options=rn.options(max_ctas=7, shape=4))
+    assert_matches_oracle(x, lens, got, 1024, label="short-row persistent")
+    # the wide shape on whole rows, 6 CTAs
+    got = rn.run(x, lens, 1024, options=rn.options(max_ctas=6, shape=1))
+    assert_matches_oracle(x, lens, got, 1024, label="wide persistent")
     # 2 groups of 4 CTAs: every group loops over 150 rows, reusing its workspace
     got = rn.run(x, lens, 1024, options=rn.options(max_ctas=8, force_ctas_per_group=4))
     assert_matches_oracle(x, lens, got, 1024, label="G=4 persistent")

@@ -13,15 +13,17 @@ def _built():
     build.build_library()
 
 
-def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, pair=(0, 0), small=(0, 0)):
+def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, pair=(0, 0), small=(0, 0),
+          short=(0, 0)):
     """A made-up device; clusters maps a cluster size to its co-resident count (none by default);
-    pair and small are (shared memory, CTAs per SM) of those shapes (absent by default)."""
+    pair, small and short are (shared memory, CTAs per SM) of those shapes (absent by default)."""
     p = sar.TopkDeviceProps()
     p.num_sms, p.ctas_per_sm, p.smem_per_cta, p.max_smem_optin = num_sms, occ, smem, optin
     for c, n in (clusters or {}).items():
         p.cluster_groups[c] = n
     p.pair_smem_per_cta, p.pair_ctas_per_sm = pair
     p.small_smem_per_cta, p.small_ctas_per_sm = small
+    p.short_smem_per_cta, p.short_ctas_per_sm = short
     return p
 
 
@@ -29,6 +31,9 @@ GB300_SMALL = (85000, 2)
 
 
 GB300_PAIR = (113536, 2)
+
+
+GB300_SHORT = (220 * 1024, 1)
 
 
 def gb300_clusters():
@@ -196,7 +201,8 @@ def test_paired_shape():
     rc, pl = plan(gb, 16, 131072, shape=2)
     assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1
     assert plan(props(), 8, 4096, shape=2)[0] == sar.TOPK_ERR_PLAN
-    assert plan(gb, 8, 4096, shape=4)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 4096, shape=5)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 4096, shape=4)[0] == sar.TOPK_ERR_PLAN  # no short-row kernel on this made-up device
     assert plan(gb, 8, 4096, shape=3)[0] == sar.TOPK_ERR_PLAN  # no small shape on this made-up device
     # TopK above 2048 runs on the wide shape only
     rc, pl = plan(gb, 4096, 65536, topk=3000)
@@ -249,3 +255,46 @@ def test_threshold_and_capacity_knobs():
     assert rc == 0 and pl.ctas_per_group == 1
     rc, pl = plan(gb, 3, 4096, force_ctas_per_group=4)
     assert rc == 0 and pl.grid == 12 and pl.cooperative
+
+
+def test_static_scratch_capacity_is_reachable_on_larger_devices():
+    """topk_ragged_static's fixed array holds 76 row-group areas: every split plan on a GPU of up
+    to 152 SMs fits (G >= 2 leaves at most num_sms / 2 groups), and a larger device can need more,
+    which that entry point refuses with TOPK_ERR_WORKSPACE_TOO_SMALL."""
+    static_groups = 76
+    for rows in range(1, 152):
+        for stride in (65536, 262144, 1 << 20):
+            rc, pl = plan(props(), rows, stride)
+            assert rc == 0
+            if pl.ctas_per_group > 1:
+                assert pl.num_groups <= static_groups
+    # 200 SMs, no clusters: 90 rows of 1M elements split two ways through the workspace
+    rc, pl = plan(props(num_sms=200), 90, 1 << 20)
+    assert rc == 0 and pl.ctas_per_group == 2 and not pl.cluster and pl.num_groups == 90 > static_groups
+
+
+def test_short_row_kernel():
+    """Whole rows of at most 32768 elements take the short-row kernel where the device holds it."""
+    gb = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT)
+    for rows, stride, k in ((8, 4096, 512), (64, 32768, 2048), (1, 1, 1), (4096, 32768, 2048), (300, 6000, 4096)):
+        rc, pl = plan(gb, rows, stride, topk=k)
+        assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1 and pl.threads == 1024
+        assert pl.grid == min(rows, 152) and not pl.cooperative and not pl.cluster
+    # longer rows keep the streaming shapes
+    rc, pl = plan(gb, 64, 32769)
+    assert rc == 0 and pl.shape != 4
+    rc, pl = plan(gb, 16, 131072)
+    assert rc == 0 and pl.shape == 1 and pl.cluster
+    # forcing: shape 4 needs rows that fit and one CTA per row
+    rc, pl = plan(gb, 10, 32768, shape=4, max_ctas=3)
+    assert rc == 0 and pl.shape == 4 and pl.grid == 3
+    assert plan(gb, 10, 40000, shape=4)[0] == sar.TOPK_ERR_PLAN
+    assert plan(gb, 10, 30000, shape=4, force_ctas_per_group=2)[0] == sar.TOPK_ERR_INVALID_ARG
+    rc, pl = plan(gb, 10, 30000, force_ctas_per_group=2)
+    assert rc == 0 and pl.shape == 1 and pl.ctas_per_group == 2
+    # a device that cannot hold it (GB10-class shared memory) never plans it
+    gb10 = props(num_sms=48, smem=224 * 1024, optin=99 * 1024, pair=(113536, 0), small=(85000, 1),
+                 short=(220 * 1024, 0))
+    rc, pl = plan(gb10, 8, 4096, topk=512)
+    assert rc == 0 and pl.shape == 3
+    assert plan(gb10, 8, 4096, topk=512, shape=4)[0] == sar.TOPK_ERR_PLAN

@@ -79,3 +79,47 @@ def test_timed_out_group_wait_reports_and_recovers(rn):
     got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=2, merge=1))
     assert_matches_oracle(w.logits, w.lengths, got, w.topk, label="after recovery")
     assert rn.workspace_clean()
+
+
+def test_dirty_workspace_is_refused_not_merged(rn):
+    """After a time-out the group words are stale; a later split launch must not merge through them.
+
+    Without topk_workspace_init, the next call that splits rows writes rows of -1 and sets
+    TOPK_DEV_WORKSPACE_DIRTY (wrong indices with a clean status would be the failure); whole-row
+    calls never read the group words and stay exact.
+    """
+    sar = rn.sar
+    w = workloads.make("long_coop", 4)
+    rn.sel.reset()
+    opts = rn.options(force_ctas_per_group=2, merge=1, inject_skip_arrival=1, barrier_timeout_us=20000)
+    rn.run(w.logits, w.lengths, w.topk, options=opts, check_status=False)
+    assert rn.sel.status() & sar.TOPK_DEV_BARRIER_TIMEOUT
+    for G, merge in ((2, 1), (4, 2)):
+        got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=G, merge=merge),
+                     check_status=False)
+        assert rn.sel.status() & sar.TOPK_DEV_WORKSPACE_DIRTY, f"G={G} merge={merge}"
+        assert (got == -1).all(), f"G={G} merge={merge}: a refused launch writes rows of -1"
+    got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=1), check_status=False)
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, label="whole rows on a dirty workspace")
+    rn.sel.reset()
+    got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=2, merge=1))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, label="after re-initialisation")
+    assert rn.workspace_clean()
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_timed_out_cluster_sync_reports_and_every_cta_leaves(rn, G):
+    """A cluster member that withholds its merge arrivals: every member's bounded wait runs out,
+    the launch ends (all CTAs meet at the cluster's exit barrier), and the context stays usable."""
+    sar = rn.sar
+    w = workloads.make("long_coop", 3)
+    rn.sel.reset()
+    opts = rn.options(force_ctas_per_group=G, merge=2, inject_skip_arrival=2, barrier_timeout_us=20000)
+    rn.run(w.logits, w.lengths, w.topk, options=opts, check_status=False)
+    st = rn.sel.status()
+    assert st & sar.TOPK_DEV_BARRIER_TIMEOUT, f"status {st:#x}"
+    assert not st & sar.TOPK_DEV_STAGE_TIMEOUT, f"status {st:#x}: the members' copies all landed"
+    rn.sel.reset()
+    got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=G, merge=2))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, label=f"cluster G={G} after recovery")
+    assert rn.workspace_clean()
