@@ -1,5 +1,5 @@
 // Short rows: one CTA holds a whole row in shared memory (rows of at most
-// kShortMaxLen elements, one CTA per row).
+// kShortMaxLen elements, whole rows only).
 //
 // This is the single-CTA path of the method: a shared-memory histogram seeds a
 // threshold, a filter keeps the elements at or above it as candidates with
@@ -10,25 +10,29 @@
 // at least 128 KB of shared memory, vLLM PR #54110 page, "Feature and
 // motivation").
 //
-// Latency is what counts for these rows (a decode step runs one call over a
-// few dozen rows), so the kernel is built around the arrival of the data:
-//   - thread 0 issues bulk copies (cp.async.bulk) of the row's window in 8 KB
-//     pieces, each completing on its own mbarrier; for a CTA's first row it
-//     does so at kernel start, before the row's length is known (the window
-//     is sized by the row stride, so every piece a length can need is in
-//     flight from the first cycle);
-//   - the first 4096 window elements are histogrammed (top 12 key bits) as
-//     soon as they land and seed a threshold aimed at about 1.25 K survivors;
-//   - every warp then filters its float4s of each piece as the piece lands
-//     (one fp32 compare per element); survivors go, as (key, index), into the
-//     warp's own region of the candidate buffer, so no atomic reserves space,
-//     and a histogram of their top 12 key bits is kept;
-//   - the K-th key's bin t, then its 8-bit sub-bin, are found by one warp
-//     each; candidates above them are written out directly, the few left in
-//     the sub-bin are ranked by (key desc, index asc).
-// Anything the seed misjudged (fewer than K survivors, a full warp region, a
-// crowded threshold bin) falls back to an exact radix select over the resident
-// row, whose ties are taken in index order by a block-wide scan.
+// A decode step runs one call over a few dozen rows, so what counts is how
+// soon after its data lands a row is done, and within the CTA that is set by
+// how many instructions the 32 warps issue, not by memory:
+//   - warp 0's lanes issue the row's window as 8 KB bulk copies (cp.async.bulk),
+//     one mbarrier each; for a CTA's first row at kernel start, sized by the
+//     row stride before the length is known;
+//   - piece 0 (2048 elements) is histogrammed on the top 12 key bits and one
+//     warp picks the seed bin t0 for about 1.25 K survivors over the row;
+//   - every warp filters tasks of 512 elements (4 float4 per lane) as their
+//     pieces land, one fp32 compare per element. A lane notes where its
+//     survivors are straight in the warp's own region of the candidate
+//     buffer; the warp then converts them 32 at a time and counts them by
+//     their bin relative to t0 (8 bins, one ballot each): no atomics;
+//   - one warp finds the K-th key's bin t from those counts and gives every
+//     warp its output offsets; the warps write the winners above t and list
+//     bin t, counting the list by its next 4 key bits; one warp finds the
+//     K-th key's sub-bin and the offsets again; the warps write the winners
+//     above it and stage the sub-bin's entries, which are ranked by (key desc,
+//     index asc). Six block barriers per row, no contended atomics.
+// Anything outside that shape (fewer than K survivors, a full region, a K-th
+// bin more than 8 bins above t0, a crowded list or sub-bin) falls back to an
+// exact radix select over the resident row, whose ties are taken in index
+// order by a block-wide scan.
 //
 // Strided logits (a column stride above 1) are loaded into the same buffer by
 // every thread with plain loads; the rest is the same.
@@ -43,38 +47,40 @@ namespace shortrow {
 constexpr int kThreads = kShortCtaThreads;  // 32 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kPiece = 2048;                        // elements per bulk copy (8 KB), one mbarrier each
+constexpr int kTask = 512;                          // window elements a warp filters at a time (4 float4 per lane)
 constexpr int kRowCap = kShortMaxLen + 4;           // window: the row plus up to 3 elements before it
 constexpr int kPieces = (kRowCap + kPiece - 1) / kPiece;
 constexpr int kSeed = kPiece;                       // window elements histogrammed for the seed (piece 0)
 constexpr int kRegion = 256;                        // candidate slots per warp
 constexpr int kCand = kWarps * kRegion;
-constexpr int kList = 2048;                         // candidates of the threshold bin, listed
-constexpr int kRank = 128;                          // sub-bin entries ranked directly
+constexpr int kFine = 17;                           // fine bins: the top 15 key bits (key >> 17)
+constexpr int kTrack = 64;                          // fine bins counted during the filter, from the seed bin's edge
+constexpr int kRank = 128;                          // entries of the K-th key's fine bin ranked directly
 static_assert(kShortMaxLen < 65536, "candidate indices are 16-bit");
 static_assert(kPieces <= 32, "piece phases fit one 32-bit mask");
-static_assert(kWarps == 32, "a warp reads every warp's survivor count with one lane each");
-static_assert(kPiece % (4 * 32) == 0 && (kThreads * 4) % kPiece == 0, "a warp's float4s lie in one piece");
+static_assert(kWarps == 32, "one lane of warp 0 per warp when offsets are scanned");
+static_assert(kPiece % kTask == 0 && kTask == 4 * 4 * 32, "a task is 4 float4 per lane, inside one piece");
 
 struct __align__(128) Smem {
   float row[(kRowCap + 3) & ~3];  // the row's window (bulk-copy destination)
   uint32_t ckey[kCand];           // candidate keys, warp w in [w * kRegion, (w + 1) * kRegion)
-  uint16_t cidx[kCand];           // candidate indices
+  uint16_t cidx[kCand];           // candidate indices (first the survivors' task positions)
   uint32_t hseed[kBins];          // seed histogram; scratch of the fallback
-  uint32_t hcand[kBins];          // histogram of the candidates' top 12 key bits
-  uint16_t list[kList];           // candidate positions in the threshold bin
-  alignas(16) uint32_t sub[256];  // 8-bit sub-histogram of the threshold bin
-  uint32_t bsum[kBins / 32];      // 32-bin block sums (find_top)
+  uint32_t bsum[kBins / 32];      // 32-bin block sums (find_top, in the fallback)
   alignas(16) uint32_t rk[kRank];
   alignas(16) int32_t ri[kRank];
-  unsigned long long bar[kPieces];
+  alignas(16) int wbin[kWarps][kTrack + 4];  // per warp: candidates in fine bin f0 + j (f0: the seed bin's
+                                             // edge); rows padded by 16 bytes so a lane per row reads no bank twice
+  int woff[kWarps][2];            // per warp: output offset, ranking-slot offset
   int wcnt[kWarps];               // survivors per warp (may exceed kRegion: overflow)
   int tcnt[kWarps];               // fallback: ties per warp before the scan
+  unsigned long long bar[kPieces];
   int abort;
   int len_next;
-  int fb, fgt;                    // find_top result
-  int n_out, n_list, n_rank;
-  uint32_t thr_bits;
+  int fb, fgt;                    // find_top result (fallback)
+  int n_out;
   uint32_t key_max;
+  int t0, t, need, in_t, sel_ok;  // seed bin, the K-th key's fine bin, its entries taken and held, fast path ok
 };
 
 // ---------------------------------------------------------------- primitives
@@ -161,7 +167,8 @@ __device__ __forceinline__ float pick(const float4 f, int j) {
   return j == 0 ? f.x : j == 1 ? f.y : j == 2 ? f.z : f.w;
 }
 
-// Appends val at out[*counter ...] for every lane with pred: one shared atomic per warp.
+// Appends val at out[*counter ...] for every lane with pred: one shared atomic
+// per warp (the fallback's emission; the fast path reserves nothing).
 __device__ __forceinline__ void warp_emit(int32_t* out, int* counter, int cap, bool pred, int32_t val) {
   const uint32_t m = __ballot_sync(0xFFFFFFFFu, pred);
   if (m == 0) return;
@@ -229,40 +236,6 @@ __device__ __noinline__ void find_top(Smem& s, const uint32_t* h, int need) {
   __syncthreads();
 }
 
-// One warp, over h[0, 256): the largest bin b whose suffix sum reaches need
-// (1 <= need <= total); b into s.fb, the count above it into s.fgt.
-__device__ __forceinline__ void warp_find_top256(Smem& s, const uint32_t* h, int need) {
-  const int lane = static_cast<int>(lane_id());
-  const uint4 lo4 = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
-  const uint4 hi4 = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
-  const uint32_t v[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};  // bins 255-8l down
-  uint32_t own = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) own += v[k];
-  uint32_t incl = own;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += x;
-  }
-  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
-  const int L = hit ? __ffs(hit) - 1 : 31;
-  if (lane == L) {
-    uint32_t run = incl - own;
-    int b = 255 - 8 * lane - 7;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (run + v[k] >= static_cast<uint32_t>(need)) {
-        b = 255 - 8 * lane - k;
-        break;
-      }
-      run += v[k];
-    }
-    s.fb = b;
-    s.fgt = static_cast<int>(run);
-  }
-}
-
 // ------------------------------------------------------------------ copies
 
 struct Win {
@@ -296,10 +269,10 @@ __device__ __forceinline__ Win make_win(const Params& p, int64_t r, int n) {
 // warp issues piece q, so the copies leave together. Each 16-byte granule
 // copied holds at least one element of the row, so no copy leaves the row's
 // pages.
-__device__ __forceinline__ void issue_pieces(Smem& s, const Win& w, int np) {
+__device__ __forceinline__ void issue_pieces(Smem& s, const Win& w, int np, bool after_use) {
   const int q = static_cast<int>(lane_id());
   if (q < np) {
-    fence_proxy_async();
+    if (after_use) fence_proxy_async();  // the buffer was read through the generic proxy
     const int e0 = q * kPiece;
     const int e1 = min(e0 + kPiece, w.nwin);
     bulk_copy(&s.row[e0], w.rowp - w.mis + e0, static_cast<uint32_t>(e1 - e0) * 4u, &s.bar[q]);
@@ -389,6 +362,33 @@ __device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r
 
 // ------------------------------------------------------------------ kernel
 
+// Waits for an mbarrier phase, the thread suspended (not spinning) until it
+// completes or the hint runs out.
+__device__ __forceinline__ bool mbar_wait_sleep(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits (bounded) for piece q's phase `parity`. Warp-uniform answer.
+__device__ __forceinline__ bool piece_ready(Smem& s, int q, uint32_t parity, uint64_t timeout_ns) {
+  bool ok = mbar_try_wait(&s.bar[q], parity);
+  if (!__all_sync(0xFFFFFFFFu, ok)) {
+    const uint64_t t0 = global_timer();
+    while (!ok) {
+      ok = mbar_wait_sleep(&s.bar[q], parity);
+      if (!ok && global_timer() - t0 > timeout_ns) break;
+    }
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // One warp, every lane with the same answer: scanning h down from bin `top`
 // (counts above it are zero), the bin b where the suffix sum (bins >= b)
 // reaches need; `above` = the count in bins > b. Requires 1 <= need <= total.
@@ -420,77 +420,16 @@ __device__ __forceinline__ void warp_scan_down(const uint32_t* h, int top, int n
   above = static_cast<int>(carry);  // unreachable when the total reaches need
 }
 
-// One warp, every lane with the same answer: scanning h up from bin lo (bins
-// below it are empty), the smallest bin t whose prefix sum (lo..t) exceeds
-// skip; `upto` = that prefix sum. Requires skip < total.
-__device__ __forceinline__ void warp_scan_up(const uint32_t* h, int lo, int skip, int& t, int& upto) {
+// Exclusive prefix over the lanes of a warp.
+__device__ __forceinline__ int warp_excl(int v) {
   const int lane = static_cast<int>(lane_id());
-  uint32_t carry = 0;
-#pragma unroll 1
-  for (int b0 = lo; b0 < kBins; b0 += 32) {
-    const int b = b0 + lane;
-    const uint32_t v = (b < kBins) ? h[b] : 0u;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += x;
-    }
-    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, carry + incl > static_cast<uint32_t>(skip));
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      t = b0 + L;
-      upto = static_cast<int>(carry + __shfl_sync(0xFFFFFFFFu, incl, L));
-      return;
-    }
-    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-  }
-  t = kBins - 1;
-  upto = static_cast<int>(carry);  // unreachable when skip < total
-}
-
-// One warp, every lane with the same answer: over h[0, 256), the largest bin b
-// whose suffix sum reaches need (1 <= need <= total); `above` = the count in
-// bins > b.
-__device__ __forceinline__ void warp_find256(const uint32_t* h, int need, int& bin, int& above) {
-  const int lane = static_cast<int>(lane_id());
-  const uint4 lo4 = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
-  const uint4 hi4 = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
-  const uint32_t v[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};  // bins 255-8l down
-  uint32_t own = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) own += v[k];
-  uint32_t incl = own;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += x;
   }
-  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
-  const int L = hit ? __ffs(hit) - 1 : 31;
-  // lane L's eight bins, walked down from its top by every lane alike
-  uint32_t run = __shfl_sync(0xFFFFFFFFu, incl - own, L);
-  int b = 255 - 8 * L - 7;
-  bool found = false;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t vk = __shfl_sync(0xFFFFFFFFu, v[k], L);
-    if (!found && run + vk >= static_cast<uint32_t>(need)) {
-      b = 255 - 8 * L - k;
-      found = true;
-    }
-    if (!found) run += vk;
-  }
-  bin = b;
-  above = static_cast<int>(run);
-}
-
-// Waits for piece q's phase `parity`: the common case (landed) inline, the
-// bounded wait out of line. Warp-uniform answer.
-__device__ __forceinline__ bool piece_ready(Smem& s, int q, uint32_t parity, uint64_t timeout_ns) {
-  bool ok = mbar_try_wait(&s.bar[q], parity);
-  if (!__all_sync(0xFFFFFFFFu, ok)) ok = wait_piece(&s.bar[q], parity, timeout_ns, &s.abort);
-  return __all_sync(0xFFFFFFFFu, ok);
+  return incl - v;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p) {
@@ -499,37 +438,31 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   const int tid = threadIdx.x;
   const int lane = static_cast<int>(lane_id());
   const int warp = tid >> 5;
+  const uint32_t lt = lanemask_lt();
   const int K = p.topk;
   const bool bulk = p.col_stride == 1;
   int64_t r = blockIdx.x;
   if (r >= p.num_rows) return;
 
-  // Set-up: thread 0 initialises the piece barriers and, with contiguous rows,
-  // issues the first row's blind window (sized by max_len) before anything
-  // else; the first length is loaded now and waited for only after the data.
+  // Set-up: warp 0's lanes initialise the piece barriers and, with contiguous
+  // rows, issue the first row's blind window (sized by max_len) before
+  // anything else; the first length is loaded now, used once the data is in.
   const int32_t len_raw0 = __ldg(p.lengths + r);
   int blind = 0;  // pieces of the first row in flight before its length is known
   if (bulk) blind = make_win(p, r, static_cast<int>(p.max_len)).np;  // the same in every thread
   if (warp == 0) {
-    // lane q initialises piece q's barrier and issues its copy
     if (lane < kPieces) {
       mbar_init(&s.bar[lane], 1u);
       fence_mbar_init();
     }
-    if (lane == 0) s.abort = 0;
-    if (bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), blind);
+    if (lane == 0) {
+      s.abort = 0;
+      s.key_max = 0;
+    }
+    if (bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), blind, false);
   }
-  for (int b = tid; b < kBins; b += kThreads) {
-    s.hseed[b] = 0;
-    s.hcand[b] = 0;
-  }
-  if (tid < 256) s.sub[tid] = 0;
-  if (tid == 0) {
-    s.key_max = 0;
-    s.n_out = 0;
-    s.n_list = 0;
-    s.n_rank = 0;
-  }
+  for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
+  for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
   __syncthreads();
   int len = clamp_len(p, len_raw0, tid == 0);
 
@@ -552,8 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
         for (int e = tid; e < len; e += kThreads) s.row[e] = __ldg(w.rowp + static_cast<int64_t>(e) * cs);
         __syncthreads();
       }
-      // seed: the top 12 key bits of the first piece (kSeed window elements),
-      // and their largest key
+      // ---- seed: the top 12 key bits of piece 0 and its largest key
       bool ok = !bulk || piece_ready(s, 0, par & 1u, p.timeout_ns);
       const int seed_hi = min(kSeed, w.nwin);
       uint32_t kmax = 0;
@@ -567,178 +499,223 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
       }
       kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
       if (lane == 0 && kmax) atomicMax(&s.key_max, kmax);
-      const int n_seed = min(len, kSeed - w.mis);
-      int target = K;
-      if (n_seed < len) {
-        const int64_t tt = (5ll * K * n_seed + 4ll * len - 1) / (4ll * len);
-        target = static_cast<int>(tt < 1 ? 1 : tt);
-      }
-      target = min(target, n_seed);
       if (sync_or(!ok)) {
         aborted = true;
       } else {
-        // every warp finds the seed bin itself (no second barrier)
-        int t0, above0;
-        warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
+        if (warp == 0) {
+          const int n_seed = min(len, kSeed - w.mis);
+          int target = K;
+          if (n_seed < len) {
+            const int64_t tt = (5ll * K * n_seed + 4ll * len - 1) / (4ll * len);
+            target = static_cast<int>(tt < 1 ? 1 : tt);
+          }
+          target = min(target, n_seed);
+          int t0, above0;
+          warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
+          if (lane == 0) s.t0 = t0;
+        }
+        __syncthreads();
+        // ---- filter: warp tasks of 512 window elements; lane l of a task takes
+        // float4s l, l + 32, l + 64, l + 96 of it
+        const int t0 = s.t0;
         const float thr = key_floor_value(static_cast<uint32_t>(t0) << 20);
-        // filter: warp w takes float4s v = 32 w + lane + j * kThreads, all in
-        // piece (4 v) / kPiece; survivors go to the warp's own region
+        const int f0 = t0 << (20 - kFine);  // the seed bin's lower edge as a fine bin
         const int nvec = w.nwin >> 2;
+        const int ntask = (w.nwin + kTask - 1) / kTask;
         const int base = warp * kRegion;
         int wc = 0;
+        int* my_bins = s.wbin[warp];  // this warp's own counters: no other warp touches them
 #pragma unroll 1
-        for (int v0 = warp * 32; v0 < nvec; v0 += kThreads) {
-          const int q = (4 * v0) / kPiece;
+        for (int task = warp; task < ntask; task += kWarps) {
+          const int q = (task * kTask) / kPiece;
           if (bulk && q >= 1 && !piece_ready(s, q, (par >> q) & 1u, p.timeout_ns)) {
             ok = false;  // the whole warp leaves the filter; the barrier below decides for the CTA
             break;
           }
-          const int v = v0 + lane;
+          const int v0 = task * (kTask / 4);
           uint32_t m = 0;
-          float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-          const int e0 = 4 * v - w.mis;
-          if (v < nvec) {
-            f = *reinterpret_cast<const float4*>(&s.row[4 * v]);
-            m = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) | (f.w >= thr ? 8u : 0u);
-            if (e0 < 0 || e0 + 3 >= len) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (e0 + j < 0 || e0 + j >= len) m &= ~(1u << j);
+          for (int i = 0; i < 4; ++i) {
+            const int v = v0 + lane + 32 * i;
+            if (v < nvec) {
+              const float4 f = *reinterpret_cast<const float4*>(&s.row[4 * v]);
+              uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                           (f.w >= thr ? 8u : 0u);
+              const int e0 = 4 * v - w.mis;
+              if (e0 < 0 || e0 + 3 >= len) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  if (e0 + c < 0 || e0 + c >= len) b &= ~(1u << c);
+              }
+              m |= b << (4 * i);
             }
           }
           const int c = __popc(m);
-          const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, c & 1);
-          const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, c & 2);
-          const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, c & 4);
-          const int tot = __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2);
-          if (tot == 0) continue;
-          const uint32_t lt = lanemask_lt();
-          int oo = wc + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt);
-          wc += tot;
-          while (m) {
-            const int j = __ffs(m) - 1;
-            m &= m - 1;
-            if (oo < kRegion) {
-              const uint32_t key = fkey(pick(f, j));
-              s.ckey[base + oo] = key;
-              s.cidx[base + oo] = static_cast<uint16_t>(e0 + j);
-              atomicAdd(&s.hcand[key >> 20], 1u);
-            }
-            ++oo;
+          uint32_t qb[5];
+#pragma unroll
+          for (int bit = 0; bit < 5; ++bit) qb[bit] = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+          int tot = 0, pre = 0;
+#pragma unroll
+          for (int bit = 0; bit < 5; ++bit) {
+            tot += __popc(qb[bit]) << bit;
+            pre += __popc(qb[bit] & lt) << bit;
           }
+          if (tot == 0) continue;
+          if (wc + tot <= kRegion) {
+            // each lane notes where its survivors are (task positions) in the
+            // region, then the warp converts them 32 at a time
+            int at = base + wc + pre;
+            while (m) {
+              const int j = __ffs(m) - 1;
+              m &= m - 1;
+              s.cidx[at++] = static_cast<uint16_t>(4 * (lane + 32 * (j >> 2)) + (j & 3));
+            }
+            __syncwarp();
+#pragma unroll 1
+            for (int e0 = 0; e0 < tot; e0 += 32) {
+              const int e = e0 + lane;
+              const bool valid = e < tot;
+              if (valid) {
+                const int pos = task * kTask + s.cidx[base + wc + e];
+                const uint32_t key = fkey(s.row[pos]);
+                s.ckey[base + wc + e] = key;
+                s.cidx[base + wc + e] = static_cast<uint16_t>(pos - w.mis);
+                const int d = static_cast<int>(key >> kFine) - f0;
+                if (d < kTrack) atomicAdd(&my_bins[d], 1);
+              }
+            }
+            __syncwarp();
+          }
+          wc += tot;
         }
         if (lane == 0) s.wcnt[warp] = wc;
         if (sync_or(!ok)) {
           aborted = true;
         } else {
-          // every piece has landed and been read. Every warp sums the counts
-          // and finds the K-th key's bin t itself, scanning up from t0.
-          const int wcl = s.wcnt[lane];
-          const int n_c = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(wcl));
-          const bool over = __any_sync(0xFFFFFFFFu, wcl > kRegion);
-          bool done = false;
-          if (!over && n_c >= K) {
-            int t, upto;
-            warp_scan_up(s.hcand, t0, n_c - K, t, upto);
-            const int in_t = static_cast<int>(s.hcand[t]);
-            const int need = K - (n_c - upto);  // of bin t's candidates, the best `need` are taken
+          // ---- the K-th key's fine bin t, and every warp's offsets (warp 0; lane l
+          // speaks for warp l, and sums fine bins 2l and 2l + 1 over the warps)
+          if (warp == 0) {
+            const int n_l = s.wcnt[lane];
+            int c0 = 0, c1 = 0;
+#pragma unroll 8
+            for (int q = 0; q < kWarps; ++q) {
+              const int2 v2 = *reinterpret_cast<const int2*>(&s.wbin[q][2 * lane]);
+              c0 += v2.x;
+              c1 += v2.y;
+            }
+            const bool over = __any_sync(0xFFFFFFFFu, n_l > kRegion);
+            const int n_c = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(n_l)));
+            const int skip = n_c - K;  // the K-th key's bin: the first whose prefix (from f0) passes skip
+            const int pair = c0 + c1;
+            int incl = pair;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+              if (lane >= o) incl += x;
+            }
+            const int p0 = incl - pair + c0;  // prefix through bin 2 lane
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > skip);
+            const int L = hit ? __ffs(hit) - 1 : 0;
+            const bool first = __shfl_sync(0xFFFFFFFFu, p0, L) > skip;
+            const int jt = 2 * L + (first ? 0 : 1);
+            const int cum = first ? __shfl_sync(0xFFFFFFFFu, p0, L) : __shfl_sync(0xFFFFFFFFu, incl, L);
+            const int in_t = first ? __shfl_sync(0xFFFFFFFFu, c0, L) : __shfl_sync(0xFFFFFFFFu, c1, L);
+            const int need = K - (n_c - cum);
             const bool all_t = need == in_t;
-            // candidate pass: winners above t out; bin t counted by its next 8 bits and listed
-            const int cnt = min(wcl, kRegion);  // lane-held; the warp's own count is lane `warp`'s
-            const int mine = __shfl_sync(0xFFFFFFFFu, cnt, warp);
-#pragma unroll 1
-            for (int i0 = 0; i0 < mine; i0 += 32) {
-              const int i = i0 + lane;
-              uint32_t key = 0;
-              int d = -1;
-              if (i < mine) {
-                key = s.ckey[base + i];
-                d = static_cast<int>(key >> 20);
-              }
-              warp_emit(o, &s.n_out, K, d > t || (all_t && d == t), i < mine ? static_cast<int32_t>(s.cidx[base + i]) : 0);
-              const bool inbin = !all_t && d == t;
-              const uint32_t bm = __ballot_sync(0xFFFFFFFFu, inbin);
-              if (bm) {
-                if (inbin) atomicAdd(&s.sub[(key >> 12) & 0xFFu], 1u);
-                int lb = 0;
-                if (lane == 0) lb = atomicAdd(&s.n_list, __popc(bm));
-                lb = __shfl_sync(0xFFFFFFFFu, lb, 0) + __popc(bm & lanemask_lt());
-                if (inbin && lb < kList) s.list[lb] = static_cast<uint16_t>(base + i);
-              }
+            const bool sel_ok = !over && n_c >= K && hit != 0 && (all_t || in_t <= kRank);
+            // this warp's (lane l's) candidates above bin t, and in it
+            int below_l = 0;
+#pragma unroll 4
+            for (int j4 = 0; j4 < kTrack; j4 += 4) {
+              const int4 v4 = *reinterpret_cast<const int4*>(&s.wbin[lane][j4]);
+              below_l += (j4 <= jt ? v4.x : 0) + (j4 + 1 <= jt ? v4.y : 0) + (j4 + 2 <= jt ? v4.z : 0) +
+                         (j4 + 3 <= jt ? v4.w : 0);
             }
-            __syncthreads();
+            int bt_l = s.wbin[lane][jt];
+            int win_l = n_l - below_l;
             if (all_t) {
-              done = true;
-            } else if (s.n_list <= kList) {
-              // the sub-bin of the K-th key (every warp finds it), its entries ranked
-              int b2, above2;
-              warp_find256(s.sub, need, b2, above2);
-              const int need2 = need - above2;
-              const int c2 = static_cast<int>(s.sub[b2]);
-              if (c2 <= kRank) {
-                const int nl = s.n_list;
-                const bool all2 = need2 == c2;
-                for (int e0 = warp * 32; e0 < nl; e0 += kThreads) {
-                  const int e = e0 + lane;
-                  int pos = 0, sd = -1;
-                  uint32_t key = 0;
-                  if (e < nl) {
-                    pos = s.list[e];
-                    key = s.ckey[pos];
-                    sd = static_cast<int>((key >> 12) & 0xFFu);
-                  }
-                  warp_emit(o, &s.n_out, K, sd > b2 || (all2 && sd == b2), e < nl ? s.cidx[pos] : 0);
-                  const bool stage = !all2 && sd == b2;
-                  const uint32_t bm = __ballot_sync(0xFFFFFFFFu, stage);
-                  if (bm) {
-                    int lb = 0;
-                    if (lane == 0) lb = atomicAdd(&s.n_rank, __popc(bm));
-                    lb = __shfl_sync(0xFFFFFFFFu, lb, 0) + __popc(bm & lanemask_lt());
-                    if (stage && lb < kRank) {
-                      s.rk[lb] = key;
-                      s.ri[lb] = s.cidx[pos];
-                    }
-                  }
+              win_l += bt_l;
+              bt_l = 0;
+            }
+            const int packed = warp_excl(sel_ok ? (win_l | (bt_l << 16)) : 0);  // both below 2^16
+            s.woff[lane][0] = packed & 0xFFFF;
+            s.woff[lane][1] = packed >> 16;
+            if (lane == 0) {
+              s.sel_ok = sel_ok ? 1 : 0;
+              s.t = (t0 << (20 - kFine)) + jt;
+              s.need = all_t ? 0 : need;  // 0: bin t is taken whole
+              s.in_t = in_t;
+            }
+          }
+          __syncthreads();
+          bool done = false;
+          if (s.sel_ok) {
+            // ---- winners above bin t out; bin t's entries into the ranking slots
+            const int t = s.t;
+            const int need = s.need;
+            const bool all_t = need == 0;
+            int ow = s.woff[warp][0];
+            int os = s.woff[warp][1];
+            const int cnt = min(s.wcnt[warp], kRegion);
+#pragma unroll 1
+            for (int e0 = 0; e0 < cnt; e0 += 32) {
+              const int e = e0 + lane;
+              uint32_t key = 0;
+              int32_t idx = 0;
+              int d = -1;
+              if (e < cnt) {
+                key = s.ckey[base + e];
+                idx = s.cidx[base + e];
+                d = static_cast<int>(key >> kFine);
+              }
+              const bool win = d > t || (all_t && d == t);
+              const bool inb = !all_t && d == t;
+              const uint32_t bw = __ballot_sync(0xFFFFFFFFu, win);
+              if (win) o[ow + __popc(bw & lt)] = idx;
+              ow += __popc(bw);
+              const uint32_t bb = __ballot_sync(0xFFFFFFFFu, inb);
+              if (inb) {
+                const int at = os + __popc(bb & lt);
+                s.rk[at] = key;
+                s.ri[at] = idx;
+              }
+              os += __popc(bb);
+            }
+            if (!all_t) {
+              const int in_t = s.in_t;
+              const int c4 = (in_t + 3) & ~3;
+              if (tid >= in_t && tid < c4) {  // padding never beats a real entry
+                s.rk[tid] = 0u;
+                s.ri[tid] = 0x7FFFFFFF;
+              }
+              __syncthreads();
+              if (tid < in_t) {
+                const uint32_t kj = s.rk[tid];
+                const int32_t ij = s.ri[tid];
+                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+                for (int i0 = 0; i0 < in_t; i0 += 4) {
+                  const uint4 k4 = *reinterpret_cast<const uint4*>(&s.rk[i0]);
+                  const int4 x4 = *reinterpret_cast<const int4*>(&s.ri[i0]);
+                  r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
+                  r1 += (k4.y > kj || (k4.y == kj && x4.y < ij)) ? 1 : 0;
+                  r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
+                  r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
                 }
-                const int c4 = (c2 + 3) & ~3;
-                if (tid >= c2 && tid < c4) {  // padding never beats a real entry
-                  s.rk[tid] = 0u;
-                  s.ri[tid] = 0x7FFFFFFF;
-                }
-                __syncthreads();
-                if (!all2 && tid < c2) {
-                  const uint32_t kj = s.rk[tid];
-                  const int32_t ij = s.ri[tid];
-                  int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-                  for (int i0 = 0; i0 < c2; i0 += 4) {
-                    const uint4 k4 = *reinterpret_cast<const uint4*>(&s.rk[i0]);
-                    const int4 x4 = *reinterpret_cast<const int4*>(&s.ri[i0]);
-                    r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
-                    r1 += (k4.y > kj || (k4.y == kj && x4.y < ij)) ? 1 : 0;
-                    r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
-                    r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
-                  }
-                  const int rank = r0 + r1 + r2 + r3;
-                  const int at = s.n_out + rank;
-                  if (rank < need2 && at < K) o[at] = ij;
-                }
-                done = true;
+                const int rank = r0 + r1 + r2 + r3;
+                if (rank < need) o[K - need + rank] = ij;
               }
             }
+            done = true;
           }
           if (!done) fallback_select(s, p, r, w);
         }
       }
     }
-    // the row's end: clear the histograms and counters, learn the next length,
-    // issue its window
+    // the row's end: clear the seed histogram, learn the next length, issue its window
     if (aborted) break;
     __syncthreads();
-    for (int b = tid; b < kBins; b += kThreads) {
-      s.hseed[b] = 0;
-      s.hcand[b] = 0;
-    }
-    if (tid < 256) s.sub[tid] = 0;
+    for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
+    for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
     if (warp == 0) {
       // blind pieces past this row's window may still be landing: wait for
       // them before the buffer takes the next window (lane q, piece q)
@@ -748,14 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
       const int ln = (rn < p.num_rows) ? clamp_len(p, __shfl_sync(0xFFFFFFFFu, len_n_raw, 0), lane == 0) : 0;
       if (lane == 0) {
         s.key_max = 0;
-        s.n_out = 0;
-        s.n_list = 0;
-        s.n_rank = 0;
         s.len_next = ln;
       }
       if (rn < p.num_rows && bulk) {
         const Win wn = make_win(p, rn, ln);
-        issue_pieces(s, wn, wn.np);
+        issue_pieces(s, wn, wn.np, true);
       }
     }
     par ^= issued;
