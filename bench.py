@@ -274,7 +274,9 @@ class GpuBench:
             return {"error": self.sar.topk_status_string(rc)}
         merge = "cluster" if pl.cluster else ("workspace" if pl.ctas_per_group > 1 else "none")
         shape = {1: "wide (24 consumer warps, 1 CTA/SM)", 2: "paired (12 consumer warps, 2 CTAs/SM)",
-                 3: "small (8 consumer warps)"}.get(pl.shape, str(pl.shape))
+                 3: "small (8 consumer warps)",
+                 4: "short-row (32 warps, 1 CTA/SM, row resident in or streamed through a 128 KB ring)"
+                 }.get(pl.shape, str(pl.shape))
         return {"ctas_per_row": pl.ctas_per_group, "grid": pl.grid, "merge": merge, "shape": shape}
 
     def flush_l2(self):

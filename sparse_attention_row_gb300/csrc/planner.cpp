@@ -69,8 +69,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   const bool wide_ok = props->ctas_per_sm >= 1 && props->smem_per_cta <= props->max_smem_optin;
   const bool pair_ok = props->pair_ctas_per_sm >= 1 && props->pair_smem_per_cta <= props->max_smem_optin;
   const bool small_ok = props->small_ctas_per_sm >= 1 && props->small_smem_per_cta <= props->max_smem_optin;
-  const bool short_ok = props->short_ctas_per_sm >= 1 && props->short_smem_per_cta <= props->max_smem_optin &&
-                        row_stride <= ltk::kShortMaxLen;
+  const bool short_ok = props->short_ctas_per_sm >= 1 && props->short_smem_per_cta <= props->max_smem_optin;
 
   // the CTA shape when it is not the planner's to choose, or when the wide
   // shape does not fit the device (then the largest whole-row shape that fits)
@@ -100,7 +99,8 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
         if (merge == 2 && clusters_of(G) < 1) return TOPK_ERR_PLAN;
         cluster = merge == 2 || (merge == 0 && clusters_of(G) >= 1);
       }
-    } else if (num_rows > 0 && row_stride > threshold && num_rows < cap) {
+    } else if (num_rows > 0 && row_stride > threshold && num_rows < cap &&
+               (!short_ok || shape == ltk::kShapeWide || row_stride >= ltk::kShortSplitStride)) {
       G = cap / num_rows;
       G = std::min<int64_t>(G, ltk::kMaxGroup);
       G = std::min<int64_t>(G, std::max<int64_t>(1, row_stride / ltk::kMinSpan));
@@ -125,7 +125,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     if (chosen == 0) {
       const bool pair = G == 1 && topk <= ltk::kPairMaxTopK && pair_ok && props->pair_ctas_per_sm >= 2 &&
                         num_rows >= ltk::kPairRowsPerSm * props->num_sms;
-      chosen = (G == 1 && short_ok) ? ltk::kShapeShort : pair ? ltk::kShapePair : ltk::kShapeWide;
+      chosen = pair ? ltk::kShapePair : (G == 1 && short_ok) ? ltk::kShapeShort : ltk::kShapeWide;
     }
   }
   plan->shape = chosen;

@@ -40,7 +40,13 @@ constexpr int kWideCtaThreads = 800;   // 24 consumer warps + the copy warp
 constexpr int kPairCtaThreads = 416;   // 12 consumer warps + the copy warp
 constexpr int kSmallCtaThreads = 288;  // 8 consumer warps + the copy warp
 constexpr int kShortCtaThreads = 1024;
-constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds
+constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds resident in its ring
+// Rows at least this long are split across CTAs even where the short-row
+// kernel could stream them whole: on a GB300 it streams a whole row faster
+// than a split of the other kernel merges it up to the workloads measured
+// (131072 and 163840 elements: 30.6 and 26.6 us whole against 34.5 and 30.0 us
+// split), so only far longer rows are split.
+constexpr int64_t kShortSplitStride = 1 << 20;
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.

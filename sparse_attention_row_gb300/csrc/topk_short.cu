@@ -47,26 +47,28 @@ namespace shortrow {
 constexpr int kThreads = kShortCtaThreads;  // 32 warps
 constexpr int kWarps = kThreads / 32;
 constexpr int kPiece = 2048;                        // elements per bulk copy (8 KB), one mbarrier each
+constexpr int kRing = 16;                           // ring slots of one piece (128 KB): a row of up to 16
+                                                    // pieces is resident; longer rows stream through it
 constexpr int kTask = 512;                          // window elements a warp filters at a time (4 float4 per lane)
-constexpr int kRowCap = kShortMaxLen + 4;           // window: the row plus up to 3 elements before it
-constexpr int kPieces = (kRowCap + kPiece - 1) / kPiece;
 constexpr int kSeed = kPiece;                       // window elements histogrammed for the seed (piece 0)
 constexpr int kRegion = 256;                        // candidate slots per warp
 constexpr int kCand = kWarps * kRegion;
 constexpr int kFine = 17;                           // fine bins: the top 15 key bits (key >> 17)
 constexpr int kTrack = 64;                          // fine bins counted during the filter, from the seed bin's edge
-constexpr int kRank = 128;                          // entries of the K-th key's fine bin ranked directly
-static_assert(kShortMaxLen < 65536, "candidate indices are 16-bit");
-static_assert(kPieces <= 32, "piece phases fit one 32-bit mask");
+constexpr int kRank = 512;                          // entries of the K-th key's fine bin ranked directly
+static_assert(kRing <= 32, "slot phases fit one 32-bit mask");
+static_assert(((kRing * kPiece) & (kRing * kPiece - 1)) == 0, "ring indices wrap with a mask");
+constexpr int kWrap = kRing * kPiece - 1;
 static_assert(kWarps == 32, "one lane of warp 0 per warp when offsets are scanned");
 static_assert(kPiece % kTask == 0 && kTask == 4 * 4 * 32, "a task is 4 float4 per lane, inside one piece");
 
 struct __align__(128) Smem {
-  float row[(kRowCap + 3) & ~3];  // the row's window (bulk-copy destination)
+  float row[kRing * kPiece];      // the ring: slot q holds pieces q, q + kRing, ... of the window
   uint32_t ckey[kCand];           // candidate keys, warp w in [w * kRegion, (w + 1) * kRegion)
-  uint16_t cidx[kCand];           // candidate indices (first the survivors' task positions)
+  int32_t cidx[kCand];            // candidate indices (first the survivors' task positions)
   uint32_t hseed[kBins];          // seed histogram; scratch of the fallback
   uint32_t bsum[kBins / 32];      // 32-bin block sums (find_top, in the fallback)
+  alignas(16) uint32_t hsub[256]; // the seed bin's 8-bit sub-histogram (key bits 19..12)
   alignas(16) uint32_t rk[kRank];
   alignas(16) int32_t ri[kRank];
   alignas(16) int wbin[kWarps][kTrack + 4];  // per warp: candidates in fine bin f0 + j (f0: the seed bin's
@@ -74,13 +76,18 @@ struct __align__(128) Smem {
   int woff[kWarps][2];            // per warp: output offset, ranking-slot offset
   int wcnt[kWarps];               // survivors per warp (may exceed kRegion: overflow)
   int tcnt[kWarps];               // fallback: ties per warp before the scan
-  unsigned long long bar[kPieces];
+  unsigned long long bar[kRing];
+  int pdone[kRing];               // warps done with the piece in a slot (streaming rows)
+  int slot_issues[kRing];         // copies issued into each slot since the launch began
   int abort;
   int len_next;
   int fb, fgt;                    // find_top result (fallback)
   int n_out;
   uint32_t key_max;
   int t0, t, need, in_t, sel_ok;  // seed bin, the K-th key's fine bin, its entries taken and held, fast path ok
+  int crowded;                    // the seed bin of a streamed row is crowded (heavy ties)
+  int refine, need_in;            // the seed bin is wide: refine the threshold inside it, to `need_in` of its entries
+  uint32_t thr_key;               // the filter keeps keys >= thr_key
 };
 
 // ---------------------------------------------------------------- primitives
@@ -265,40 +272,58 @@ __device__ __forceinline__ Win make_win(const Params& p, int64_t r, int n) {
   return w;
 }
 
-// Issues the bulk copies of pieces [0, np) of window w: lane q of the calling
-// warp issues piece q, so the copies leave together. Each 16-byte granule
-// copied holds at least one element of the row, so no copy leaves the row's
-// pages.
-__device__ __forceinline__ void issue_pieces(Smem& s, const Win& w, int np, bool after_use) {
-  const int q = static_cast<int>(lane_id());
-  if (q < np) {
-    if (after_use) fence_proxy_async();  // the buffer was read through the generic proxy
-    const int e0 = q * kPiece;
-    const int e1 = min(e0 + kPiece, w.nwin);
-    bulk_copy(&s.row[e0], w.rowp - w.mis + e0, static_cast<uint32_t>(e1 - e0) * 4u, &s.bar[q]);
+// Issues the bulk copy of window piece j into ring slot q. Each 16-byte
+// granule copied holds at least one element of the row, so no copy leaves the
+// row's pages.
+__device__ __forceinline__ void issue_piece(Smem& s, const Win& w, int j, int q, bool after_use) {
+  if (after_use) fence_proxy_async();  // the slot was read through the generic proxy
+  const int e0 = j * kPiece;
+  const int e1 = min(e0 + kPiece, w.nwin);
+  s.slot_issues[q] += 1;
+  bulk_copy(&s.row[q * kPiece], w.rowp - w.mis + e0, static_cast<uint32_t>(e1 - e0) * 4u, &s.bar[q]);
+}
+
+// Pieces [i0, i1) of window w (i1 - i0 <= 32), piece i into slot (s0 + i) %
+// kRing: lane l of the calling warp issues piece i0 + l, so the copies leave
+// together.
+__device__ __forceinline__ void issue_pieces(Smem& s, const Win& w, int i0, int i1, int s0, bool after_use) {
+  const int i = i0 + static_cast<int>(lane_id());
+  if (i < i1) issue_piece(s, w, i, (s0 + i) % kRing, after_use);
+}
+
+// Parity flips of the slots over the ring positions [s0, s0 + span) of one row.
+__device__ __forceinline__ uint32_t slot_flips(int s0, int span) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int q = 0; q < kRing; ++q) {
+    const int d = (q - s0 + kRing) % kRing;  // the row's first position in slot q
+    const int uses = (d < span) ? (span - 1 - d) / kRing + 1 : 0;
+    m |= static_cast<uint32_t>(uses & 1) << q;
   }
+  return m;
+}
+
+// Element e of a row: in the ring, at (off + e) & wrap; else x[e * xs].
+__device__ __forceinline__ float xload(const float* x, int64_t xs, int off, int wrap, int e) {
+  return wrap ? x[(off + e) & wrap] : x[static_cast<int64_t>(e) * xs];
 }
 
 // ---------------------------------------------------------------- fallback
 
-// Exact selection over the resident row, whatever the data: three radix levels
-// over the full key (12, 12 and 8 bits) find the K-th key T and how many of the
-// keys equal to T are taken; then the keys above T are written out, and the
-// ties in index order (each thread owns a contiguous segment of the row; a
-// block-wide scan of the segments' tie counts ranks them). Histograms count runs
-// of equal digits within a segment with one atomic, so tie-heavy rows cost few
-// atomics. Rewrites the whole output row.
-__device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r, const Win& w) {
+// The K-th key of x[0, n) (stride xs), exactly, whatever the data: three radix
+// levels over the full key (12, 12 and 8 bits). Returns the key T; `need` is
+// how many of the keys equal to T are among the K best (the first ones in
+// index order). Each thread owns a contiguous segment of x; histograms count
+// runs of equal digits within a segment with one atomic, so tie-heavy rows cost
+// few atomics. Uses s.hseed. Block-wide; every thread gets the answer.
+__device__ __noinline__ uint32_t exact_kth(Smem& s, const float* x, int64_t xs, int off, int wrap, int n, int K,
+                                          int& need) {
   const int tid = threadIdx.x;
-  const int lane = static_cast<int>(lane_id());
-  const int warp = tid >> 5;
-  const int K = p.topk;
-  const int seg = (((w.len + kThreads - 1) / kThreads) + 3) & ~3;
-  const int e_lo = min(tid * seg, w.len);
-  const int e_hi = min(e_lo + seg, w.len);
-  const float* x = s.row + w.mis;
+  const int seg = (((n + kThreads - 1) / kThreads) + 3) & ~3;
+  const int e_lo = min(tid * seg, n);
+  const int e_hi = min(e_lo + seg, n);
   uint32_t prefix = 0;
-  int need = K;
+  need = K;
   // levels: bits 31..20, 19..8 (within prefix), 7..0 (within prefix)
 #pragma unroll 1
   for (int lv = 0; lv < 3; ++lv) {
@@ -309,7 +334,7 @@ __device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r
     __syncthreads();
     uint32_t cur = 0xFFFFFFFFu, run = 0;
     for (int e = e_lo; e < e_hi; ++e) {
-      const uint32_t k = fkey(x[e]);
+      const uint32_t k = fkey(xload(x, xs, off, wrap, e));
       if (pshift < 32 && (k >> pshift) != prefix) continue;
       const uint32_t d = (k >> shift) & mask;
       if (d != cur) {
@@ -325,10 +350,29 @@ __device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r
     need -= s.fgt;
     prefix = (prefix << (lv == 2 ? 8 : 12)) | static_cast<uint32_t>(s.fb);
   }
-  const uint32_t T = prefix;  // the K-th key; `need` of the keys equal to T are taken
+  return prefix;
+}
+
+// Exact selection over a whole row, whatever the data (the fallback of the
+// fast path): the K-th key T from exact_kth, then the keys above T are written
+// out, and the ties in index order (each thread owns a contiguous segment of
+// the row; a block-wide scan of the segments' tie counts ranks them).
+// Rewrites the whole output row. x is the resident window or the row in
+// global memory.
+__device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r, const Win& w, const float* x,
+                                             int64_t xs, int off, int wrap) {
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const int warp = tid >> 5;
+  const int K = p.topk;
+  const int seg = (((w.len + kThreads - 1) / kThreads) + 3) & ~3;
+  const int e_lo = min(tid * seg, w.len);
+  const int e_hi = min(e_lo + seg, w.len);
+  int need;
+  const uint32_t T = exact_kth(s, x, xs, off, wrap, w.len, K, need);  // `need` of the keys equal to T are taken
   // ties per thread segment, then an exclusive scan over the threads in order
   int ties = 0;
-  for (int e = e_lo; e < e_hi; ++e) ties += (fkey(x[e]) == T) ? 1 : 0;
+  for (int e = e_lo; e < e_hi; ++e) ties += (fkey(xload(x, xs, off, wrap, e)) == T) ? 1 : 0;
   int incl = ties;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -347,7 +391,7 @@ __device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r
     const int e = e_lo + j;
     bool sel = false;
     if (e < e_hi) {
-      const uint32_t k = fkey(x[e]);
+      const uint32_t k = fkey(xload(x, xs, off, wrap, e));
       if (k > T) {
         sel = true;
       } else if (k == T) {
@@ -420,6 +464,39 @@ __device__ __forceinline__ void warp_scan_down(const uint32_t* h, int top, int n
   above = static_cast<int>(carry);  // unreachable when the total reaches need
 }
 
+// One warp, every lane with the same answer: over h[0, 256), the largest bin b
+// whose suffix sum reaches need (1 <= need <= total).
+__device__ __forceinline__ int warp_find256(const uint32_t* h, int need) {
+  const int lane = static_cast<int>(lane_id());
+  const uint4 lo4 = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
+  const uint4 hi4 = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
+  const uint32_t v[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};  // bins 255-8l down
+  uint32_t own = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) own += v[k];
+  uint32_t incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= static_cast<uint32_t>(need));
+  const int L = hit ? __ffs(hit) - 1 : 31;
+  uint32_t run = __shfl_sync(0xFFFFFFFFu, incl - own, L);
+  int b = 255 - 8 * L - 7;
+  bool found = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t vk = __shfl_sync(0xFFFFFFFFu, v[k], L);
+    if (!found && run + vk >= static_cast<uint32_t>(need)) {
+      b = 255 - 8 * L - k;
+      found = true;
+    }
+    if (!found) run += vk;
+  }
+  return b;
+}
+
 // Exclusive prefix over the lanes of a warp.
 __device__ __forceinline__ int warp_excl(int v) {
   const int lane = static_cast<int>(lane_id());
@@ -430,6 +507,15 @@ __device__ __forceinline__ int warp_excl(int v) {
     if (lane >= o) incl += x;
   }
   return incl - v;
+}
+
+__device__ __forceinline__ int atom_add_acq_rel_cta(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(smem_addr(p)), "r"(v)
+               : "memory");
+  return old;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p) {
@@ -444,40 +530,57 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   int64_t r = blockIdx.x;
   if (r >= p.num_rows) return;
 
-  // Set-up: warp 0's lanes initialise the piece barriers and, with contiguous
-  // rows, issue the first row's blind window (sized by max_len) before
-  // anything else; the first length is loaded now, used once the data is in.
+  // Set-up: warp 0's lanes initialise the slot barriers and, with contiguous
+  // rows, issue the first row's blind window (sized by max_len, at most a
+  // ring's worth) before anything else; the first length is loaded now, used
+  // once the data is in.
   const int32_t len_raw0 = __ldg(p.lengths + r);
   int blind = 0;  // pieces of the first row in flight before its length is known
-  if (bulk) blind = make_win(p, r, static_cast<int>(p.max_len)).np;  // the same in every thread
+  if (bulk) blind = min(make_win(p, r, static_cast<int>(p.max_len)).np, kRing);  // the same in every thread
   if (warp == 0) {
-    if (lane < kPieces) {
+    if (lane < kRing) {
       mbar_init(&s.bar[lane], 1u);
       fence_mbar_init();
+      s.pdone[lane] = 0;
+      s.slot_issues[lane] = 0;
     }
     if (lane == 0) {
       s.abort = 0;
       s.key_max = 0;
     }
-    if (bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), blind, false);
+    if (bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), 0, blind, 0, false);
   }
   for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
   for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
+  if (tid < 256) s.hsub[tid] = 0;
   __syncthreads();
   int len = clamp_len(p, len_raw0, tid == 0);
 
-  uint32_t par = 0;  // bit q: parity of the next phase of piece q's barrier
+  uint32_t par = 0;  // bit q: parity of the next phase of slot q's barrier
+  int S = 0;         // ring slot of the current row's piece 0 (rows follow one another round the ring)
   bool aborted = false;
 #pragma unroll 1
   for (int64_t k = 0; r < p.num_rows; ++k) {
     const int64_t rn = r + gridDim.x;
-    int32_t len_n_raw = 0;
-    if (tid == 0 && rn < p.num_rows) len_n_raw = __ldg(p.lengths + rn);  // consumed at the row's end
+    if (tid == 0) s.len_next = (rn < p.num_rows) ? clamp_len(p, __ldg(p.lengths + rn), true) : 0;
     const Win w = make_win(p, r, len);
     int32_t* o = p.out + r * static_cast<int64_t>(K);
-    const uint32_t issued = (k == 0) ? ((1u << blind) - 1u) : ((1u << w.np) - 1u);
+    const int dead = (k == 0) ? blind : 0;     // the first row's blind pieces (those past its window are dead)
+    const bool stream = bulk && w.np > kRing;  // the row streams through the ring
+    // ring positions the row takes (its pieces, and the first row's dead blind ones)
+    const int span = bulk ? max(w.np, dead) : 0;
+    const int S_next = (S + span) % kRing;
+    // cross-row prefetch: the next row's first pieces go into the ring while this
+    // row is still being filtered, as slots come free (not after a row of dead
+    // blind pieces, whose slots free up only at its end, nor after a trivial row)
+    const bool cross = bulk && rn < p.num_rows && w.nwin > 0 && dead <= w.np;
+    Win wn{};
+    int np_next = 0;  // the next row's pieces that this row hands slots to
     if (w.nwin == 0) {
       for (int j = tid; j < K; j += kThreads) o[j] = (j < len) ? j : -1;
+    } else if (!bulk && w.nwin > kRing * kPiece) {
+      // a strided row longer than the ring: exact selection straight from global memory
+      fallback_select(s, p, r, w, w.rowp, p.col_stride, 0, 0);
     } else {
       if (!bulk) {
         // strided rows: every thread loads its elements into the window
@@ -485,14 +588,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
         for (int e = tid; e < len; e += kThreads) s.row[e] = __ldg(w.rowp + static_cast<int64_t>(e) * cs);
         __syncthreads();
       }
-      // ---- seed: the top 12 key bits of piece 0 and its largest key
-      bool ok = !bulk || piece_ready(s, 0, par & 1u, p.timeout_ns);
+      // ---- seed: the top 12 key bits of piece 0 (slot S) and its largest key
+      bool ok = !bulk || piece_ready(s, S, (par >> S) & 1u, p.timeout_ns);
       const int seed_hi = min(kSeed, w.nwin);
+      const float* seed = s.row + S * kPiece;  // a piece never wraps round the ring
       uint32_t kmax = 0;
       for (int i = tid; i < seed_hi; i += kThreads) {
         const int e = i - w.mis;
         if (e >= 0 && e < len) {
-          const uint32_t key = fkey(s.row[i]);
+          const uint32_t key = fkey(seed[i]);
           kmax = max(kmax, key);
           atomicAdd(&s.hseed[key >> 20], 1u);
         }
@@ -502,43 +606,134 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
       if (sync_or(!ok)) {
         aborted = true;
       } else {
+        if (cross) {
+          // the next row's length is in (thread 0 wrote it before the barrier); its
+          // first pieces whose slots this row never takes go into the ring now
+          wn = make_win(p, rn, s.len_next);
+          np_next = min(wn.np, kRing);
+          if (warp == 0) issue_pieces(s, wn, 0, min(np_next, kRing - span), S_next, true);
+        }
         if (warp == 0) {
           const int n_seed = min(len, kSeed - w.mis);
           int target = K;
           if (n_seed < len) {
-            const int64_t tt = (5ll * K * n_seed + 4ll * len - 1) / (4ll * len);
-            target = static_cast<int>(tt < 1 ? 1 : tt);
+            // mu = the expected count of the row's K best in the sample; aim three
+            // standard deviations above it (mu is small on long rows), so a sample
+            // that runs short of it still leaves K survivors
+            const float mu = static_cast<float>(K) * static_cast<float>(n_seed) / static_cast<float>(len);
+            target = max(1, static_cast<int>(ceilf(mu + 3.0f * sqrtf(mu) + 2.0f)));
           }
           target = min(target, n_seed);
           int t0, above0;
           warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
-          if (lane == 0) s.t0 = t0;
+          const int c0 = static_cast<int>(s.hseed[t0]);
+          const int need_in = target - above0;  // of bin t0's sample entries, 1 .. c0
+          // a crowded seed bin on a streamed row (heavy ties): the seed piece holds
+          // K or more elements at or above t0, and the projection over the row
+          // overflows the candidate regions
+          const int at_or_above = above0 + static_cast<int>(s.hseed[t0]);
+          const bool crowded = stream && n_seed >= K && at_or_above >= K &&
+                               static_cast<int64_t>(at_or_above) * len > (3ll * kCand / 4) * n_seed;
+          // a wide seed bin (its sample count well beyond what the target needs from
+          // it) is split on the next 8 key bits, so the threshold lands close to it
+          const bool refine = !crowded && c0 - need_in > max(target / 4, 16);
+          if (lane == 0) {
+            s.t0 = t0;
+            s.crowded = crowded ? 1 : 0;
+            s.refine = refine ? 1 : 0;
+            s.need_in = need_in;
+            s.thr_key = static_cast<uint32_t>(t0) << 20;
+          }
         }
         __syncthreads();
-        // ---- filter: warp tasks of 512 window elements; lane l of a task takes
-        // float4s l, l + 32, l + 64, l + 96 of it
-        const int t0 = s.t0;
-        const float thr = key_floor_value(static_cast<uint32_t>(t0) << 20);
-        const int f0 = t0 << (20 - kFine);  // the seed bin's lower edge as a fine bin
-        const int nvec = w.nwin >> 2;
-        const int ntask = (w.nwin + kTask - 1) / kTask;
+        if (s.refine) {
+          const uint32_t t0 = static_cast<uint32_t>(s.t0);
+          for (int i = tid; i < seed_hi; i += kThreads) {
+            const int e = i - w.mis;
+            if (e >= 0 && e < len) {
+              const uint32_t key = fkey(seed[i]);
+              if ((key >> 20) == t0) atomicAdd(&s.hsub[(key >> 12) & 0xFFu], 1u);
+            }
+          }
+          __syncthreads();
+          if (warp == 0) {
+            const int b = warp_find256(s.hsub, s.need_in);
+            if (lane == 0) s.thr_key = (t0 << 20) | (static_cast<uint32_t>(b) << 12);
+          }
+          __syncthreads();
+        }
+        // ---- filter: warp tasks of 128 F window elements; lane l of a task takes
+        // float4s l, l + 32, ... of it. Piece j sits in slot j % kRing; on a
+        // streamed row the last of its tasks hands the slot to piece j + kRing.
+        uint32_t thr_key = s.thr_key;  // the filter keeps keys >= thr_key
+        float thr = key_floor_value(thr_key);
         const int base = warp * kRegion;
         int wc = 0;
         int* my_bins = s.wbin[warp];  // this warp's own counters: no other warp touches them
+        if (s.crowded) {
+          // The seed piece's own K best: its K-th key T, and the first need_t of
+          // its elements equal to T in index order. Every later element of the
+          // row has a larger index than all of them, so one equal to T can never
+          // be selected: the filter keeps key > T only (exact for any data).
+          const int n_seed = min(len, kSeed - w.mis);
+          int need_t;
+          const uint32_t T = exact_kth(s, seed, 1, w.mis, 0, n_seed, K, need_t);
+          thr_key = T;  // the fine bins count from T's (the ties are candidates)
+          thr = key_floor_value(T + 1u);  // T is at most the key of +inf, so T + 1 does not wrap
+          // thread i owns seed elements 2i and 2i + 1; a block scan ranks the ties
+          const int ea = 2 * tid;
+          const bool ta = ea < n_seed && fkey(seed[w.mis + ea]) == T;
+          const bool tb = ea + 1 < n_seed && fkey(seed[w.mis + ea + 1]) == T;
+          const int mine = (ta ? 1 : 0) + (tb ? 1 : 0);
+          int incl = mine;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += x;
+          }
+          if (lane == 31) s.tcnt[warp] = incl;
+          __syncthreads();
+          int before = incl - mine;
+          for (int q = 0; q < warp; ++q) before += s.tcnt[q];
+          const bool sa = ta && before < need_t;
+          const bool sb = tb && before + (ta ? 1 : 0) < need_t;
+          const int sel = (sa ? 1 : 0) + (sb ? 1 : 0);
+          const int at = base + warp_excl(sel);  // at most 64 per warp: inside its region
+          if (sa) {
+            s.ckey[at] = T;
+            s.cidx[at] = ea;
+          }
+          if (sb) {
+            s.ckey[at + (sa ? 1 : 0)] = T;
+            s.cidx[at + (sa ? 1 : 0)] = ea + 1;
+          }
+          wc = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(sel)));
+          if (lane == 0 && wc) atomicAdd(&my_bins[0], wc);  // fine bin T >> kFine is f0
+          __syncthreads();
+        }
+        const int f0 = static_cast<int>(thr_key >> kFine);  // every candidate's fine bin is at least f0
+        const int nvec = w.nwin >> 2;
+        // float4s per lane in a task: short windows take smaller tasks, so that every
+        // warp gets some and no warp's region has to hold a large share of survivors
+        const int F = (w.nwin > 16 * kTask) ? 4 : (w.nwin > 8 * kTask) ? 2 : 1;
+        const int tsz = 128 * F;  // window elements per task
+        const int ntask = (w.nwin + tsz - 1) / tsz;
 #pragma unroll 1
         for (int task = warp; task < ntask; task += kWarps) {
-          const int q = (task * kTask) / kPiece;
-          if (bulk && q >= 1 && !piece_ready(s, q, (par >> q) & 1u, p.timeout_ns)) {
+          const int j = (task * tsz) / kPiece;    // window piece
+          const int q = (S + j) % kRing;          // its slot
+          if (bulk && j >= 1 && !piece_ready(s, q, ((par >> q) ^ static_cast<uint32_t>(j / kRing)) & 1u, p.timeout_ns)) {
             ok = false;  // the whole warp leaves the filter; the barrier below decides for the CTA
             break;
           }
-          const int v0 = task * (kTask / 4);
+          const int sb = q * kPiece + (task * tsz) % kPiece;  // the task's first element in the ring
+          const int v0 = task * (tsz / 4);                    // and its first float4 in the window
           uint32_t m = 0;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int v = v0 + lane + 32 * i;
-            if (v < nvec) {
-              const float4 f = *reinterpret_cast<const float4*>(&s.row[4 * v]);
+            if (i < F && v < nvec) {
+              const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
               uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
                            (f.w >= thr ? 8u : 0u);
               const int e0 = 4 * v - w.mis;
@@ -560,33 +755,50 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
             tot += __popc(qb[bit]) << bit;
             pre += __popc(qb[bit] & lt) << bit;
           }
-          if (tot == 0) continue;
-          if (wc + tot <= kRegion) {
-            // each lane notes where its survivors are (task positions) in the
-            // region, then the warp converts them 32 at a time
-            int at = base + wc + pre;
-            while (m) {
-              const int j = __ffs(m) - 1;
-              m &= m - 1;
-              s.cidx[at++] = static_cast<uint16_t>(4 * (lane + 32 * (j >> 2)) + (j & 3));
-            }
-            __syncwarp();
-#pragma unroll 1
-            for (int e0 = 0; e0 < tot; e0 += 32) {
-              const int e = e0 + lane;
-              const bool valid = e < tot;
-              if (valid) {
-                const int pos = task * kTask + s.cidx[base + wc + e];
-                const uint32_t key = fkey(s.row[pos]);
-                s.ckey[base + wc + e] = key;
-                s.cidx[base + wc + e] = static_cast<uint16_t>(pos - w.mis);
-                const int d = static_cast<int>(key >> kFine) - f0;
-                if (d < kTrack) atomicAdd(&my_bins[d], 1);
+          if (tot > 0) {
+            if (wc + tot <= kRegion) {
+              // each lane notes where its survivors are (task positions) in the
+              // region, then the warp converts them 32 at a time
+              int at = base + wc + pre;
+              while (m) {
+                const int jb = __ffs(m) - 1;
+                m &= m - 1;
+                s.cidx[at++] = 4 * (lane + 32 * (jb >> 2)) + (jb & 3);
               }
+              __syncwarp();
+#pragma unroll 1
+              for (int e0 = 0; e0 < tot; e0 += 32) {
+                const int e = e0 + lane;
+                if (e < tot) {
+                  const int pos = s.cidx[base + wc + e];
+                  const uint32_t key = fkey(s.row[sb + pos]);
+                  s.ckey[base + wc + e] = key;
+                  s.cidx[base + wc + e] = task * tsz + pos - w.mis;
+                  const int d = static_cast<int>(key >> kFine) - f0;
+                  if (d < kTrack) atomicAdd(&my_bins[d], 1);
+                }
+              }
+              __syncwarp();
             }
-            __syncwarp();
+            wc += tot;
           }
-          wc += tot;
+          // once every task of piece j is done, its slot goes to piece j + kRing of
+          // this row, or, on a streamed row, on to the next row's piece j + kRing -
+          // np (a resident row keeps its slots until it is selected: its exact
+          // fallback reads them)
+          const bool same = bulk && j + kRing < w.np;
+          const bool onto_next = cross && stream && !same && j + kRing - w.np < np_next;
+          if (same || onto_next) {
+            const int tasks_j = min(kPiece / tsz, ntask - j * (kPiece / tsz));  // a last piece may be short
+            __syncwarp();  // every lane's reads of the slot come before the hand-over
+            if (lane == 0 && atom_add_acq_rel_cta(&s.pdone[q], 1) == tasks_j - 1) {
+              s.pdone[q] = 0;
+              if (same)
+                issue_piece(s, w, j + kRing, q, true);
+              else
+                issue_piece(s, wn, j + kRing - w.np, q, true);
+            }
+          }
         }
         if (lane == 0) s.wcnt[warp] = wc;
         if (sync_or(!ok)) {
@@ -642,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
             s.woff[lane][1] = packed >> 16;
             if (lane == 0) {
               s.sel_ok = sel_ok ? 1 : 0;
-              s.t = (t0 << (20 - kFine)) + jt;
+              s.t = f0 + jt;
               s.need = all_t ? 0 : need;  // 0: bin t is taken whole
               s.in_t = in_t;
             }
@@ -707,44 +919,55 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
             }
             done = true;
           }
-          if (!done) fallback_select(s, p, r, w);
+          // a streamed row is read again from global memory; a resident one (strided rows
+          // included: they were loaded contiguously) from the ring
+          if (!done) {
+            if (stream)
+              fallback_select(s, p, r, w, w.rowp, 1, 0, 0);
+            else
+              fallback_select(s, p, r, w, s.row, 1, (bulk ? S * kPiece : 0) + w.mis, kWrap);
+          }
         }
       }
     }
     // the row's end: clear the seed histogram, learn the next length, issue its window
     if (aborted) break;
     __syncthreads();
+    // read here, between two barriers: thread 0 writes the one after it at the next row's start
+    const int len_next = s.len_next;
     for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
     for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
+    if (tid < 256) s.hsub[tid] = 0;
     if (warp == 0) {
-      // blind pieces past this row's window may still be landing: wait for
-      // them before the buffer takes the next window (lane q, piece q)
-      if (lane < kPieces && lane >= w.np && ((issued >> lane) & 1u))
+      // the first row's blind pieces past its window may still be landing:
+      // wait for them before the ring takes the next window (lane q, slot q;
+      // the first row starts at slot 0)
+      if (lane < kRing && lane >= w.np && lane < dead)
         wait_piece(&s.bar[lane], (par >> lane) & 1u, p.timeout_ns, &s.abort);
       __syncwarp();
-      const int ln = (rn < p.num_rows) ? clamp_len(p, __shfl_sync(0xFFFFFFFFu, len_n_raw, 0), lane == 0) : 0;
-      if (lane == 0) {
-        s.key_max = 0;
-        s.len_next = ln;
-      }
-      if (rn < p.num_rows && bulk) {
-        const Win wn = make_win(p, rn, ln);
-        issue_pieces(s, wn, wn.np, true);
+      if (lane == 0) s.key_max = 0;
+      // the next row's first pieces not yet in the ring: all of them without
+      // cross-row prefetch, else those whose slots a resident row kept
+      if (rn < p.num_rows && bulk && !(cross && stream)) {
+        const Win wn2 = make_win(p, rn, len_next);
+        const int i0 = cross ? max(0, kRing - span) : 0;
+        issue_pieces(s, wn2, i0, min(wn2.np, kRing), S_next, true);
       }
     }
-    par ^= issued;
+    par ^= slot_flips(S, span);
+    S = S_next;
     __syncthreads();
     r = rn;
-    if (r < p.num_rows) len = s.len_next;
+    len = len_next;
   }
   if (aborted && tid == 0) {
-    // a piece did not land in time: flag it, and wait (bounded) for every
-    // copy of the row still in flight before the CTA leaves
+    // a piece did not land in time: flag it, and wait (bounded) for the last
+    // copy issued into every slot before the CTA leaves
     atomicOr(p.status, 0x4u);
-    const uint32_t issued = (r == static_cast<int64_t>(blockIdx.x)) ? ((1u << blind) - 1u)
-                                                                   : ((1u << make_win(p, r, len).np) - 1u);
-    for (int q = 0; q < 32; ++q)
-      if ((issued >> q) & 1u) wait_piece(&s.bar[q], (par >> q) & 1u, p.timeout_ns, nullptr);
+    for (int q = 0; q < kRing; ++q) {
+      const int n = s.slot_issues[q];
+      if (n > 0) wait_piece(&s.bar[q], static_cast<uint32_t>(n - 1) & 1u, p.timeout_ns, nullptr);
+    }
   }
 }
 

@@ -91,11 +91,13 @@ SHORT_CASES = 40
 
 
 def _short_case(seed: int):
-    """Batches for the short-row kernel: rows of at most 32768 elements, one CTA per row (or
-    several rows per CTA), every value mix, TopK up to 4096."""
+    """Batches for the short-row kernel: rows resident in its ring (up to 32768 elements) and
+    rows streamed through it (up to 140000), one CTA per row or several rows per CTA, every value
+    mix, TopK up to 4096."""
     rng = np.random.default_rng(2_000_029 * seed + 5)
     topk = int(rng.choice([int(rng.integers(1, 65)), 512, 1024, 2048, int(rng.integers(1, 4097))]))
-    stride = int(rng.choice([int(rng.integers(1, 5000)), int(rng.integers(5000, 32769)), 32768]))
+    stride = int(rng.choice([int(rng.integers(1, 5000)), int(rng.integers(5000, 32769)), 32768,
+                             int(rng.integers(32769, 140000))]))
     num_rows = int(rng.integers(1, min(200, MAX_ELEMENTS // stride) + 1))
     x = np.stack([_row(rng, stride) for _ in range(num_rows)])
     lengths = rng.integers(0, stride + 1, size=num_rows)

@@ -30,12 +30,11 @@ def test_workloads_small_auto(rn, name, rows):
 @pytest.mark.parametrize("shape", [1, 2, 3, 4])
 @pytest.mark.parametrize("name,rows", SMALL)
 def test_workloads_small_other_shapes(rn, name, rows, shape):
-    """Every CTA shape forced on every workload it can hold: the wide one (24 consumer warps), the
-    paired one (two CTAs of 12 consumer warps per SM), the small, low-shared-memory one (8 consumer
-    warps), and the short-row kernel (a whole row of at most 32768 elements in shared memory)."""
+    """Every CTA shape forced on every workload: the wide one (24 consumer warps), the paired one
+    (two CTAs of 12 consumer warps per SM), the small, low-shared-memory one (8 consumer warps), and
+    the short-row kernel (32 warps; rows of up to 16 pieces resident, longer rows streamed through
+    its ring of 16 slots)."""
     w = workloads.make(name, rows)
-    if shape == 4 and w.row_stride > 32768:
-        pytest.skip("the short-row kernel holds rows of at most 32768 elements")
     got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=shape))
     assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} shape={shape}")
     assert rn.workspace_clean()
@@ -48,7 +47,7 @@ def test_runtime_topk(rn, topk, G, merge, shape):
     if shape in (2, 3) and topk > 2048:
         pytest.skip("the paired and small shapes serve TopK up to 2048")
     rng = np.random.default_rng(topk)
-    S = 40000 if shape != 4 else 32768
+    S = 40000
     x = np.round(rng.standard_normal((12, S)) * 32).astype(np.float32) / 32  # heavy ties
     lens = rng.integers(0, S, 12, endpoint=True).astype(np.int32)
     lens[:4] = [0, topk - 1 if topk > 1 else 0, topk, S]
@@ -201,8 +200,6 @@ def _edge_rows(S: int, K: int, rng) -> tuple[np.ndarray, np.ndarray]:
 @pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 1), (0, 0, 2), (0, 0, 3), (4, 1, 0), (4, 2, 0), (8, 2, 0),
                                            (0, 0, 4)])
 def test_edge_cases(rn, topk, S, G, merge, shape):
-    if shape == 4 and S > 32768:
-        pytest.skip("the short-row kernel holds rows of at most 32768 elements")
     # with G = 8 and K = 2048 the all-equal row keeps 8 x K candidates at one
     # key, more than the leader's buffer: the cluster merge hands over to the
     # workspace merge

@@ -274,24 +274,32 @@ def test_static_scratch_capacity_is_reachable_on_larger_devices():
 
 
 def test_short_row_kernel():
-    """Whole rows of at most 32768 elements take the short-row kernel where the device holds it."""
+    """Whole rows take the short-row kernel where the device holds it (rows of up to 16 pieces
+    stay resident in its ring, longer ones stream through it), except batches of at least four
+    rows per SM, which the paired shape streams; only very long rows are split across CTAs."""
     gb = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT)
-    for rows, stride, k in ((8, 4096, 512), (64, 32768, 2048), (1, 1, 1), (4096, 32768, 2048), (300, 6000, 4096)):
+    for rows, stride, k in ((8, 4096, 512), (64, 32768, 2048), (1, 1, 1), (300, 6000, 4096),
+                            (16, 131072, 2048), (64, 163840, 1024), (4096, 65536, 3000)):
         rc, pl = plan(gb, rows, stride, topk=k)
-        assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1 and pl.threads == 1024
+        assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1 and pl.threads == 1024, (rows, stride, k)
         assert pl.grid == min(rows, 152) and not pl.cooperative and not pl.cluster
-    # longer rows keep the streaming shapes
-    rc, pl = plan(gb, 64, 32769)
-    assert rc == 0 and pl.shape != 4
-    rc, pl = plan(gb, 16, 131072)
-    assert rc == 0 and pl.shape == 1 and pl.cluster
-    # forcing: shape 4 needs rows that fit and one CTA per row
+    for rows, stride in ((4096, 65536), (4096, 32768), (608, 20000)):
+        rc, pl = plan(gb, rows, stride)
+        assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1
+    # rows of a million elements and more, few of them, are still split across CTAs
+    rc, pl = plan(gb, 16, 1 << 21)
+    assert rc == 0 and pl.shape == 1 and pl.ctas_per_group > 1
+    # forcing: shape 4 takes any length, but one CTA per row
     rc, pl = plan(gb, 10, 32768, shape=4, max_ctas=3)
     assert rc == 0 and pl.shape == 4 and pl.grid == 3
-    assert plan(gb, 10, 40000, shape=4)[0] == sar.TOPK_ERR_PLAN
+    rc, pl = plan(gb, 10, 400000, shape=4)
+    assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1
     assert plan(gb, 10, 30000, shape=4, force_ctas_per_group=2)[0] == sar.TOPK_ERR_INVALID_ARG
     rc, pl = plan(gb, 10, 30000, force_ctas_per_group=2)
     assert rc == 0 and pl.shape == 1 and pl.ctas_per_group == 2
+    # the wide shape forced: the split rule of that kernel applies
+    rc, pl = plan(gb, 16, 131072, shape=1)
+    assert rc == 0 and pl.shape == 1 and pl.cluster and pl.ctas_per_group == 6
     # a device that cannot hold it (GB10-class shared memory) never plans it
     gb10 = props(num_sms=48, smem=224 * 1024, optin=99 * 1024, pair=(113536, 0), small=(85000, 1),
                  short=(220 * 1024, 0))

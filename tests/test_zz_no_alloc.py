@@ -39,10 +39,11 @@ def test_static_matches_the_oracle_on_two_calls_in_a_row():
     # rows split over clusters (long_coop, mtp), whole rows (decode_batch), and rows
     # split eight ways whose all-equal values overflow the cluster leader, so the
     # members merge through the row-group areas of the fixed array
-    tied = np.ones((4, 131072), np.float32)
+    S = 1 << 20  # rows this long are split across CTAs
+    tied = np.ones((4, S), np.float32)
     tied[1, ::3] = 2.0
-    tied_lens = np.array([131072, 131072, 100000, 70001], np.int32)
-    pl = _plan(rn, 4, 131072, 1, 2048)
+    tied_lens = np.array([S, S, 700000, 300001], np.int32)
+    pl = _plan(rn, 4, S, 1, 2048)
     assert pl.ctas_per_group == 8 and pl.cluster, "the tied case is planned as clusters of eight"
     cases = [(w.name, w.logits, w.lengths, w.topk, w.next_n)
              for w in (workloads.make("long_coop", 3), workloads.make("decode_batch", 10), workloads.make("mtp", 4))]
