@@ -239,7 +239,12 @@ int topk_ragged_strided(const float* logits, int64_t row_stride, int64_t col_str
 int topk_gather_sort(const float* logits, int64_t row_stride, int64_t col_stride, int64_t max_len,
                      int64_t num_rows, int topk, int32_t* out_idx, float* out_val, int sort, void* stream);
 
-/* topk_ragged with options (NULL options = topk_ragged). */
+/*
+ * topk_ragged with options (NULL options = topk_ragged). The pages have no
+ * counterpart: this is the library's own entry for tests and tuning (forced
+ * splits, merge kind, CTA shape, time-out, injected failures); the selection
+ * it computes is the one topk_ragged computes.
+ */
 int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengths,
                    int64_t num_rows, int next_n, int topk, int32_t* out_idx,
                    void* workspace, void* stream, const topk_options* options);
@@ -247,11 +252,14 @@ int topk_ragged_ex(const float* logits, int64_t row_stride, const int32_t* lengt
 /*
  * Synchronises `stream` and copies the workspace's sticky status word
  * (TOPK_DEV_* bits) to *device_status. For tests and debugging, not for the
- * hot path. Returns TOPK_OK, or TOPK_ERR_CUDA if the copy failed.
+ * hot path. Returns TOPK_OK, or TOPK_ERR_CUDA if the copy failed. The library's
+ * own: the pages' launcher reports errors by exceptions on the host and has no
+ * device-side status. The word is a bit set, hence unsigned (uint32_t*).
  */
 int topk_get_status(const void* workspace, void* stream, uint32_t* device_status);
 
-/* Static description of a topk_status code (never NULL). */
+/* Static description of a topk_status code (never NULL). The library's own (the
+ * pages report errors as exception messages); no passage corresponds. */
 const char* topk_status_string(int code);
 
 /*

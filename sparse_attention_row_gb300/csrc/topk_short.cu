@@ -56,11 +56,15 @@ constexpr int kCand = kWarps * kRegion;
 constexpr int kFine = 17;                           // fine bins: the top 15 key bits (key >> 17)
 constexpr int kTrack = 64;                          // fine bins counted during the filter, from the seed bin's edge
 constexpr int kRank = 512;                          // entries of the K-th key's fine bin ranked directly
+constexpr int kTaskSurvivors = 128;                 // expected survivors a filter task may take
+constexpr int kMinTasks = 8;                        // filter tasks a window is split into at least
+constexpr int kRefineExcess = 256;                  // a resident row refines its seed bin only when that
+                                                    // keeps more than this many extra survivors out
 static_assert(kRing <= 32, "slot phases fit one 32-bit mask");
 static_assert(((kRing * kPiece) & (kRing * kPiece - 1)) == 0, "ring indices wrap with a mask");
 constexpr int kWrap = kRing * kPiece - 1;
 static_assert(kWarps == 32, "one lane of warp 0 per warp when offsets are scanned");
-static_assert(kPiece % kTask == 0 && kTask == 4 * 4 * 32, "a task is 4 float4 per lane, inside one piece");
+static_assert(kPiece % (2 * kTask) == 0 && kTask == 4 * 4 * 32, "tasks of up to 8 float4 per lane tile a piece");
 
 struct __align__(128) Smem {
   float row[kRing * kPiece];      // the ring: slot q holds pieces q, q + kRing, ... of the window
@@ -73,7 +77,8 @@ struct __align__(128) Smem {
   alignas(16) int32_t ri[kRank];
   alignas(16) int wbin[kWarps][kTrack + 4];  // per warp: candidates in fine bin f0 + j (f0: the seed bin's
                                              // edge); rows padded by 16 bytes so a lane per row reads no bank twice
-  int woff[kWarps][2];            // per warp: output offset, ranking-slot offset
+  alignas(16) int ftot[kTrack];   // fine-bin counts summed over the warps
+  int n_win, n_bt;                // winners above bin t written, bin t's entries held (emission)
   int wcnt[kWarps];               // survivors per warp (may exceed kRegion: overflow)
   int tcnt[kWarps];               // fallback: ties per warp before the scan
   unsigned long long bar[kRing];
@@ -85,6 +90,7 @@ struct __align__(128) Smem {
   int n_out;
   uint32_t key_max;
   int t0, t, need, in_t, sel_ok;  // seed bin, the K-th key's fine bin, its entries taken and held, fast path ok
+  int target;                     // the sample's best that the seed threshold keeps
   int crowded;                    // the seed bin of a streamed row is crowded (heavy ties)
   int refine, need_in;            // the seed bin is wide: refine the threshold inside it, to `need_in` of its entries
   uint32_t thr_key;               // the filter keeps keys >= thr_key
@@ -293,14 +299,12 @@ __device__ __forceinline__ void issue_pieces(Smem& s, const Win& w, int i0, int 
 
 // Parity flips of the slots over the ring positions [s0, s0 + span) of one row.
 __device__ __forceinline__ uint32_t slot_flips(int s0, int span) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int q = 0; q < kRing; ++q) {
-    const int d = (q - s0 + kRing) % kRing;  // the row's first position in slot q
-    const int uses = (d < span) ? (span - 1 - d) / kRing + 1 : 0;
-    m |= static_cast<uint32_t>(uses & 1) << q;
-  }
-  return m;
+  // positions s0 .. s0 + span - 1 round the ring: every slot takes span / kRing
+  // of them, and the span % kRing slots from s0 on one more
+  constexpr uint32_t kAll = (1u << kRing) - 1u;
+  const uint32_t extra = (1u << (span % kRing)) - 1u;
+  const uint32_t m = ((span / kRing) & 1) ? kAll : 0u;
+  return m ^ (((extra << s0) | (extra >> (kRing - s0))) & kAll);
 }
 
 // Element e of a row: in the ring, at (off + e) & wrap; else x[e * xs].
@@ -535,6 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   // ring's worth) before anything else; the first length is loaded now, used
   // once the data is in.
   const int32_t len_raw0 = __ldg(p.lengths + r);
+  // thread 0 holds the raw length of the next row, loaded a row ahead of its use
+  int32_t nl_raw = (tid == 0 && r + gridDim.x < p.num_rows) ? __ldg(p.lengths + r + gridDim.x) : 0;
   int blind = 0;  // pieces of the first row in flight before its length is known
   if (bulk) blind = min(make_win(p, r, static_cast<int>(p.max_len)).np, kRing);  // the same in every thread
   if (warp == 0) {
@@ -553,6 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
   for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
   if (tid < 256) s.hsub[tid] = 0;
+  if (tid < kTrack) s.ftot[tid] = 0;
+  if (tid == 0) {
+    s.n_win = 0;
+    s.n_bt = 0;
+  }
   __syncthreads();
   int len = clamp_len(p, len_raw0, tid == 0);
 
@@ -562,7 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
 #pragma unroll 1
   for (int64_t k = 0; r < p.num_rows; ++k) {
     const int64_t rn = r + gridDim.x;
-    if (tid == 0) s.len_next = (rn < p.num_rows) ? clamp_len(p, __ldg(p.lengths + rn), true) : 0;
+    if (tid == 0) {
+      s.len_next = (rn < p.num_rows) ? clamp_len(p, nl_raw, true) : 0;
+      const int64_t rnn = rn + gridDim.x;
+      nl_raw = (rnn < p.num_rows) ? __ldg(p.lengths + rnn) : 0;
+    }
     const Win w = make_win(p, r, len);
     int32_t* o = p.out + r * static_cast<int64_t>(K);
     const int dead = (k == 0) ? blind : 0;     // the first row's blind pieces (those past its window are dead)
@@ -588,7 +603,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
         for (int e = tid; e < len; e += kThreads) s.row[e] = __ldg(w.rowp + static_cast<int64_t>(e) * cs);
         __syncthreads();
       }
-      // ---- seed: the top 12 key bits of piece 0 (slot S) and its largest key
+      // ---- seed: the top 12 key bits of piece 0 (slot S) and its largest key. Warp 0
+      // first works out how many of the sample's best the threshold should keep
+      // (it needs no data)
+      const int n_seed = min(len, kSeed - w.mis);
+      int target = K;
+      if (warp == 0 && n_seed < len) {
+        // mu = the expected count of the row's K best in the sample; aim three
+        // standard deviations above it (mu is small on long rows), so a sample
+        // that runs short of it still leaves K survivors
+        const float mu = static_cast<float>(K) * static_cast<float>(n_seed) / static_cast<float>(len);
+        target = max(1, static_cast<int>(ceilf(mu + 3.0f * sqrtf(mu) + 2.0f)));
+      }
+      target = min(target, n_seed);
       bool ok = !bulk || piece_ready(s, S, (par >> S) & 1u, p.timeout_ns);
       const int seed_hi = min(kSeed, w.nwin);
       const float* seed = s.row + S * kPiece;  // a piece never wraps round the ring
@@ -614,16 +641,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           if (warp == 0) issue_pieces(s, wn, 0, min(np_next, kRing - span), S_next, true);
         }
         if (warp == 0) {
-          const int n_seed = min(len, kSeed - w.mis);
-          int target = K;
-          if (n_seed < len) {
-            // mu = the expected count of the row's K best in the sample; aim three
-            // standard deviations above it (mu is small on long rows), so a sample
-            // that runs short of it still leaves K survivors
-            const float mu = static_cast<float>(K) * static_cast<float>(n_seed) / static_cast<float>(len);
-            target = max(1, static_cast<int>(ceilf(mu + 3.0f * sqrtf(mu) + 2.0f)));
-          }
-          target = min(target, n_seed);
           int t0, above0;
           warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
           const int c0 = static_cast<int>(s.hseed[t0]);
@@ -636,8 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
                                static_cast<int64_t>(at_or_above) * len > (3ll * kCand / 4) * n_seed;
           // a wide seed bin (its sample count well beyond what the target needs from
           // it) is split on the next 8 key bits, so the threshold lands close to it
-          const bool refine = !crowded && c0 - need_in > max(target / 4, 16);
+          const bool refine = !crowded && c0 - need_in > max(target / 4, 16) &&
+                              (stream || static_cast<int64_t>(c0 - need_in) * len > static_cast<int64_t>(kRefineExcess) * n_seed);
           if (lane == 0) {
+            s.target = target;
             s.t0 = t0;
             s.crowded = crowded ? 1 : 0;
             s.refine = refine ? 1 : 0;
@@ -662,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           }
           __syncthreads();
         }
-        // ---- filter: warp tasks of 128 F window elements; lane l of a task takes
+        // ---- filter: warp tasks of 128 F window elements (F = 1, 2, 4 or 8); lane l of a task takes
         // float4s l, l + 32, ... of it. Piece j sits in slot j % kRing; on a
         // streamed row the last of its tasks hands the slot to piece j + kRing.
         uint32_t thr_key = s.thr_key;  // the filter keeps keys >= thr_key
@@ -675,7 +694,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           // its elements equal to T in index order. Every later element of the
           // row has a larger index than all of them, so one equal to T can never
           // be selected: the filter keeps key > T only (exact for any data).
-          const int n_seed = min(len, kSeed - w.mis);
           int need_t;
           const uint32_t T = exact_kth(s, seed, 1, w.mis, 0, n_seed, K, need_t);
           thr_key = T;  // the fine bins count from T's (the ties are candidates)
@@ -713,9 +731,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
         }
         const int f0 = static_cast<int>(thr_key >> kFine);  // every candidate's fine bin is at least f0
         const int nvec = w.nwin >> 2;
-        // float4s per lane in a task: short windows take smaller tasks, so that every
-        // warp gets some and no warp's region has to hold a large share of survivors
-        const int F = (w.nwin > 16 * kTask) ? 4 : (w.nwin > 8 * kTask) ? 2 : 1;
+        // float4s per lane in a task: the most (up to 8, which spreads the per-task
+        // work over the most elements) that keep a task's expected survivors (the
+        // seed's share of the row) within kTaskSurvivors, and the window in at least
+        // kMinTasks tasks
+        int F = 8;
+        while (F > 1 && (static_cast<int64_t>(128 * F) * s.target > static_cast<int64_t>(kTaskSurvivors) * n_seed ||
+                         w.nwin < kMinTasks * 128 * F))
+          F >>= 1;
         const int tsz = 128 * F;  // window elements per task
         const int ntask = (w.nwin + tsz - 1) / tsz;
 #pragma unroll 1
@@ -729,29 +752,39 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           const int sb = q * kPiece + (task * tsz) % kPiece;  // the task's first element in the ring
           const int v0 = task * (tsz / 4);                    // and its first float4 in the window
           uint32_t m = 0;
+          if (v0 + 32 * F <= nvec && 4 * v0 - w.mis >= 0 && 4 * v0 + tsz - w.mis <= len) {
+            // a task inside the row: no element needs a bounds check
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int v = v0 + lane + 32 * i;
-            if (i < F && v < nvec) {
-              const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
-              uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
-                           (f.w >= thr ? 8u : 0u);
-              const int e0 = 4 * v - w.mis;
-              if (e0 < 0 || e0 + 3 >= len) {
+            for (int i = 0; i < 8; ++i) {
+              if (i < F) {
+                const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
+                m |= ((f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                      (f.w >= thr ? 8u : 0u)) << (4 * i);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int v = v0 + lane + 32 * i;
+              if (i < F && v < nvec) {
+                const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
+                uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                             (f.w >= thr ? 8u : 0u);
+                const int e0 = 4 * v - w.mis;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                   if (e0 + c < 0 || e0 + c >= len) b &= ~(1u << c);
+                m |= b << (4 * i);
               }
-              m |= b << (4 * i);
             }
           }
-          const int c = __popc(m);
-          uint32_t qb[5];
+          const int c = __popc(m);  // at most 32
+          uint32_t qb[6];
 #pragma unroll
-          for (int bit = 0; bit < 5; ++bit) qb[bit] = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+          for (int bit = 0; bit < 6; ++bit) qb[bit] = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
           int tot = 0, pre = 0;
 #pragma unroll
-          for (int bit = 0; bit < 5; ++bit) {
+          for (int bit = 0; bit < 6; ++bit) {
             tot += __popc(qb[bit]) << bit;
             pre += __popc(qb[bit] & lt) << bit;
           }
@@ -801,20 +834,21 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           }
         }
         if (lane == 0) s.wcnt[warp] = wc;
+        if (wc > 0) {
+          // this warp's fine-bin counts into the totals over the warps
+          const int2 v2 = *reinterpret_cast<const int2*>(&my_bins[2 * lane]);
+          if (v2.x) atomicAdd(&s.ftot[2 * lane], v2.x);
+          if (v2.y) atomicAdd(&s.ftot[2 * lane + 1], v2.y);
+        }
         if (sync_or(!ok)) {
           aborted = true;
         } else {
-          // ---- the K-th key's fine bin t, and every warp's offsets (warp 0; lane l
-          // speaks for warp l, and sums fine bins 2l and 2l + 1 over the warps)
+          // ---- the K-th key's fine bin t (warp 0; lane l reads warp l's survivor
+          // count and the totals of fine bins 2l and 2l + 1)
           if (warp == 0) {
             const int n_l = s.wcnt[lane];
-            int c0 = 0, c1 = 0;
-#pragma unroll 8
-            for (int q = 0; q < kWarps; ++q) {
-              const int2 v2 = *reinterpret_cast<const int2*>(&s.wbin[q][2 * lane]);
-              c0 += v2.x;
-              c1 += v2.y;
-            }
+            const int2 c2 = *reinterpret_cast<const int2*>(&s.ftot[2 * lane]);
+            const int c0 = c2.x, c1 = c2.y;
             const bool over = __any_sync(0xFFFFFFFFu, n_l > kRegion);
             const int n_c = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(n_l)));
             const int skip = n_c - K;  // the K-th key's bin: the first whose prefix (from f0) passes skip
@@ -835,26 +869,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
             const int need = K - (n_c - cum);
             const bool all_t = need == in_t;
             const bool sel_ok = !over && n_c >= K && hit != 0 && (all_t || in_t <= kRank);
-            // this warp's (lane l's) candidates above bin t, and in it
-            int below_l = 0;
-#pragma unroll 4
-            for (int j4 = 0; j4 < kTrack; j4 += 4) {
-              const int4 v4 = *reinterpret_cast<const int4*>(&s.wbin[lane][j4]);
-              below_l += (j4 <= jt ? v4.x : 0) + (j4 + 1 <= jt ? v4.y : 0) + (j4 + 2 <= jt ? v4.z : 0) +
-                         (j4 + 3 <= jt ? v4.w : 0);
-            }
-            int bt_l = s.wbin[lane][jt];
-            int win_l = n_l - below_l;
-            if (all_t) {
-              win_l += bt_l;
-              bt_l = 0;
-            }
-            const int packed = warp_excl(sel_ok ? (win_l | (bt_l << 16)) : 0);  // both below 2^16
-            s.woff[lane][0] = packed & 0xFFFF;
-            s.woff[lane][1] = packed >> 16;
             if (lane == 0) {
               s.sel_ok = sel_ok ? 1 : 0;
-              s.t = f0 + jt;
+              s.t = jt;  // relative to f0
               s.need = all_t ? 0 : need;  // 0: bin t is taken whole
               s.in_t = in_t;
             }
@@ -863,12 +880,30 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           bool done = false;
           if (s.sel_ok) {
             // ---- winners above bin t out; bin t's entries into the ranking slots
-            const int t = s.t;
+            const int jt = s.t;
+            const int t = f0 + jt;
             const int need = s.need;
             const bool all_t = need == 0;
-            int ow = s.woff[warp][0];
-            int os = s.woff[warp][1];
-            const int cnt = min(s.wcnt[warp], kRegion);
+            const int cnt = s.wcnt[warp];  // at most kRegion here
+            // this warp's candidates above bin t and in it, from its own fine bins;
+            // its output range and ranking slots come from two shared counters (the
+            // order of a row's indices is free)
+            const int2 b2 = *reinterpret_cast<const int2*>(&my_bins[2 * lane]);
+            const int below = static_cast<int>(__reduce_add_sync(
+                0xFFFFFFFFu, static_cast<uint32_t>((2 * lane <= jt ? b2.x : 0) + (2 * lane + 1 <= jt ? b2.y : 0))));
+            int bt = my_bins[jt];
+            int nw = cnt - below;
+            if (all_t) {
+              nw += bt;
+              bt = 0;
+            }
+            int ow = 0, os = 0;
+            if (lane == 0) {
+              if (nw) ow = atomicAdd(&s.n_win, nw);
+              if (bt) os = atomicAdd(&s.n_bt, bt);
+            }
+            ow = __shfl_sync(0xFFFFFFFFu, ow, 0);
+            os = __shfl_sync(0xFFFFFFFFu, os, 0);
 #pragma unroll 1
             for (int e0 = 0; e0 < cnt; e0 += 32) {
               const int e = e0 + lane;
@@ -901,11 +936,19 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
                 s.ri[tid] = 0x7FFFFFFF;
               }
               __syncthreads();
-              if (tid < in_t) {
-                const uint32_t kj = s.rk[tid];
-                const int32_t ij = s.ri[tid];
+              // each entry's rank, by a group of 2^lg lanes (the most that fit the
+              // block, at most a warp): lane `sub` of the group compares the entry
+              // with entries 4 sub .. 4 sub + 3, then every 4 * 2^lg-th group on
+              int lg = 5;
+              while ((in_t << lg) > kThreads) --lg;
+              const int e = tid >> lg;
+              const int sub = tid & ((1 << lg) - 1);
+              if (((warp << 5) >> lg) < in_t) {  // the warp holds an entry's group (groups never straddle warps)
+                const bool act = e < in_t;
+                const uint32_t kj = act ? s.rk[e] : 0u;
+                const int32_t ij = act ? s.ri[e] : 0;
                 int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-                for (int i0 = 0; i0 < in_t; i0 += 4) {
+                for (int i0 = 4 * sub; i0 < c4; i0 += 4 << lg) {
                   const uint4 k4 = *reinterpret_cast<const uint4*>(&s.rk[i0]);
                   const int4 x4 = *reinterpret_cast<const int4*>(&s.ri[i0]);
                   r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
@@ -913,8 +956,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
                   r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
                   r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
                 }
-                const int rank = r0 + r1 + r2 + r3;
-                if (rank < need) o[K - need + rank] = ij;
+                int rank = r0 + r1 + r2 + r3;
+                for (int o2 = 1; o2 < (1 << lg); o2 <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o2);
+                if (act && sub == 0 && rank < need) o[K - need + rank] = ij;
               }
             }
             done = true;
@@ -932,12 +976,25 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
     }
     // the row's end: clear the seed histogram, learn the next length, issue its window
     if (aborted) break;
+    if (rn >= p.num_rows) {
+      // the CTA's last row: nothing to clear; only the first row's dead blind
+      // pieces may still be landing (lane q waits for slot q)
+      if (warp == 0 && lane < kRing && lane >= w.np && lane < dead)
+        wait_piece(&s.bar[lane], (par >> lane) & 1u, p.timeout_ns, &s.abort);
+      break;
+    }
     __syncthreads();
     // read here, between two barriers: thread 0 writes the one after it at the next row's start
     const int len_next = s.len_next;
-    for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
-    for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
+    static_assert(kBins == 4 * kThreads, "one 16-byte store per thread clears the seed histogram");
+    reinterpret_cast<uint4*>(s.hseed)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<int2*>(&s.wbin[warp][2 * lane]) = make_int2(0, 0);
     if (tid < 256) s.hsub[tid] = 0;
+    if (tid < kTrack) s.ftot[tid] = 0;
+    if (tid == 0) {
+      s.n_win = 0;
+      s.n_bt = 0;
+    }
     if (warp == 0) {
       // the first row's blind pieces past its window may still be landing:
       // wait for them before the ring takes the next window (lane q, slot q;
