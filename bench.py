@@ -419,6 +419,73 @@ def run_only(args) -> None:
                       "frac_of_hbm_peak": gbs / peak, "steps": args.steps}), flush=True)
 
 
+SWEEP_LENGTHS = (4096, 8192, 16384, 32768, 65536, 131072, 262144)
+SWEEP_ROWS = (1, 4, 16, 64, 152, 608, 4096)
+
+
+def run_sweep(args) -> None:
+    """Times every launch shape over row length x row count (all rows full length,
+    N(0,1) logits from torch's CUDA generator seeded 0) and prints a markdown table:
+    the planner's choice beside each shape's time, L2 flushed before every call."""
+    gb = GpuBench(0)
+    t, sar = gb.torch, gb.sar
+    props = sar.topk_query_device(0)
+    K = args.sweep_topk
+    gen = t.Generator(device=gb.dev)
+    arms = [("short", dict(shape=4)), ("paired", dict(shape=2)), ("wide", dict(shape=1, force_ctas_per_group=1))]
+    arms += [(f"split{g}", dict(shape=1, force_ctas_per_group=g, merge=2)) for g in (2, 4, 8)]
+    print(f"| row length | rows | planner | {' | '.join(a for a, _ in arms)} | best |")
+    print("|---:|---:|---|" + "---:|" * (len(arms) + 1))
+    stream = t.cuda.current_stream()
+    for L in SWEEP_LENGTHS:
+        for R in SWEEP_ROWS:
+            if R * L * 4 > (5 << 30):
+                continue
+            gen.manual_seed(0)
+            x = t.randn((R, L), generator=gen, device=gb.dev, dtype=t.float32)
+            ln = t.full((R,), L, dtype=t.int32, device=gb.dev)
+            out = t.empty((R, K), dtype=t.int32, device=gb.dev)
+            rc, pl = sar.topk_make_plan(props, R, L, 1, K)
+            planner = f"{ {1: 'wide', 2: 'paired', 3: 'small', 4: 'short'}.get(pl.shape, '?')}" + (
+                f" x{pl.ctas_per_group}" if pl.ctas_per_group > 1 else "")
+            times = []
+            for _, kw in arms:
+                o = sar.TopkOptions()
+                for k, v in kw.items():
+                    setattr(o, k, v)
+                rc, plo = sar.topk_make_plan(props, R, L, 1, K, o)
+                if rc != 0 or (kw.get("force_ctas_per_group", 1) > 1 and (R >= props.num_sms or
+                                                                         plo.ctas_per_group != kw["force_ctas_per_group"])):
+                    times.append(None)
+                    continue
+                fn = lambda: sar.topk_ragged_ex(x, L, ln, R, 1, K, out, gb.sel.workspace, gb.stream_handle, o)
+                ok = True
+                for _ in range(3):
+                    gb.flush_l2()
+                    ok = ok and fn() == 0
+                if not ok:
+                    times.append(None)
+                    continue
+                st = [t.cuda.Event(enable_timing=True) for _ in range(args.sweep_steps)]
+                en = [t.cuda.Event(enable_timing=True) for _ in range(args.sweep_steps)]
+                t.cuda.synchronize()
+                t.cuda._sleep(5_000_000)
+                for i in range(args.sweep_steps):
+                    gb.flush_l2()
+                    st[i].record(stream)
+                    fn()
+                    en[i].record(stream)
+                t.cuda.synchronize()
+                rc2, word = sar.topk_get_status(gb.sel.workspace)
+                if rc2 != 0 or word != 0:
+                    raise RuntimeError(f"device status {word:#x} at rows {R}, length {L}")
+                times.append(float(np.median([a.elapsed_time(b) * 1e3 for a, b in zip(st, en)])))
+            best = min((v, a) for (a, _), v in zip(arms, times) if v is not None)[1]
+            cells = " | ".join("-" if v is None else f"{v:.1f}" for v in times)
+            print(f"| {L} | {R} | {planner} | {cells} | {best} |", flush=True)
+            del x, ln, out
+
+
 def run_dry(args) -> None:
     """The multi-rank launch and aggregation with zero-work steps (no GPU needed)."""
     rank, world, local = dist_env()
@@ -551,6 +618,9 @@ def main(argv=None) -> None:
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timings")
     ap.add_argument("--only", default="", help="time only this workload's kernel (profiling runs)")
     ap.add_argument("--dry-run", action="store_true", help="launch and aggregate with zero-work steps, no GPU")
+    ap.add_argument("--sweep", action="store_true", help="time every launch shape over row length x rows")
+    ap.add_argument("--sweep-topk", type=int, default=2048)
+    ap.add_argument("--sweep-steps", type=int, default=10)
     raw = list(sys.argv[1:] if argv is None else argv)
     args = ap.parse_args(raw)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
@@ -562,6 +632,8 @@ def main(argv=None) -> None:
         run_reference(args)
     elif args.only:
         run_only(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -55,7 +55,9 @@ constexpr int kRegion = 256;                        // candidate slots per warp
 constexpr int kCand = kWarps * kRegion;
 constexpr int kFine = 17;                           // fine bins: the top 15 key bits (key >> 17)
 constexpr int kTrack = 64;                          // fine bins counted during the filter, from the seed bin's edge
-constexpr int kRank = 512;                          // entries of the K-th key's fine bin ranked directly
+constexpr int kRank = 512;                          // entries of the K-th key's fine bin at most (fast path)
+constexpr int kRankDirect = 192;                    // up to this many are ranked at once; more are first
+                                                    // split on 8 more key bits
 constexpr int kTaskSurvivors = 128;                 // expected survivors a filter task may take
 constexpr int kMinTasks = 8;                        // filter tasks a window is split into at least
 constexpr int kRefineExcess = 256;                  // a resident row refines its seed bin only when that
@@ -80,7 +82,7 @@ struct __align__(128) Smem {
   alignas(16) int ftot[kTrack];   // fine-bin counts summed over the warps
   int n_win, n_bt;                // winners above bin t written, bin t's entries held (emission)
   int wcnt[kWarps];               // survivors per warp (may exceed kRegion: overflow)
-  int tcnt[kWarps];               // fallback: ties per warp before the scan
+  int tcnt[2][kWarps];            // tie counts per warp (block scans; two buffers, one barrier each)
   unsigned long long bar[kRing];
   int pdone[kRing];               // warps done with the piece in a slot (streaming rows)
   int slot_issues[kRing];         // copies issued into each slot since the launch began
@@ -91,6 +93,7 @@ struct __align__(128) Smem {
   uint32_t key_max;
   int t0, t, need, in_t, sel_ok;  // seed bin, the K-th key's fine bin, its entries taken and held, fast path ok
   int target;                     // the sample's best that the seed threshold keeps
+  int sub_b, sub_above;           // a large K-th fine bin: the sub-bin holding the K-th, the count above it
   int crowded;                    // the seed bin of a streamed row is crowded (heavy ties)
   int refine, need_in;            // the seed bin is wide: refine the threshold inside it, to `need_in` of its entries
   uint32_t thr_key;               // the filter keeps keys >= thr_key
@@ -307,27 +310,48 @@ __device__ __forceinline__ uint32_t slot_flips(int s0, int span) {
   return m ^ (((extra << s0) | (extra >> (kRing - s0))) & kAll);
 }
 
-// Element e of a row: in the ring, at (off + e) & wrap; else x[e * xs].
-__device__ __forceinline__ float xload(const float* x, int64_t xs, int off, int wrap, int e) {
-  return wrap ? x[(off + e) & wrap] : x[static_cast<int64_t>(e) * xs];
+// A row's window as 16-byte groups: group v holds window elements 4v .. 4v + 3
+// (window element i is row element i - mis). The window sits in the ring (from
+// float4 `ring0` on, wrapping round it), or in global memory: contiguous float4s
+// from a 16-byte aligned base, or a row with a column stride (mis = 0; elements
+// at or past the length are not read).
+struct Src {
+  const float* g;  // global memory: the window's base, or the strided row
+  int64_t cs;      // global memory: the column stride (1: float4 loads)
+  int ring0;       // the window's first float4 in the ring; -1: global memory
+  int len;         // the row's length
+};
+
+__device__ __forceinline__ float4 load_group(const Smem& s, const Src& src, int v) {
+  if (src.ring0 >= 0) return reinterpret_cast<const float4*>(s.row)[(src.ring0 + v) & (kWrap >> 2)];
+  if (src.cs == 1) return __ldg(reinterpret_cast<const float4*>(src.g) + v);
+  float f[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * v + j;
+    f[j] = (e < src.len) ? __ldg(src.g + static_cast<int64_t>(e) * src.cs) : 0.0f;
+  }
+  return make_float4(f[0], f[1], f[2], f[3]);
 }
 
 // ---------------------------------------------------------------- fallback
 
-// The K-th key of x[0, n) (stride xs), exactly, whatever the data: three radix
-// levels over the full key (12, 12 and 8 bits). Returns the key T; `need` is
-// how many of the keys equal to T are among the K best (the first ones in
-// index order). Each thread owns a contiguous segment of x; histograms count
-// runs of equal digits within a segment with one atomic, so tie-heavy rows cost
-// few atomics. Uses s.hseed. Block-wide; every thread gets the answer.
-__device__ __noinline__ uint32_t exact_kth(Smem& s, const float* x, int64_t xs, int off, int wrap, int n, int K,
-                                          int& need) {
+// The K-th key of the window elements [lo, lo + n), exactly, whatever the
+// data: three radix levels over the full key (12, 12 and 8 bits). Returns the
+// key T; `need` is how many of the keys equal to T are among the K best (the
+// first ones in index order) and `equal` how many keys equal T. Thread t reads
+// groups t, t + kThreads, ... (coalesced in global memory, free of bank
+// conflicts in the ring); a thread counts each run of equal digits with one
+// atomic, so tie-heavy rows cost few atomics. Uses s.hseed and clears s.n_out.
+// Block-wide; every thread gets the answer.
+__device__ __noinline__ uint32_t exact_kth(Smem& s, const Src src, int lo, int n, int K, int& need,
+                                          int& equal) {
   const int tid = threadIdx.x;
-  const int seg = (((n + kThreads - 1) / kThreads) + 3) & ~3;
-  const int e_lo = min(tid * seg, n);
-  const int e_hi = min(e_lo + seg, n);
+  const int hi = lo + n;
+  const int nv = (hi + 3) >> 2;
   uint32_t prefix = 0;
   need = K;
+  if (tid == 0) s.n_out = 0;
   // levels: bits 31..20, 19..8 (within prefix), 7..0 (within prefix)
 #pragma unroll 1
   for (int lv = 0; lv < 3; ++lv) {
@@ -337,16 +361,23 @@ __device__ __noinline__ uint32_t exact_kth(Smem& s, const float* x, int64_t xs, 
     for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
     __syncthreads();
     uint32_t cur = 0xFFFFFFFFu, run = 0;
-    for (int e = e_lo; e < e_hi; ++e) {
-      const uint32_t k = fkey(xload(x, xs, off, wrap, e));
-      if (pshift < 32 && (k >> pshift) != prefix) continue;
-      const uint32_t d = (k >> shift) & mask;
-      if (d != cur) {
-        if (run) atomicAdd(&s.hseed[cur], run);
-        cur = d;
-        run = 0;
+#pragma unroll 4
+    for (int v = tid; v < nv; v += kThreads) {
+      const float4 f = load_group(s, src, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = 4 * v + j;
+        if (i < lo || i >= hi) continue;
+        const uint32_t k = fkey(pick(f, j));
+        if (pshift < 32 && (k >> pshift) != prefix) continue;
+        const uint32_t d = (k >> shift) & mask;
+        if (d != cur) {
+          if (run) atomicAdd(&s.hseed[cur], run);
+          cur = d;
+          run = 0;
+        }
+        ++run;
       }
-      ++run;
     }
     if (run) atomicAdd(&s.hseed[cur], run);
     __syncthreads();
@@ -354,56 +385,76 @@ __device__ __noinline__ uint32_t exact_kth(Smem& s, const float* x, int64_t xs, 
     need -= s.fgt;
     prefix = (prefix << (lv == 2 ? 8 : 12)) | static_cast<uint32_t>(s.fb);
   }
+  equal = static_cast<int>(s.hseed[s.fb]);  // the last level's bin holds exactly the keys equal to T
   return prefix;
 }
 
 // Exact selection over a whole row, whatever the data (the fallback of the
-// fast path): the K-th key T from exact_kth, then the keys above T are written
-// out, and the ties in index order (each thread owns a contiguous segment of
-// the row; a block-wide scan of the segments' tie counts ranks them).
-// Rewrites the whole output row. x is the resident window or the row in
-// global memory.
-__device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r, const Win& w, const float* x,
-                                             int64_t xs, int off, int wrap) {
+// fast path, and the path of strided rows longer than the ring): the K-th key
+// T from exact_kth, then one pass writes the keys above T and the keys equal
+// to T, the first `need` of them in index order when not all are taken (a
+// block-wide scan ranks the ties of every kThreads groups). Rewrites the whole
+// output row.
+__device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r, const Win& w, const Src src) {
   const int tid = threadIdx.x;
   const int lane = static_cast<int>(lane_id());
   const int warp = tid >> 5;
   const int K = p.topk;
-  const int seg = (((w.len + kThreads - 1) / kThreads) + 3) & ~3;
-  const int e_lo = min(tid * seg, w.len);
-  const int e_hi = min(e_lo + seg, w.len);
-  int need;
-  const uint32_t T = exact_kth(s, x, xs, off, wrap, w.len, K, need);  // `need` of the keys equal to T are taken
-  // ties per thread segment, then an exclusive scan over the threads in order
-  int ties = 0;
-  for (int e = e_lo; e < e_hi; ++e) ties += (fkey(xload(x, xs, off, wrap, e)) == T) ? 1 : 0;
-  int incl = ties;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s.tcnt[warp] = incl;
-  if (tid == 0) s.n_out = 0;
-  __syncthreads();
-  int before = incl - ties;
-  for (int q = 0; q < warp; ++q) before += s.tcnt[q];
+  int need, equal;
+  const uint32_t T = exact_kth(s, src, w.mis, w.len, K, need, equal);
+  const bool ranked = equal > need;  // keys equal to T are left out: take the first ones
   int32_t* o = p.out + r * static_cast<int64_t>(K);
-  // keys above T, and the first `need` ties in index order: one reservation
-  // per warp and step (every warp takes seg steps)
-  for (int j = 0; j < seg; ++j) {
-    const int e = e_lo + j;
-    bool sel = false;
-    if (e < e_hi) {
-      const uint32_t k = fkey(xload(x, xs, off, wrap, e));
-      if (k > T) {
-        sel = true;
-      } else if (k == T) {
-        sel = before < need;  // the tie's rank in index order
-        ++before;
+  const int lo = w.mis, hi = w.mis + w.len;
+  const int nv = (hi + 3) >> 2;
+  int before = 0;  // keys equal to T in the groups already passed
+#pragma unroll 1
+  for (int c = 0; c * kThreads < nv; ++c) {
+    const int v = c * kThreads + tid;
+    uint32_t above = 0, tie = 0;  // bit j: window element 4v + j
+    if (v < nv) {
+      const float4 f = load_group(s, src, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = 4 * v + j;
+        if (i >= lo && i < hi) {
+          const uint32_t k = fkey(pick(f, j));
+          above |= (k > T ? 1u : 0u) << j;
+          tie |= (k == T ? 1u : 0u) << j;
+        }
       }
     }
-    warp_emit(o, &s.n_out, K, sel, e);
+    if (ranked) {
+      const int nt = __popc(tie);
+      int incl = nt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += x;
+      }
+      if (lane == 31) s.tcnt[c & 1][warp] = incl;
+      __syncthreads();
+      const int wt = s.tcnt[c & 1][lane];
+      int wincl = wt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int x = __shfl_up_sync(0xFFFFFFFFu, wincl, d);
+        if (lane >= d) wincl += x;
+      }
+      int rank = before + __shfl_sync(0xFFFFFFFFu, wincl - wt, warp) + incl - nt;
+      before += __shfl_sync(0xFFFFFFFFu, wincl, 31);
+      uint32_t keep = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if ((tie >> j) & 1u) {
+          if (rank < need) keep |= 1u << j;
+          ++rank;
+        }
+      }
+      tie = keep;
+    }
+    const uint32_t sel = above | tie;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) warp_emit(o, &s.n_out, K, (sel >> j) & 1u, 4 * v + j - lo);
   }
   __syncthreads();
 }
@@ -437,40 +488,85 @@ __device__ __forceinline__ bool piece_ready(Smem& s, int q, uint32_t parity, uin
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// One warp, every lane with the same answer: scanning h down from bin `top`
-// (counts above it are zero), the bin b where the suffix sum (bins >= b)
-// reaches need; `above` = the count in bins > b. Requires 1 <= need <= total.
+// One warp, every lane with the same answer: over h[0, kBins), with no counts
+// above bin `top`, the bin b where the suffix sum (bins >= b) reaches need;
+// `above` = the count in bins > b. Requires 1 <= need <= total. Up to two
+// steps of 128 bins down from top (lane l: four bins, one 16-byte load); a
+// crossing lower down is found at once (lane l sums 128 bins), then within
+// that lane's stretch, four bins a lane.
 __device__ __forceinline__ void warp_scan_down(const uint32_t* h, int top, int need, int& bin, int& above) {
   const int lane = static_cast<int>(lane_id());
-  uint32_t carry = 0;
-#pragma unroll 1
-  for (int b0 = top; b0 >= 0; b0 -= 32) {
-    const int b = b0 - lane;
-    const uint32_t v = (b >= 0) ? h[b] : 0u;
-    uint32_t incl = v;
+  const uint32_t u_need = static_cast<uint32_t>(need);
+  uint32_t carry = 0;  // the count in bins above the current step
+  // one step over bins hi - 127 .. hi (hi = 4 k + 3): lane l holds hi - 4l - 3 .. hi - 4l
+  auto step4 = [&](int hi) -> bool {
+    const int lo4 = hi - 4 * lane - 3;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (lo4 >= 0) q = *reinterpret_cast<const uint4*>(h + lo4);
+    const uint32_t own = q.x + q.y + q.z + q.w;
+    uint32_t incl = own;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
       if (lane >= o) incl += x;
     }
-    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, carry + incl >= static_cast<uint32_t>(need));
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      const uint32_t il = __shfl_sync(0xFFFFFFFFu, incl, L);
-      const uint32_t vl = __shfl_sync(0xFFFFFFFFu, v, L);
-      bin = b0 - L;
-      above = static_cast<int>(carry + il - vl);
-      return;
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, carry + incl >= u_need);
+    if (hit == 0) {
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      return false;
     }
-    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-  }
+    const int L = __ffs(hit) - 1;
+    uint32_t run = carry + __shfl_sync(0xFFFFFFFFu, incl - own, L);
+    const uint32_t v3 = __shfl_sync(0xFFFFFFFFu, q.w, L), v2 = __shfl_sync(0xFFFFFFFFu, q.z, L);
+    const uint32_t v1 = __shfl_sync(0xFFFFFFFFu, q.y, L);
+    const int base = hi - 4 * L - 3;
+    if (run + v3 >= u_need) {
+      bin = base + 3;
+    } else if (run += v3, run + v2 >= u_need) {
+      bin = base + 2;
+    } else if (run += v2, run + v1 >= u_need) {
+      bin = base + 1;
+    } else {
+      run += v1;
+      bin = base;
+    }
+    above = static_cast<int>(run);
+    return true;
+  };
+  int b0 = top | 3;
+#pragma unroll 1
+  for (int st = 0; st < 2 && b0 >= 0; ++st, b0 -= 128)
+    if (step4(b0)) return;
   bin = 0;
-  above = static_cast<int>(carry);  // unreachable when the total reaches need
+  above = static_cast<int>(carry);
+  if (b0 < 0) return;  // unreachable when the total reaches need
+  // the rest at once: lane l sums bins b0 - 128 l - 127 .. b0 - 128 l
+  uint32_t own = 0;
+#pragma unroll 8
+  for (int k = 0; k < 32; ++k) {
+    const int lo4 = b0 - 128 * lane - 4 * k - 3;
+    if (lo4 >= 0) {
+      const uint4 q = *reinterpret_cast<const uint4*>(h + lo4);
+      own += q.x + q.y + q.z + q.w;
+    }
+  }
+  uint32_t incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, carry + incl >= u_need);
+  if (hit == 0) return;  // unreachable when the total reaches need
+  const int L = __ffs(hit) - 1;
+  carry += __shfl_sync(0xFFFFFFFFu, incl - own, L);
+  step4(b0 - 128 * L);
 }
 
 // One warp, every lane with the same answer: over h[0, 256), the largest bin b
-// whose suffix sum reaches need (1 <= need <= total).
-__device__ __forceinline__ int warp_find256(const uint32_t* h, int need) {
+// whose suffix sum reaches need (1 <= need <= total); `above` = the count in
+// bins > b.
+__device__ __forceinline__ int warp_find256(const uint32_t* h, int need, int& above) {
   const int lane = static_cast<int>(lane_id());
   const uint4 lo4 = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
   const uint4 hi4 = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
@@ -498,7 +594,40 @@ __device__ __forceinline__ int warp_find256(const uint32_t* h, int need) {
     }
     if (!found) run += vk;
   }
+  above = static_cast<int>(run);
   return b;
+}
+
+// Ranks entries [0, n) of (kk, ii) by key descending, then index ascending
+// (entries [n, c4) hold padding that never beats a real entry), and writes the
+// index of every entry of rank < need at out[rank]. Groups of 2^lg lanes (the
+// most that fit the block, at most a warp) share an entry: lane `sub` of a
+// group compares it with entries 4 sub .. 4 sub + 3, then every 4 * 2^lg-th
+// on. Needs n <= kThreads / 2. Block-wide (no barrier).
+__device__ __forceinline__ void rank_out(const uint32_t* kk, const int32_t* ii, int n, int c4, int need,
+                                         int32_t* out) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  int lg = 5;
+  while ((n << lg) > kThreads) --lg;
+  const int e = tid >> lg;
+  const int sub = tid & ((1 << lg) - 1);
+  if (((warp << 5) >> lg) >= n) return;  // no entry's group in this warp (groups never straddle warps)
+  const bool act = e < n;
+  const uint32_t kj = act ? kk[e] : 0u;
+  const int32_t ij = act ? ii[e] : 0;
+  int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+  for (int i0 = 4 * sub; i0 < c4; i0 += 4 << lg) {
+    const uint4 k4 = *reinterpret_cast<const uint4*>(&kk[i0]);
+    const int4 x4 = *reinterpret_cast<const int4*>(&ii[i0]);
+    r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
+    r1 += (k4.y > kj || (k4.y == kj && x4.y < ij)) ? 1 : 0;
+    r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
+    r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
+  }
+  int rank = r0 + r1 + r2 + r3;
+  for (int o2 = 1; o2 < (1 << lg); o2 <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o2);
+  if (act && sub == 0 && rank < need) out[rank] = ij;
 }
 
 // Exclusive prefix over the lanes of a warp.
@@ -520,6 +649,53 @@ __device__ __forceinline__ int atom_add_acq_rel_cta(int* p, int v) {
                : "r"(smem_addr(p)), "r"(v)
                : "memory");
   return old;
+}
+
+// A crowded seed bin on a streamed row (heavy ties): the seed piece's own K
+// best, that is its K-th key T and the first `need` of its elements equal to T
+// in index order, go into the candidate regions (warp w's at most 64 into its
+// own). Every later element of the row has a larger index than all of them,
+// so one equal to T can never be selected: the filter then keeps key > T only,
+// which is exact for any data. Returns T; `wc` = this warp's candidates, also
+// counted in its fine bin 0 (T's). Block-wide.
+__device__ __noinline__ uint32_t crowded_seed(Smem& s, int S, int mis, int n_seed, int len, int K, int& wc) {
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const int warp = tid >> 5;
+  const float* seed = s.row + S * kPiece;
+  int need_t, equal_t;
+  const uint32_t T = exact_kth(s, Src{nullptr, 1, S * (kPiece / 4), len}, mis, n_seed, K, need_t, equal_t);
+  // thread i owns seed elements 2i and 2i + 1; a block scan ranks the ties
+  const int ea = 2 * tid;
+  const bool ta = ea < n_seed && fkey(seed[mis + ea]) == T;
+  const bool tb = ea + 1 < n_seed && fkey(seed[mis + ea + 1]) == T;
+  const int mine = (ta ? 1 : 0) + (tb ? 1 : 0);
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) s.tcnt[0][warp] = incl;
+  __syncthreads();
+  int before = incl - mine;
+  for (int q = 0; q < warp; ++q) before += s.tcnt[0][q];
+  const bool sa = ta && before < need_t;
+  const bool sb = tb && before + (ta ? 1 : 0) < need_t;
+  const int sel = (sa ? 1 : 0) + (sb ? 1 : 0);
+  const int at = warp * kRegion + warp_excl(sel);  // at most 64 per warp: inside its region
+  if (sa) {
+    s.ckey[at] = T;
+    s.cidx[at] = ea;
+  }
+  if (sb) {
+    s.ckey[at + (sa ? 1 : 0)] = T;
+    s.cidx[at + (sa ? 1 : 0)] = ea + 1;
+  }
+  wc = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(sel)));
+  if (lane == 0 && wc) atomicAdd(&s.wbin[warp][0], wc);  // fine bin T >> kFine is f0
+  __syncthreads();
+  return T;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p) {
@@ -595,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
       for (int j = tid; j < K; j += kThreads) o[j] = (j < len) ? j : -1;
     } else if (!bulk && w.nwin > kRing * kPiece) {
       // a strided row longer than the ring: exact selection straight from global memory
-      fallback_select(s, p, r, w, w.rowp, p.col_stride, 0, 0);
+      fallback_select(s, p, r, w, Src{w.rowp, p.col_stride, -1, len});
     } else {
       if (!bulk) {
         // strided rows: every thread loads its elements into the window
@@ -676,10 +852,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           }
           __syncthreads();
           if (warp == 0) {
-            const int b = warp_find256(s.hsub, s.need_in);
+            int above_b;
+            const int b = warp_find256(s.hsub, s.need_in, above_b);
             if (lane == 0) s.thr_key = (t0 << 20) | (static_cast<uint32_t>(b) << 12);
           }
           __syncthreads();
+          if (tid < 256) s.hsub[tid] = 0;  // clear again for the selection (read after later barriers)
         }
         // ---- filter: warp tasks of 128 F window elements (F = 1, 2, 4 or 8); lane l of a task takes
         // float4s l, l + 32, ... of it. Piece j sits in slot j % kRing; on a
@@ -690,44 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
         int wc = 0;
         int* my_bins = s.wbin[warp];  // this warp's own counters: no other warp touches them
         if (s.crowded) {
-          // The seed piece's own K best: its K-th key T, and the first need_t of
-          // its elements equal to T in index order. Every later element of the
-          // row has a larger index than all of them, so one equal to T can never
-          // be selected: the filter keeps key > T only (exact for any data).
-          int need_t;
-          const uint32_t T = exact_kth(s, seed, 1, w.mis, 0, n_seed, K, need_t);
-          thr_key = T;  // the fine bins count from T's (the ties are candidates)
+          const uint32_t T = crowded_seed(s, S, w.mis, n_seed, len, K, wc);
+          thr_key = T;                    // the fine bins count from T's (the ties are candidates)
           thr = key_floor_value(T + 1u);  // T is at most the key of +inf, so T + 1 does not wrap
-          // thread i owns seed elements 2i and 2i + 1; a block scan ranks the ties
-          const int ea = 2 * tid;
-          const bool ta = ea < n_seed && fkey(seed[w.mis + ea]) == T;
-          const bool tb = ea + 1 < n_seed && fkey(seed[w.mis + ea + 1]) == T;
-          const int mine = (ta ? 1 : 0) + (tb ? 1 : 0);
-          int incl = mine;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += x;
-          }
-          if (lane == 31) s.tcnt[warp] = incl;
-          __syncthreads();
-          int before = incl - mine;
-          for (int q = 0; q < warp; ++q) before += s.tcnt[q];
-          const bool sa = ta && before < need_t;
-          const bool sb = tb && before + (ta ? 1 : 0) < need_t;
-          const int sel = (sa ? 1 : 0) + (sb ? 1 : 0);
-          const int at = base + warp_excl(sel);  // at most 64 per warp: inside its region
-          if (sa) {
-            s.ckey[at] = T;
-            s.cidx[at] = ea;
-          }
-          if (sb) {
-            s.ckey[at + (sa ? 1 : 0)] = T;
-            s.cidx[at + (sa ? 1 : 0)] = ea + 1;
-          }
-          wc = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(sel)));
-          if (lane == 0 && wc) atomicAdd(&my_bins[0], wc);  // fine bin T >> kFine is f0
-          __syncthreads();
         }
         const int f0 = static_cast<int>(thr_key >> kFine);  // every candidate's fine bin is at least f0
         const int nvec = w.nwin >> 2;
@@ -936,29 +1079,47 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
                 s.ri[tid] = 0x7FFFFFFF;
               }
               __syncthreads();
-              // each entry's rank, by a group of 2^lg lanes (the most that fit the
-              // block, at most a warp): lane `sub` of the group compares the entry
-              // with entries 4 sub .. 4 sub + 3, then every 4 * 2^lg-th group on
-              int lg = 5;
-              while ((in_t << lg) > kThreads) --lg;
-              const int e = tid >> lg;
-              const int sub = tid & ((1 << lg) - 1);
-              if (((warp << 5) >> lg) < in_t) {  // the warp holds an entry's group (groups never straddle warps)
-                const bool act = e < in_t;
-                const uint32_t kj = act ? s.rk[e] : 0u;
-                const int32_t ij = act ? s.ri[e] : 0;
-                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-                for (int i0 = 4 * sub; i0 < c4; i0 += 4 << lg) {
-                  const uint4 k4 = *reinterpret_cast<const uint4*>(&s.rk[i0]);
-                  const int4 x4 = *reinterpret_cast<const int4*>(&s.ri[i0]);
-                  r0 += (k4.x > kj || (k4.x == kj && x4.x < ij)) ? 1 : 0;
-                  r1 += (k4.y > kj || (k4.y == kj && x4.y < ij)) ? 1 : 0;
-                  r2 += (k4.z > kj || (k4.z == kj && x4.z < ij)) ? 1 : 0;
-                  r3 += (k4.w > kj || (k4.w == kj && x4.w < ij)) ? 1 : 0;
+              if (in_t <= kRankDirect) {
+                rank_out(s.rk, s.ri, in_t, c4, need, o + (K - need));
+              } else {
+                // a large bin t: its entries split on the next 8 key bits (16..9);
+                // entries above the sub-bin b that holds the need-th are taken,
+                // those in it ranked
+                if (tid < in_t) atomicAdd(&s.hsub[(s.rk[tid] >> 9) & 0xFFu], 1u);
+                __syncthreads();
+                if (warp == 0) {
+                  int above_b;
+                  const int b = warp_find256(s.hsub, need, above_b);
+                  if (lane == 0) {
+                    s.sub_b = b;
+                    s.sub_above = above_b;
+                    s.n_win = 0;  // the counters place the taken entries and gather sub-bin b's
+                    s.n_bt = 0;
+                  }
                 }
-                int rank = r0 + r1 + r2 + r3;
-                for (int o2 = 1; o2 < (1 << lg); o2 <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o2);
-                if (act && sub == 0 && rank < need) o[K - need + rank] = ij;
+                __syncthreads();
+                const int b = s.sub_b;
+                const int sab = s.sub_above;
+                const int in_b = static_cast<int>(s.hsub[b]);
+                if (tid < in_t) {
+                  const uint32_t kj = s.rk[tid];
+                  const int32_t ij = s.ri[tid];
+                  const int d = static_cast<int>((kj >> 9) & 0xFFu);
+                  if (d > b) {
+                    o[K - need + atomicAdd(&s.n_win, 1)] = ij;
+                  } else if (d == b) {
+                    const int at = atomicAdd(&s.n_bt, 1);
+                    s.ckey[at] = kj;  // the candidate slots are free once emitted
+                    s.cidx[at] = ij;
+                  }
+                }
+                const int c4b = (in_b + 3) & ~3;
+                if (tid >= in_b && tid < c4b) {
+                  s.ckey[tid] = 0u;
+                  s.cidx[tid] = 0x7FFFFFFF;
+                }
+                __syncthreads();
+                rank_out(s.ckey, s.cidx, in_b, c4b, need - sab, o + (K - need + sab));
               }
             }
             done = true;
@@ -967,9 +1128,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           // included: they were loaded contiguously) from the ring
           if (!done) {
             if (stream)
-              fallback_select(s, p, r, w, w.rowp, 1, 0, 0);
+              fallback_select(s, p, r, w, Src{w.rowp - w.mis, 1, -1, len});
             else
-              fallback_select(s, p, r, w, s.row, 1, (bulk ? S * kPiece : 0) + w.mis, kWrap);
+              fallback_select(s, p, r, w, Src{nullptr, 1, bulk ? S * (kPiece / 4) : 0, len});
           }
         }
       }

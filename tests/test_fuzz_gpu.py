@@ -27,7 +27,7 @@ def rn():
 
 
 def _row(rng: np.random.Generator, n: int) -> np.ndarray:
-    kind = rng.integers(0, 8)
+    kind = rng.integers(0, 9)
     if kind == 0:
         return rng.standard_normal(n).astype(np.float32)
     if kind == 1:  # bf16 grid: many equal values
@@ -47,6 +47,11 @@ def _row(rng: np.random.Generator, n: int) -> np.ndarray:
         return x
     if kind == 6:  # heavy tails
         return rng.standard_cauchy(n).astype(np.float32)
+    if kind == 8:  # a dense cluster: many elements share the K-th key's top bits
+        x = rng.standard_normal(n).astype(np.float32)
+        m = rng.random(n) < rng.uniform(0.02, 0.3)
+        x[m] = (4.0 + rng.choice([0.02, 0.1, 0.3]) * rng.standard_normal(int(m.sum()))).astype(np.float32)
+        return x
     return (rng.standard_normal(n) * 0.01).astype(np.float32)
 
 

@@ -210,6 +210,45 @@ def test_edge_cases(rn, topk, S, G, merge, shape):
     assert rn.workspace_clean()
 
 
+def _dense_cluster_rows(S: int, rng) -> np.ndarray:
+    """Rows of N(0,1) with about 3000 of their elements in a narrow cluster around 4 (sd
+    0.05, 0.15 or 0.3), the last three also rounded to multiples of 2^-12 (equal keys)."""
+    rows = []
+    for i in range(6):
+        x = rng.standard_normal(S).astype(np.float32)
+        m = rng.random(S) < 3000.0 / S
+        x[m] = (4.0 + (0.05, 0.15, 0.3)[i % 3] * rng.standard_normal(int(m.sum()))).astype(np.float32)
+        if i >= 3:
+            x = (np.round(x * 4096.0) / 4096.0).astype(np.float32)
+        rows.append(x)
+    return np.stack(rows)
+
+
+def _kth_bin_size(row: np.ndarray, K: int) -> int:
+    """Elements of the row that share the K-th largest value's top 15 key bits (sign,
+    exponent and 6 mantissa bits): the size of the K-th key's bin in a radix select."""
+    u = row.view(np.uint32).astype(np.uint64)
+    keys = np.where(u >> 31 == 1, (~u) & 0xFFFFFFFF, u | 0x80000000)
+    kth = np.sort(keys)[::-1][K - 1]
+    return int(np.count_nonzero(keys >> 17 == kth >> 17))
+
+
+@pytest.mark.parametrize("S", [30000, 100000])
+@pytest.mark.parametrize("shape", [0, 4])
+def test_large_kth_key_bin(rn, S, shape):
+    """Hundreds of elements share the K-th key's bin (a dense cluster): the selection
+    splits that bin further before ranking; with equal keys inside it, by index."""
+    rng = np.random.default_rng(S + shape)
+    K = 2048
+    x = _dense_cluster_rows(S, rng)
+    lens = np.full(x.shape[0], S, np.int32)
+    sizes = [_kth_bin_size(r, K) for r in x]
+    assert any(192 < n <= 512 for n in sizes), sizes  # the data reach the split
+    got = rn.run(x, lens, K, options=rn.options(shape=shape))
+    assert_matches_oracle(x, lens, got, K, label=f"dense cluster S={S} shape={shape} bins {sizes}")
+    assert rn.workspace_clean()
+
+
 @pytest.mark.parametrize("G", [1, 3])
 def test_poison_beyond_length_is_never_used(rn, G):
     w = workloads.make("decode_batch", 8)
