@@ -437,8 +437,10 @@ def run_sweep(args) -> None:
     print(f"| row length | rows | planner | {' | '.join(a for a, _ in arms)} | best |")
     print("|---:|---:|---|" + "---:|" * (len(arms) + 1))
     stream = t.cuda.current_stream()
-    for L in SWEEP_LENGTHS:
-        for R in SWEEP_ROWS:
+    lengths = [int(v) for v in args.sweep_lengths.split(",")] if args.sweep_lengths else SWEEP_LENGTHS
+    rows = [int(v) for v in args.sweep_rows.split(",")] if args.sweep_rows else SWEEP_ROWS
+    for L in lengths:
+        for R in rows:
             if R * L * 4 > (5 << 30):
                 continue
             gen.manual_seed(0)
@@ -621,6 +623,8 @@ def main(argv=None) -> None:
     ap.add_argument("--sweep", action="store_true", help="time every launch shape over row length x rows")
     ap.add_argument("--sweep-topk", type=int, default=2048)
     ap.add_argument("--sweep-steps", type=int, default=10)
+    ap.add_argument("--sweep-lengths", default="", help="comma list of row lengths (default 4096 .. 262144)")
+    ap.add_argument("--sweep-rows", default="", help="comma list of row counts (default 1 .. 4096)")
     raw = list(sys.argv[1:] if argv is None else argv)
     args = ap.parse_args(raw)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps

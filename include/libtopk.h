@@ -94,8 +94,9 @@ typedef struct {
    * 2 = two CTAs of 12 consumer warps per SM (whole rows only); 3 = a CTA of 8
    * consumer warps in about 83 KB of shared memory (whole rows only), the
    * low-shared-memory mode for devices or partitions where 1 and 2 do not fit;
-   * 4 = the short-row kernel: one CTA of 32 warps holds a whole row in shared
-   * memory (rows of at most 32768 elements, whole rows only). */
+   * 4 = the short-row kernel: one CTA of 32 warps per SM owns whole rows, held
+   * in a 128 KB shared-memory ring (rows of up to 32768 elements) or streamed
+   * through it. */
   int shape;
 } topk_options;
 
@@ -112,7 +113,7 @@ typedef struct {
   int pair_ctas_per_sm;
   int small_smem_per_cta; /* the same for the small shape */
   int small_ctas_per_sm;
-  int short_smem_per_cta; /* the same for the short-row kernel (whole rows held in shared memory) */
+  int short_smem_per_cta; /* the same for the short-row kernel */
   int short_ctas_per_sm;
 } topk_device_props;
 
@@ -127,7 +128,7 @@ typedef struct {
   int cluster;        /* 1 when the CTAs of a group form a cluster and merge in its shared memory */
   int shape;          /* 1 = one CTA of 24 consumer warps per SM, 2 = two CTAs of 12 per SM,
                          3 = the small shape (8 consumer warps, low shared memory),
-                         4 = the short-row kernel (a whole row in shared memory) */
+                         4 = the short-row kernel */
 } topk_plan;
 
 /*

@@ -30,8 +30,9 @@ constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 // rows per SM one CTA's row finish overlaps the other's streaming.
 // kShapeSmall: 8 consumer warps in about 83 KB of shared memory, whole rows
 // only, for devices or partitions with less shared memory per block.
-// kShapeShort: the short-row kernel (topk_short.cu), one CTA of 32 warps that
-// holds a whole row of at most kShortMaxLen elements in shared memory.
+// kShapeShort: the short-row kernel (topk_short.cu), one CTA of 32 warps per
+// SM; a row of at most kShortMaxLen elements stays resident in its 128 KB ring,
+// a longer one streams through it.
 constexpr int kShapeWide = 1;
 constexpr int kShapePair = 2;
 constexpr int kShapeSmall = 3;

@@ -53,9 +53,9 @@ constexpr int kTask = 512;                          // window elements a warp fi
 constexpr int kSeed = kPiece;                       // window elements histogrammed for the seed (piece 0)
 constexpr int kRegion = 256;                        // candidate slots per warp
 constexpr int kCand = kWarps * kRegion;
-constexpr int kFine = 17;                           // fine bins: the top 15 key bits (key >> 17)
+constexpr int kFine = 17;                           // fine bins: (key - threshold) >> 17, or coarser
 constexpr int kTrack = 64;                          // fine bins counted during the filter, from the seed bin's edge
-constexpr int kRank = 512;                          // entries of the K-th key's fine bin at most (fast path)
+constexpr int kRank = kThreads / 2;                 // entries of the K-th key's fine bin at most (fast path)
 constexpr int kRankDirect = 192;                    // up to this many are ranked at once; more are first
                                                     // split on 8 more key bits
 constexpr int kTaskSurvivors = 128;                 // expected survivors a filter task may take
@@ -63,9 +63,8 @@ constexpr int kMinTasks = 8;                        // filter tasks a window is 
 constexpr int kRefineExcess = 256;                  // a resident row refines its seed bin only when that
                                                     // keeps more than this many extra survivors out
 static_assert(kRing <= 32, "slot phases fit one 32-bit mask");
-static_assert(((kRing * kPiece) & (kRing * kPiece - 1)) == 0, "ring indices wrap with a mask");
-constexpr int kWrap = kRing * kPiece - 1;
-static_assert(kWarps == 32, "one lane of warp 0 per warp when offsets are scanned");
+constexpr int kRingF4 = kRing * kPiece / 4;        // float4s in the ring
+static_assert(kWarps <= 32, "one lane of warp 0 per warp when counts are gathered");
 static_assert(kPiece % (2 * kTask) == 0 && kTask == 4 * 4 * 32, "tasks of up to 8 float4 per lane tile a piece");
 
 struct __align__(128) Smem {
@@ -75,9 +74,9 @@ struct __align__(128) Smem {
   uint32_t hseed[kBins];          // seed histogram; scratch of the fallback
   uint32_t bsum[kBins / 32];      // 32-bin block sums (find_top, in the fallback)
   alignas(16) uint32_t hsub[256]; // the seed bin's 8-bit sub-histogram (key bits 19..12)
-  alignas(16) uint32_t rk[kRank];
+  alignas(16) uint32_t rk[kRank];  // bin t's entries, ranked
   alignas(16) int32_t ri[kRank];
-  alignas(16) int wbin[kWarps][kTrack + 4];  // per warp: candidates in fine bin f0 + j (f0: the seed bin's
+  alignas(16) int wbin[kWarps][kTrack + 4];  // per warp: candidates in fine bin j, (key - thr) >> shift (thr: the
                                              // edge); rows padded by 16 bytes so a lane per row reads no bank twice
   alignas(16) int ftot[kTrack];   // fine-bin counts summed over the warps
   int n_win, n_bt;                // winners above bin t written, bin t's entries held (emission)
@@ -94,6 +93,8 @@ struct __align__(128) Smem {
   int t0, t, need, in_t, sel_ok;  // seed bin, the K-th key's fine bin, its entries taken and held, fast path ok
   int target;                     // the sample's best that the seed threshold keeps
   int sub_b, sub_above;           // a large K-th fine bin: the sub-bin holding the K-th, the count above it
+  int wide;                       // the K-th key lies above the counted fine bins: count again, coarser
+  uint32_t cmax;                  // the largest candidate key of the row
   int crowded;                    // the seed bin of a streamed row is crowded (heavy ties)
   int refine, need_in;            // the seed bin is wide: refine the threshold inside it, to `need_in` of its entries
   uint32_t thr_key;               // the filter keeps keys >= thr_key
@@ -323,7 +324,7 @@ struct Src {
 };
 
 __device__ __forceinline__ float4 load_group(const Smem& s, const Src& src, int v) {
-  if (src.ring0 >= 0) return reinterpret_cast<const float4*>(s.row)[(src.ring0 + v) & (kWrap >> 2)];
+  if (src.ring0 >= 0) return reinterpret_cast<const float4*>(s.row)[(src.ring0 + v) % kRingF4];
   if (src.cs == 1) return __ldg(reinterpret_cast<const float4*>(src.g) + v);
   float f[4];
 #pragma unroll
@@ -433,7 +434,7 @@ __device__ __noinline__ void fallback_select(Smem& s, const Params& p, int64_t r
       }
       if (lane == 31) s.tcnt[c & 1][warp] = incl;
       __syncthreads();
-      const int wt = s.tcnt[c & 1][lane];
+      const int wt = lane < kWarps ? s.tcnt[c & 1][lane] : 0;
       int wincl = wt;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -665,11 +666,15 @@ __device__ __noinline__ uint32_t crowded_seed(Smem& s, int S, int mis, int n_see
   const float* seed = s.row + S * kPiece;
   int need_t, equal_t;
   const uint32_t T = exact_kth(s, Src{nullptr, 1, S * (kPiece / 4), len}, mis, n_seed, K, need_t, equal_t);
-  // thread i owns seed elements 2i and 2i + 1; a block scan ranks the ties
-  const int ea = 2 * tid;
-  const bool ta = ea < n_seed && fkey(seed[mis + ea]) == T;
-  const bool tb = ea + 1 < n_seed && fkey(seed[mis + ea + 1]) == T;
-  const int mine = (ta ? 1 : 0) + (tb ? 1 : 0);
+  // thread i owns seed elements E i .. E i + E - 1; a block scan ranks the ties
+  constexpr int E = kSeed / kThreads;
+  static_assert(E * kThreads == kSeed && 32 * E <= kRegion, "the seed's ties fit the warps' regions");
+  const int e0 = E * tid;
+  uint32_t tie = 0;
+#pragma unroll
+  for (int j = 0; j < E; ++j)
+    if (e0 + j < n_seed && fkey(seed[mis + e0 + j]) == T) tie |= 1u << j;
+  const int mine = __popc(tie);
   int incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -678,22 +683,28 @@ __device__ __noinline__ uint32_t crowded_seed(Smem& s, int S, int mis, int n_see
   }
   if (lane == 31) s.tcnt[0][warp] = incl;
   __syncthreads();
-  int before = incl - mine;
-  for (int q = 0; q < warp; ++q) before += s.tcnt[0][q];
-  const bool sa = ta && before < need_t;
-  const bool sb = tb && before + (ta ? 1 : 0) < need_t;
-  const int sel = (sa ? 1 : 0) + (sb ? 1 : 0);
-  const int at = warp * kRegion + warp_excl(sel);  // at most 64 per warp: inside its region
-  if (sa) {
-    s.ckey[at] = T;
-    s.cidx[at] = ea;
+  int rank = incl - mine;
+  for (int q = 0; q < warp; ++q) rank += s.tcnt[0][q];
+  uint32_t keep = 0;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    if ((tie >> j) & 1u) {
+      if (rank < need_t) keep |= 1u << j;
+      ++rank;
+    }
   }
-  if (sb) {
-    s.ckey[at + (sa ? 1 : 0)] = T;
-    s.cidx[at + (sa ? 1 : 0)] = ea + 1;
+  const int sel = __popc(keep);
+  int at = warp * kRegion + warp_excl(sel);  // at most 32 E per warp: inside its region
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    if ((keep >> j) & 1u) {
+      s.ckey[at] = T;
+      s.cidx[at] = e0 + j;
+      ++at;
+    }
   }
   wc = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(sel)));
-  if (lane == 0 && wc) atomicAdd(&s.wbin[warp][0], wc);  // fine bin T >> kFine is f0
+  if (lane == 0 && wc) atomicAdd(&s.wbin[warp][0], wc);  // T's fine bin: 0
   __syncthreads();
   return T;
 }
@@ -739,6 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   if (tid == 0) {
     s.n_win = 0;
     s.n_bt = 0;
+    s.cmax = 0;
   }
   __syncthreads();
   int len = clamp_len(p, len_raw0, tid == 0);
@@ -872,7 +884,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           thr_key = T;                    // the fine bins count from T's (the ties are candidates)
           thr = key_floor_value(T + 1u);  // T is at most the key of +inf, so T + 1 does not wrap
         }
-        const int f0 = static_cast<int>(thr_key >> kFine);  // every candidate's fine bin is at least f0
         const int nvec = w.nwin >> 2;
         // float4s per lane in a task: the most (up to 8, which spreads the per-task
         // work over the most elements) that keep a task's expected survivors (the
@@ -950,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
                   const uint32_t key = fkey(s.row[sb + pos]);
                   s.ckey[base + wc + e] = key;
                   s.cidx[base + wc + e] = task * tsz + pos - w.mis;
-                  const int d = static_cast<int>(key >> kFine) - f0;
+                  const uint32_t d = (key - thr_key) >> kFine;
                   if (d < kTrack) atomicAdd(&my_bins[d], 1);
                 }
               }
@@ -987,9 +998,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           aborted = true;
         } else {
           // ---- the K-th key's fine bin t (warp 0; lane l reads warp l's survivor
-          // count and the totals of fine bins 2l and 2l + 1)
+          // count and the totals of fine bins 2l and 2l + 1). When the K-th key lies
+          // above the 64 bins counted, the candidates are counted once more in bins
+          // wide enough to hold them all, and the search repeats.
+          int fsh = kFine;  // fine bin of a candidate: (key - thr_key) >> fsh
+#pragma unroll 1
+          for (;;) {
           if (warp == 0) {
-            const int n_l = s.wcnt[lane];
+            const int n_l = lane < kWarps ? s.wcnt[lane] : 0;
             const int2 c2 = *reinterpret_cast<const int2*>(&s.ftot[2 * lane]);
             const int c0 = c2.x, c1 = c2.y;
             const bool over = __any_sync(0xFFFFFFFFu, n_l > kRegion);
@@ -1013,18 +1029,39 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
             const bool all_t = need == in_t;
             const bool sel_ok = !over && n_c >= K && hit != 0 && (all_t || in_t <= kRank);
             if (lane == 0) {
+              s.wide = (!over && n_c >= K && hit == 0 && fsh == kFine) ? 1 : 0;
               s.sel_ok = sel_ok ? 1 : 0;
-              s.t = jt;  // relative to f0
+              s.t = jt;
               s.need = all_t ? 0 : need;  // 0: bin t is taken whole
               s.in_t = in_t;
             }
           }
           __syncthreads();
+          if (!s.wide) break;
+          // count again: the smallest shift that puts every candidate in the 64 bins
+          const int cnt_w = s.wcnt[warp];  // at most kRegion: no overflow here
+          uint32_t cmax = thr_key;
+          for (int e = lane; e < cnt_w; e += 32) cmax = max(cmax, s.ckey[base + e]);
+          cmax = __reduce_max_sync(0xFFFFFFFFu, cmax);
+          if (lane == 0) atomicMax(&s.cmax, cmax);
+          *reinterpret_cast<int2*>(&my_bins[2 * lane]) = make_int2(0, 0);
+          if (tid < kTrack) s.ftot[tid] = 0;
+          __syncthreads();
+          const uint32_t span = s.cmax - thr_key;
+          while ((span >> fsh) >= static_cast<uint32_t>(kTrack)) ++fsh;
+          for (int e = lane; e < cnt_w; e += 32) atomicAdd(&my_bins[(s.ckey[base + e] - thr_key) >> fsh], 1);
+          __syncwarp();
+          if (cnt_w > 0) {
+            const int2 v2 = *reinterpret_cast<const int2*>(&my_bins[2 * lane]);
+            if (v2.x) atomicAdd(&s.ftot[2 * lane], v2.x);
+            if (v2.y) atomicAdd(&s.ftot[2 * lane + 1], v2.y);
+          }
+          __syncthreads();
+          }
           bool done = false;
           if (s.sel_ok) {
             // ---- winners above bin t out; bin t's entries into the ranking slots
             const int jt = s.t;
-            const int t = f0 + jt;
             const int need = s.need;
             const bool all_t = need == 0;
             const int cnt = s.wcnt[warp];  // at most kRegion here
@@ -1056,10 +1093,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
               if (e < cnt) {
                 key = s.ckey[base + e];
                 idx = s.cidx[base + e];
-                d = static_cast<int>(key >> kFine);
+                d = static_cast<int>((key - thr_key) >> fsh);
               }
-              const bool win = d > t || (all_t && d == t);
-              const bool inb = !all_t && d == t;
+              const bool win = d > jt || (all_t && d == jt);
+              const bool inb = !all_t && d == jt;
               const uint32_t bw = __ballot_sync(0xFFFFFFFFu, win);
               if (win) o[ow + __popc(bw & lt)] = idx;
               ow += __popc(bw);
@@ -1082,10 +1119,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
               if (in_t <= kRankDirect) {
                 rank_out(s.rk, s.ri, in_t, c4, need, o + (K - need));
               } else {
-                // a large bin t: its entries split on the next 8 key bits (16..9);
-                // entries above the sub-bin b that holds the need-th are taken,
-                // those in it ranked
-                if (tid < in_t) atomicAdd(&s.hsub[(s.rk[tid] >> 9) & 0xFFu], 1u);
+                // a large bin t: its entries split on the next 8 bits of key -
+                // thr_key; entries above the sub-bin b that holds the need-th are
+                // taken, those in it ranked
+                if (tid < in_t) atomicAdd(&s.hsub[((s.rk[tid] - thr_key) >> (fsh - 8)) & 0xFFu], 1u);
                 __syncthreads();
                 if (warp == 0) {
                   int above_b;
@@ -1104,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
                 if (tid < in_t) {
                   const uint32_t kj = s.rk[tid];
                   const int32_t ij = s.ri[tid];
-                  const int d = static_cast<int>((kj >> 9) & 0xFFu);
+                  const int d = static_cast<int>(((kj - thr_key) >> (fsh - 8)) & 0xFFu);
                   if (d > b) {
                     o[K - need + atomicAdd(&s.n_win, 1)] = ij;
                   } else if (d == b) {
@@ -1147,14 +1184,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
     __syncthreads();
     // read here, between two barriers: thread 0 writes the one after it at the next row's start
     const int len_next = s.len_next;
-    static_assert(kBins == 4 * kThreads, "one 16-byte store per thread clears the seed histogram");
-    reinterpret_cast<uint4*>(s.hseed)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    static_assert(kBins % (4 * kThreads) == 0, "16-byte stores clear the seed histogram");
+#pragma unroll
+    for (int b = tid; b < kBins / 4; b += kThreads) reinterpret_cast<uint4*>(s.hseed)[b] = make_uint4(0u, 0u, 0u, 0u);
     *reinterpret_cast<int2*>(&s.wbin[warp][2 * lane]) = make_int2(0, 0);
     if (tid < 256) s.hsub[tid] = 0;
     if (tid < kTrack) s.ftot[tid] = 0;
     if (tid == 0) {
       s.n_win = 0;
       s.n_bt = 0;
+      s.cmax = 0;
     }
     if (warp == 0) {
       // the first row's blind pieces past its window may still be landing:

@@ -249,6 +249,25 @@ def test_large_kth_key_bin(rn, S, shape):
     assert rn.workspace_clean()
 
 
+@pytest.mark.parametrize("S,K", [(4096, 1536), (4096, 2048), (6000, 2800), (8192, 4096), (40000, 4096)])
+@pytest.mark.parametrize("shape", [0, 4])
+def test_kth_key_far_from_the_threshold(rn, S, K, shape):
+    """The K-th key lies many binades above the seed's threshold: a selected fraction
+    near one half of N(0,1) rows (the K-th value near zero), and rows whose values near
+    the K-th span tiny magnitudes of both signs."""
+    rng = np.random.default_rng(S * 7 + K)
+    rows = [rng.standard_normal(S).astype(np.float32) for _ in range(4)]
+    r = -np.abs(rng.standard_normal(S)).astype(np.float32)
+    pos = rng.random(S) < (K * 0.6) / S
+    r[pos] = (np.abs(rng.standard_normal(int(pos.sum()))) * 10.0 ** rng.uniform(-30, 0, int(pos.sum()))).astype(np.float32)
+    rows.append(r)
+    x = np.stack(rows)
+    lens = np.full(x.shape[0], S, np.int32)
+    got = rn.run(x, lens, K, options=rn.options(shape=shape))
+    assert_matches_oracle(x, lens, got, K, label=f"far K-th S={S} K={K} shape={shape}")
+    assert rn.workspace_clean()
+
+
 @pytest.mark.parametrize("G", [1, 3])
 def test_poison_beyond_length_is_never_used(rn, G):
     w = workloads.make("decode_batch", 8)
