@@ -26,11 +26,11 @@
 //     kSplitGainCluster elements per CTA; otherwise they merge through the
 //     workspace with a grid-level barrier;
 //   - G = 1 launches min(num_rows, capacity) persistent CTAs, no waiting;
-//     with at least kPairRowsPerSm rows per SM it uses the paired shape (two
-//     CTAs of 12 consumer warps per SM), otherwise the wide one;
-//   - whole rows of at most kShortMaxLen elements (row_stride) take the
-//     short-row kernel, one CTA of 32 warps per row holding the row in shared
-//     memory, where the device can hold it;
+//     with at least kPairRowsPerSm rows per SM of at most kPairMaxStride
+//     elements it uses the paired shape (two CTAs of 12 consumer warps per
+//     SM); otherwise the short-row kernel (one CTA of 32 warps per SM, rows
+//     resident in or streamed through its 128 KB ring) where the device holds
+//     it and TopK is below half the row stride; otherwise the wide shape;
 //   - a device whose shared memory per block cannot hold the wide shape gets
 //     whole rows on the paired shape if it fits, else on the small shape
 //     (about 83 KB), else TOPK_ERR_PLAN;
@@ -119,13 +119,21 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
         cluster = false;
       }
     }
-    // whole rows: two narrower CTAs per SM when every SM gets several rows, so
-    // that one CTA's row finish overlaps the other's streaming (measured on a
-    // GB300 with 4096 rows of 61440+: 440 us against 509 us)
+    // whole rows: the paired shape (two narrower CTAs per SM, one CTA's row
+    // finish overlapping the other's streaming) when every SM gets several
+    // short rows; else the short-row kernel, unless TopK is half the row or
+    // more on rows longer than its sample (its sampled threshold then rarely
+    // brackets the K-th key); else the wide shape. Measured on a GB300 (bench.py --sweep, TopK 512 to 2048): the
+    // paired shape wins from 608 rows of up to 16384 elements, the short-row
+    // kernel at 32768 and beyond and for fewer rows, the wide shape for TopK
+    // 2048 of 4096-element rows
     if (chosen == 0) {
-      const bool pair = G == 1 && topk <= ltk::kPairMaxTopK && pair_ok && props->pair_ctas_per_sm >= 2 &&
-                        num_rows >= ltk::kPairRowsPerSm * props->num_sms;
-      chosen = pair ? ltk::kShapePair : (G == 1 && short_ok) ? ltk::kShapeShort : ltk::kShapeWide;
+      const bool many = num_rows >= ltk::kPairRowsPerSm * props->num_sms;
+      const bool pair = G == 1 && topk <= ltk::kPairMaxTopK && pair_ok && props->pair_ctas_per_sm >= 2 && many &&
+                        (row_stride <= ltk::kPairMaxStride || !short_ok);
+      const bool shrt = G == 1 && short_ok &&
+                        (row_stride <= ltk::kShortSeedLen || 2 * static_cast<int64_t>(topk) < row_stride);
+      chosen = pair ? ltk::kShapePair : shrt ? ltk::kShapeShort : ltk::kShapeWide;
     }
   }
   plan->shape = chosen;

@@ -23,6 +23,7 @@ constexpr int64_t kDefaultLongRowThreshold = 32768;
 constexpr int64_t kSplitGain = 90000;         // elements a workspace-merged split must save per CTA (measured)
 constexpr int64_t kSplitGainCluster = 24000;  // elements a cluster-merged split must save per CTA
 constexpr int64_t kPairRowsPerSm = 4;         // rows per SM from which the paired shape is planned
+constexpr int64_t kPairMaxStride = 16384;     // ... for rows up to this long (longer: the short-row kernel)
 constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 // CTA shapes. kShapeWide: one CTA of 24 consumer warps per SM (any row split).
@@ -42,6 +43,7 @@ constexpr int kPairCtaThreads = 416;   // 12 consumer warps + the copy warp
 constexpr int kSmallCtaThreads = 288;  // 8 consumer warps + the copy warp
 constexpr int kShortCtaThreads = 1024;
 constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds resident in its ring
+constexpr int64_t kShortSeedLen = 2048;  // elements it samples for its threshold (rows this short: all of them)
 // Rows at least this long are split across CTAs even where the short-row
 // kernel could stream them whole: on a GB300 it streams a whole row faster
 // than a split of the other kernel merges it up to the workloads measured

@@ -276,16 +276,23 @@ def test_static_scratch_capacity_is_reachable_on_larger_devices():
 def test_short_row_kernel():
     """Whole rows take the short-row kernel where the device holds it (rows of up to 16 pieces
     stay resident in its ring, longer ones stream through it), except batches of at least four
-    rows per SM, which the paired shape streams; only very long rows are split across CTAs."""
+    rows per SM of up to 16384 elements, which the paired shape streams, and TopK of half the
+    row or more, which the wide shape selects; only very long rows are split across CTAs (the
+    thresholds are the crossovers that bench.py --sweep measured on a GB300)."""
     gb = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT)
-    for rows, stride, k in ((8, 4096, 512), (64, 32768, 2048), (1, 1, 1), (300, 6000, 4096),
-                            (16, 131072, 2048), (64, 163840, 1024), (4096, 65536, 3000)):
+    for rows, stride, k in ((8, 4096, 512), (64, 32768, 2048), (1, 1, 1), (300, 6000, 2048), (16, 131072, 2048),
+                            (64, 163840, 1024), (4096, 65536, 3000), (4096, 65536, 2048), (4096, 32768, 2048),
+                            (608, 16385, 2048), (152, 8192, 1024), (64, 4097, 2048), (10, 1000, 2048),
+                            (64, 2048, 1024), (152, 2048, 2047)):
         rc, pl = plan(gb, rows, stride, topk=k)
         assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1 and pl.threads == 1024, (rows, stride, k)
         assert pl.grid == min(rows, 152) and not pl.cooperative and not pl.cluster
-    for rows, stride in ((4096, 65536), (4096, 32768), (608, 20000)):
-        rc, pl = plan(gb, rows, stride)
-        assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1
+    for rows, stride, k in ((4096, 16384, 2048), (608, 8192, 2048), (608, 4096, 512), (4096, 2048, 1024)):
+        rc, pl = plan(gb, rows, stride, topk=k)
+        assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1, (rows, stride, k)
+    for rows, stride, k in ((64, 4096, 2048), (300, 6000, 4096), (1, 4096, 4095)):
+        rc, pl = plan(gb, rows, stride, topk=k)
+        assert rc == 0 and pl.shape == 1 and pl.ctas_per_group == 1, (rows, stride, k)
     # rows of a million elements and more, few of them, are still split across CTAs
     rc, pl = plan(gb, 16, 1 << 21)
     assert rc == 0 and pl.shape == 1 and pl.ctas_per_group > 1
