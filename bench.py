@@ -411,10 +411,10 @@ def run_only(args) -> None:
     """Times one workload's kernel alone (for profiling runs); one JSON line."""
     gb = GpuBench(0)
     peak, _ = read_peaks()
-    w = workloads.make(args.only)
+    w = workloads.make(args.only, args.rows or None)
     r = gb.time_kernel(w, args.steps, args.warmup)
     gbs = w.valid_bytes() / (r["ms_mean"] * 1e-3) / 1e9
-    print(json.dumps({"workload": args.only, "us_per_call": r["ms_mean"] * 1e3,
+    print(json.dumps({"workload": args.only, "num_rows": w.num_rows, "us_per_call": r["ms_mean"] * 1e3,
                       "us_per_call_median": r["ms_median"] * 1e3, "effective_gbs": gbs,
                       "frac_of_hbm_peak": gbs / peak, "steps": args.steps}), flush=True)
 
@@ -619,6 +619,7 @@ def main(argv=None) -> None:
     ap.add_argument("--cpu-budget", type=float, default=3.0, help="seconds of oracle wall time")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timings")
     ap.add_argument("--only", default="", help="time only this workload's kernel (profiling runs)")
+    ap.add_argument("--rows", type=int, default=0, help="with --only: that many rows of the workload (0: all)")
     ap.add_argument("--dry-run", action="store_true", help="launch and aggregate with zero-work steps, no GPU")
     ap.add_argument("--sweep", action="store_true", help="time every launch shape over row length x rows")
     ap.add_argument("--sweep-topk", type=int, default=2048)
