@@ -1,5 +1,5 @@
-// Short rows: one CTA holds a whole row in shared memory (rows of at most
-// kShortMaxLen elements, whole rows only).
+// The short-row kernel: one CTA of 32 warps per SM owns whole rows (any
+// length), held in or streamed through a shared-memory ring.
 //
 // This is the single-CTA path of the method: a shared-memory histogram seeds a
 // threshold, a filter keeps the elements at or above it as candidates with
@@ -8,34 +8,34 @@
 // take in the persistent_topk launcher of the vLLM PR #41189 page,
 // "Implementation breakdown"; the single-CTA FilteredTopK there keeps rows in
 // at least 128 KB of shared memory, vLLM PR #54110 page, "Feature and
-// motivation").
+// motivation"). Here one CTA also streams rows longer than its ring, so no row
+// up to 2^20 elements is split across CTAs.
 //
-// A decode step runs one call over a few dozen rows, so what counts is how
-// soon after its data lands a row is done, and within the CTA that is set by
-// how many instructions the 32 warps issue, not by memory:
-//   - warp 0's lanes issue the row's window as 8 KB bulk copies (cp.async.bulk),
-//     one mbarrier each; for a CTA's first row at kernel start, sized by the
-//     row stride before the length is known;
-//   - piece 0 (2048 elements) is histogrammed on the top 12 key bits and one
-//     warp picks the seed bin t0 for about 1.25 K survivors over the row;
-//   - every warp filters tasks of 512 elements (4 float4 per lane) as their
-//     pieces land, one fp32 compare per element. A lane notes where its
-//     survivors are straight in the warp's own region of the candidate
-//     buffer; the warp then converts them 32 at a time and counts them by
-//     their bin relative to t0 (8 bins, one ballot each): no atomics;
-//   - one warp finds the K-th key's bin t from those counts and gives every
-//     warp its output offsets; the warps write the winners above t and list
-//     bin t, counting the list by its next 4 key bits; one warp finds the
-//     K-th key's sub-bin and the offsets again; the warps write the winners
-//     above it and stage the sub-bin's entries, which are ranked by (key desc,
-//     index asc). Six block barriers per row, no contended atomics.
-// Anything outside that shape (fewer than K survivors, a full region, a K-th
-// bin more than 8 bins above t0, a crowded list or sub-bin) falls back to an
-// exact radix select over the resident row, whose ties are taken in index
-// order by a block-wide scan.
+// Per row:
+//   - lanes of warp 0 issue the row's window as 8 KB bulk copies
+//     (cp.async.bulk), one mbarrier per ring slot; a row of up to 16 pieces
+//     stays resident, a longer one streams (each piece's slot goes to piece
+//     j + 16, and the last pieces' slots to the next row's first pieces);
+//   - piece 0 is histogrammed on the top 12 key bits and one warp picks the
+//     seed bin for about three standard deviations more than the row's K best
+//     that the sample should hold (split on 8 more bits when it is wide);
+//   - every warp filters tasks of up to 8 float4 per lane as their pieces land,
+//     one fp32 compare per element; survivors go to the warp's own candidate
+//     region and its own fine-bin counters, (key - threshold) >> 17: no
+//     contended atomics;
+//   - one warp finds the K-th key's fine bin t from the folded counters; the
+//     warps write the winners above t through shared output counters, and t's
+//     entries are ranked by (key desc, index asc), split first on 8 more key
+//     bits when there are many.
+// Anything outside that shape (fewer than K survivors, a full region, the K-th
+// key in a crowded bin) falls back to an exact radix select over the row (from
+// the ring when resident, from global memory when streamed), whose ties are
+// taken in index order by a block-wide scan. A K-th key above the counted bins
+// only recounts the candidates with wider bins.
 //
-// Strided logits (a column stride above 1) are loaded into the same buffer by
-// every thread with plain loads; the rest is the same.
+// Strided logits (a column stride above 1) are loaded into the ring by every
+// thread with plain loads (rows up to the ring's size) or selected by the exact
+// path straight from global memory.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
