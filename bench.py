@@ -277,6 +277,9 @@ class GpuBench:
                  3: "small (8 consumer warps)",
                  4: "short-row (32 warps, 1 CTA/SM, row resident in or streamed through a 128 KB ring)"
                  }.get(pl.shape, str(pl.shape))
+        if pl.shape == 4 and pl.ctas_per_group > 1:
+            shape = (f"short-row cluster ({pl.ctas_per_group} CTAs of 32 warps per row, CTA c streaming "
+                     f"pieces c, c + {pl.ctas_per_group}, ... through its 128 KB ring)")
         return {"ctas_per_row": pl.ctas_per_group, "grid": pl.grid, "merge": merge, "shape": shape}
 
     def flush_l2(self):
@@ -432,8 +435,11 @@ def run_sweep(args) -> None:
     props = sar.topk_query_device(0)
     K = args.sweep_topk
     gen = t.Generator(device=gb.dev)
-    arms = [("short", dict(shape=4)), ("paired", dict(shape=2)), ("wide", dict(shape=1, force_ctas_per_group=1))]
+    arms = [("short", dict(shape=4, force_ctas_per_group=1)), ("paired", dict(shape=2)),
+            ("wide", dict(shape=1, force_ctas_per_group=1))]
     arms += [(f"split{g}", dict(shape=1, force_ctas_per_group=g, merge=2)) for g in (2, 4, 8)]
+    # the short-row kernel with each row split over a cluster of g CTAs
+    arms += [(f"short{g}", dict(shape=4, force_ctas_per_group=g)) for g in (2, 3, 4, 6, 8)]
     print(f"| row length | rows | planner | {' | '.join(a for a, _ in arms)} | best |")
     print("|---:|---:|---|" + "---:|" * (len(arms) + 1))
     stream = t.cuda.current_stream()
@@ -456,8 +462,8 @@ def run_sweep(args) -> None:
                 for k, v in kw.items():
                     setattr(o, k, v)
                 rc, plo = sar.topk_make_plan(props, R, L, 1, K, o)
-                if rc != 0 or (kw.get("force_ctas_per_group", 1) > 1 and (R >= props.num_sms or
-                                                                         plo.ctas_per_group != kw["force_ctas_per_group"])):
+                g = kw.get("force_ctas_per_group", 1)
+                if rc != 0 or (g > 1 and (R * g > props.num_sms or plo.ctas_per_group != g)):
                     times.append(None)
                     continue
                 fn = lambda: sar.topk_ragged_ex(x, L, ln, R, 1, K, out, gb.sel.workspace, gb.stream_handle, o)

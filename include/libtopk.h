@@ -115,6 +115,9 @@ typedef struct {
   int small_ctas_per_sm;
   int short_smem_per_cta; /* the same for the short-row kernel */
   int short_ctas_per_sm;
+  /* short_cluster_groups[c], c = 2..8: resident clusters of c CTAs of the
+   * short-row kernel's cluster form (a row split over a cluster). */
+  int short_cluster_groups[9];
 } topk_device_props;
 
 /* A launch configuration. */

@@ -86,7 +86,8 @@ class TopkDeviceProps(ctypes.Structure):
                 ("small_smem_per_cta", ctypes.c_int),
                 ("small_ctas_per_sm", ctypes.c_int),
                 ("short_smem_per_cta", ctypes.c_int),
-                ("short_ctas_per_sm", ctypes.c_int)]
+                ("short_ctas_per_sm", ctypes.c_int),
+                ("short_cluster_groups", ctypes.c_int * 9)]
 
 
 class TopkPlan(ctypes.Structure):

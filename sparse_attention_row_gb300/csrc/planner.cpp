@@ -25,6 +25,13 @@
 //     resident with one per row, and kept if it saves at least
 //     kSplitGainCluster elements per CTA; otherwise they merge through the
 //     workspace with a grid-level barrier;
+//   - rows of at least 65536 elements, fewer than half the SMs, are split over
+//     thread-block clusters of the short-row kernel: the largest size up to 8
+//     with rows x size <= num_sms whose clusters can all be resident, one row
+//     per cluster, if each CTA's expected filter candidates stay within
+//     kShortMaxCandidates; whole rows take that kernel only under the same
+//     bound and up to kShortMaxWholeStride elements, and longer rows that it
+//     cannot split take the wide shape;
 //   - G = 1 launches min(num_rows, capacity) persistent CTAs, no waiting;
 //     with at least kPairRowsPerSm rows per SM of at most kPairMaxStride
 //     elements it uses the paired shape (two CTAs of 12 consumer warps per
@@ -41,6 +48,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "libtopk.h"
 #include "topk_internal.h"
@@ -48,6 +56,16 @@
 namespace {
 
 bool topk_supported(int topk) { return topk >= 1 && topk <= ltk::kWideMaxTopK; }
+
+// Candidates the short-row kernel's filter is expected to keep on a row of
+// `stride` elements: its threshold keeps mu + 3 sqrt(mu) + 2 keys of the
+// kShortSeedLen-element sample (mu = topk * kShortSeedLen / stride, the
+// sample's expected share of the row's TopK best), projected over the row.
+double short_row_candidates(int64_t stride, int topk) {
+  const double rho = static_cast<double>(stride) / static_cast<double>(ltk::kShortSeedLen);
+  if (rho <= 1.0) return topk;
+  return topk + 3.0 * std::sqrt(topk * rho) + 2.0 * rho;
+}
 
 }  // namespace
 
@@ -64,7 +82,10 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   if (shape < 0 || shape > 4) return TOPK_ERR_INVALID_ARG;
   const int force = (options != nullptr) ? options->force_ctas_per_group : 0;
   if (force < 0 || force > ltk::kMaxGroup) return TOPK_ERR_INVALID_ARG;
-  if (shape > ltk::kShapeWide && force > 1) return TOPK_ERR_INVALID_ARG;  // those shapes split no row
+  // the paired and small shapes split no row; the short-row kernel splits one
+  // over a thread-block cluster of up to 8 CTAs
+  if (shape > ltk::kShapeWide && force > 1 && (shape != ltk::kShapeShort || force > ltk::kMaxCluster))
+    return TOPK_ERR_INVALID_ARG;
   if (props->num_sms < 1) return TOPK_ERR_PLAN;
   const bool wide_ok = props->ctas_per_sm >= 1 && props->smem_per_cta <= props->max_smem_optin;
   const bool pair_ok = props->pair_ctas_per_sm >= 1 && props->pair_smem_per_cta <= props->max_smem_optin;
@@ -90,17 +111,35 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   auto clusters_of = [&](int64_t c) -> int64_t {
     return (c >= 2 && c <= ltk::kMaxCluster) ? props->cluster_groups[c] : 0;
   };
+  // the short-row kernel's cluster split of each row: the largest size up to
+  // 8 with rows x size within the SMs whose clusters are all resident at once,
+  // if its CTAs' expected candidates stay within kShortMaxCandidates (0: none)
+  const double candidates = short_row_candidates(row_stride, topk);
+  auto short_cluster_size = [&]() -> int64_t {
+    if (!short_ok || force != 0 || merge == 1 || num_rows < 1 || row_stride < ltk::kShortClusterStride ||
+        2 * static_cast<int64_t>(topk) >= row_stride)
+      return 0;
+    int64_t sms = props->num_sms;
+    if (options != nullptr && options->max_ctas > 0) sms = std::min<int64_t>(sms, options->max_ctas);
+    int64_t g = std::min<int64_t>(ltk::kMaxCluster, sms / num_rows);
+    while (g >= 2 && props->short_cluster_groups[g] < num_rows) --g;
+    return (g >= 2 && candidates / static_cast<double>(g) <= ltk::kShortMaxCandidates) ? g : 0;
+  };
+  // whole rows fit the short-row kernel's candidate regions, and its sample
+  const bool short_whole =
+      short_ok && candidates <= ltk::kShortMaxCandidates && row_stride <= ltk::kShortMaxWholeStride;
   int64_t G = 1;
   bool cluster = false;
-  if (chosen <= ltk::kShapeWide) {  // the wide shape, given or still open
+  if (chosen == 0 && short_cluster_size() >= 2) {
+    chosen = ltk::kShapeShort;  // few long rows: split over clusters of the short-row kernel
+  } else if (chosen <= ltk::kShapeWide) {  // the wide shape, given or still open
     if (force != 0) {
       G = force;
       if (G > 1) {
         if (merge == 2 && clusters_of(G) < 1) return TOPK_ERR_PLAN;
         cluster = merge == 2 || (merge == 0 && clusters_of(G) >= 1);
       }
-    } else if (num_rows > 0 && row_stride > threshold && num_rows < cap &&
-               (!short_ok || shape == ltk::kShapeWide || row_stride >= ltk::kShortSplitStride)) {
+    } else if (num_rows > 0 && row_stride > threshold && num_rows < cap && (!short_whole || shape == ltk::kShapeWide)) {
       G = cap / num_rows;
       G = std::min<int64_t>(G, ltk::kMaxGroup);
       G = std::min<int64_t>(G, std::max<int64_t>(1, row_stride / ltk::kMinSpan));
@@ -123,7 +162,8 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     // finish overlapping the other's streaming) when every SM gets several
     // short rows; else the short-row kernel, unless TopK is half the row or
     // more on rows longer than its sample (its sampled threshold then rarely
-    // brackets the K-th key); else the wide shape. Measured on a GB300 (bench.py --sweep, TopK 512 to 2048): the
+    // brackets the K-th key) or its expected candidates overflow; else the wide
+    // shape. Measured on a GB300 (bench.py --sweep, TopK 512 to 2048): the
     // paired shape wins from 608 rows of up to 16384 elements, the short-row
     // kernel at 32768 and beyond and for fewer rows, the wide shape for TopK
     // 2048 of 4096-element rows
@@ -131,9 +171,22 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
       const bool many = num_rows >= ltk::kPairRowsPerSm * props->num_sms;
       const bool pair = G == 1 && topk <= ltk::kPairMaxTopK && pair_ok && props->pair_ctas_per_sm >= 2 && many &&
                         (row_stride <= ltk::kPairMaxStride || !short_ok);
-      const bool shrt = G == 1 && short_ok &&
+      const bool shrt = G == 1 && short_whole &&
                         (row_stride <= ltk::kShortSeedLen || 2 * static_cast<int64_t>(topk) < row_stride);
       chosen = pair ? ltk::kShapePair : shrt ? ltk::kShapeShort : ltk::kShapeWide;
+    }
+  }
+  if (chosen == ltk::kShapeShort && force > 1) {
+    // a row split over a cluster of the short-row kernel: one row per cluster,
+    // merged in its shared memory only
+    if (merge == 1 || props->short_cluster_groups[force] < 1) return TOPK_ERR_PLAN;
+    G = force;
+    cluster = true;
+  } else if (chosen == ltk::kShapeShort && G == 1) {
+    const int64_t g = short_cluster_size();  // also when the short-row kernel was asked for
+    if (g >= 2) {
+      G = g;
+      cluster = true;
     }
   }
   plan->shape = chosen;
@@ -162,7 +215,12 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     return TOPK_OK;
   }
   int64_t groups;
-  if (G == 1) {
+  if (chosen == ltk::kShapeShort && G > 1) {
+    // one row per cluster; clusters that are not resident wait for a free slot
+    if (num_rows > INT32_MAX / G) return TOPK_ERR_PLAN;
+    groups = num_rows;
+    plan->cooperative = 0;
+  } else if (G == 1) {
     groups = std::min<int64_t>(num_rows, cap);
     plan->cooperative = 0;
   } else if (cluster) {

@@ -90,6 +90,12 @@ int query_device_locked(int device, topk_device_props* out) {
       if (ltk::shortrow::kernel_configure() != cudaSuccess ||
           ltk::shortrow::kernel_occupancy(&p.short_ctas_per_sm) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
+      for (int c = 2; rc == TOPK_OK && c <= ltk::kMaxCluster; ++c) {
+        if (ltk::shortrow::kernel_max_clusters(c, &p.short_cluster_groups[c]) != cudaSuccess) {
+          cudaGetLastError();  // no clusters of this size: the row split is not planned
+          p.short_cluster_groups[c] = 0;
+        }
+      }
     }
     if (prev != device) cudaSetDevice(prev);
     if (rc != TOPK_OK) {
@@ -149,9 +155,18 @@ int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t str
   topk_plan plan{};
   rc = topk_make_plan(&props, c.num_rows, c.max_len, c.next_n, c.topk, &opt, &plan);
   if (rc != TOPK_OK) return rc;
+  // the short-row kernel splits only contiguous rows over a cluster; strided
+  // ones stay whole
+  if (plan.shape == kShapeShort && plan.ctas_per_group > 1 && c.col_stride != 1) {
+    opt.force_ctas_per_group = 1;
+    rc = topk_make_plan(&props, c.num_rows, c.max_len, c.next_n, c.topk, &opt, &plan);
+    if (rc != TOPK_OK) return rc;
+  }
   if (plan.grid < 1) return TOPK_OK;
-  // a caller-provided workspace holds num_sms row groups, as many as the planner ever uses
-  if (max_groups >= 0 && plan.ctas_per_group > 1 && plan.num_groups > max_groups) return TOPK_ERR_WORKSPACE_TOO_SMALL;
+  // a caller-provided workspace holds num_sms row groups, as many as the planner
+  // ever uses (the short-row kernel's cluster split uses none)
+  if (max_groups >= 0 && plan.ctas_per_group > 1 && plan.shape != kShapeShort && plan.num_groups > max_groups)
+    return TOPK_ERR_WORKSPACE_TOO_SMALL;
 
   Params p{};
   p.logits = c.logits;

@@ -44,12 +44,27 @@ constexpr int kSmallCtaThreads = 288;  // 8 consumer warps + the copy warp
 constexpr int kShortCtaThreads = 1024;
 constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds resident in its ring
 constexpr int64_t kShortSeedLen = 2048;  // elements it samples for its threshold (rows this short: all of them)
-// Rows at least this long are split across CTAs even where the short-row
-// kernel could stream them whole: on a GB300 it streams a whole row faster
-// than a split of the other kernel merges it up to the workloads measured
-// (131072 and 163840 elements: 30.6 and 26.6 us whole against 34.5 and 30.0 us
-// split), so only far longer rows are split.
-constexpr int64_t kShortSplitStride = 1 << 20;
+// Rows at least this long, too few to give every SM its own, are split over a
+// thread-block cluster of the short-row kernel: measured on a GB300 (bench.py
+// --sweep, TopK 2048), a cluster of 2 .. 8 CTAs finishes 65536-element rows in
+// 14.3 us against 16.4 us whole (131072: 14.6 to 20.5 against 22.5; 2^20: 21.9
+// against 41.1 for the other kernel's split), and loses on shorter rows (16384:
+// 14.3 against 12.3), where its merge costs more than the streaming it shares.
+constexpr int64_t kShortClusterStride = 65536;
+// The short-row kernel samples 2048 elements for its threshold, so on very long
+// rows the threshold keeps many more candidates than TopK (expected count:
+// short_row_candidates). A CTA is planned at most this many: more overflow its
+// candidate regions now and then, and the exact fallback that follows reads
+// the row from global memory several times (measured on a GB300, TopK 2048:
+// four rows of 2^20 elements whole, about 6100 candidates each, 654 us; split
+// over clusters of 8 CTAs, 22 us).
+constexpr double kShortMaxCandidates = 4096.0;
+// Longest row the short-row kernel is planned to select whole: beyond it the
+// 2048-element sample holds so few of the row's TopK best that its threshold
+// scatters widely (TopK 512, rows of 2^20: 706 us whole against 476 us on the
+// wide shape; TopK 2048, 2^19: 354 us against 66 us), while 2^18 still wins
+// (TopK 2048, 152 rows: 36.9 us against 45.1 us).
+constexpr int64_t kShortMaxWholeStride = 1 << 18;
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.

@@ -722,9 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   if (r >= p.num_rows) return;
 
   // Set-up: warp 0's lanes initialise the slot barriers and, with contiguous
-  // rows, issue the first row's blind window (sized by max_len, at most a
-  // ring's worth) before anything else; the first length is loaded now, used
-  // once the data is in.
+  // rows, lane 0 issues piece 0 of the first row's blind window (sized by
+  // max_len) before anything else; warp 1 issues the rest of it (up to a ring's
+  // worth) after the barrier, so the seed's piece is not queued behind them.
+  // The first length is loaded now, used once the data is in.
   const int32_t len_raw0 = __ldg(p.lengths + r);
   // thread 0 holds the raw length of the next row, loaded a row ahead of its use
   int32_t nl_raw = (tid == 0 && r + gridDim.x < p.num_rows) ? __ldg(p.lengths + r + gridDim.x) : 0;
@@ -741,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
       s.abort = 0;
       s.key_max = 0;
     }
-    if (bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), 0, blind, 0, false);
+    if (bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), 0, min(blind, 1), 0, false);
   }
   for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
   for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
@@ -754,6 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   }
   __syncthreads();
   int len = clamp_len(p, len_raw0, tid == 0);
+  if (warp == 1 && bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), 1, blind, 0, false);
 
   uint32_t par = 0;  // bit q: parity of the next phase of slot q's barrier
   int S = 0;         // ring slot of the current row's piece 0 (rows follow one another round the ring)
@@ -1228,6 +1230,584 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   }
 }
 
+// ------------------------------------------------------- cluster row split
+//
+// A row split over the C CTAs (C = 2 .. 8) of a thread-block cluster, one row
+// per cluster, for launches with too few rows to fill the GPU (the same
+// single-pass shape; the merge takes the place of the pages' cross-CTA radix
+// histograms). CTA c takes window pieces c, c + C, c + 2 C, ..., a balanced
+// share whatever the length, so each issues its first pieces before the
+// length is read. CTA 0 seeds the threshold from piece 0 as one CTA does and
+// stores it into every CTA; every CTA filters its pieces into its own
+// candidate regions and stores its fine-bin counts into every CTA, so each
+// finds the K-th key's fine bin t on its own, with the same answer, and knows
+// where its winners and bin t entries go; it writes its winners and sends bin
+// t's entries to CTA 0, which ranks them. Three cluster barriers a row after a
+// start barrier (one more when the K-th key lies above the counted bins),
+// taken by every thread of every CTA whatever happened before them, so a CTA
+// that gave up still arrives; no CTA touches another's shared memory after the
+// last one. The exact fallback runs in CTA 0, over the row in global memory.
+
+// Every CTA of the cluster holds every CTA's counts (each CTA stores its own
+// into all of them), so each takes the same decision on its own. The fine-bin
+// counts of each CTA (two buffers: the second for a coarser recount) sit in
+// the seed histogram's space, unused from the seed's end to the exact path.
+struct SmemC : Smem {
+  int c_nc[kMaxCluster];             // candidates of each CTA
+  int c_fl[kMaxCluster];             // each CTA's flags: bit 0 a candidate region overflowed, bit 1 it gave up
+  uint32_t c_mx[kMaxCluster];        // each CTA's largest candidate key
+  uint32_t c_seed[4];                // from rank 0: threshold key; 1: keys above it only; target; 1: gave up
+  int c_dec[7];                      // mode, fine bin t, need (0: bin t whole), bin t's entries, bin shift,
+                                     // this CTA's first output slot and first ranking slot
+};
+static_assert(sizeof(SmemC) <= 227 * 1024, "the cluster kernel's shared memory fits one SM");
+static_assert(2 * kMaxCluster * kTrack <= kBins, "the cluster's fine-bin counts fit the seed histogram");
+
+// Fine-bin count i of CTA c, buffer b.
+__device__ __forceinline__ int* cluster_fc(SmemC& s, int b, int c) {
+  return reinterpret_cast<int*>(s.hseed) + (b * kMaxCluster + c) * kTrack;
+}
+
+constexpr int kModeSelect = 1;  // bin t found: winners out, bin t's entries ranked in rank 0
+constexpr int kModeWide = 2;    // the K-th key lies above the counted bins: count again, coarser
+constexpr int kModeExact = 3;   // the exact fallback in rank 0
+constexpr int kModeAbort = 4;   // a CTA gave up (a copy did not land in time)
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(v));
+  return v;
+}
+
+// The address of the same shared variable in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* ptr, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(ptr)), "r"(rank));
+  return a;
+}
+
+__device__ __forceinline__ void dsmem_st(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// The hardware cluster barrier: completes once every thread of every CTA of
+// the cluster has arrived; shared-memory writes before it (this CTA's own and
+// remote ones) are seen by every thread after it. Warp-uniform.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Warp 0 of each CTA: the K-th key's fine bin from the counts of all C CTAs of
+// the cluster (buffer `buf`, bins of (key - thr_key) >> fsh), into c_dec; every
+// CTA reads the same counts and takes the same decision. A K-th key above the
+// counted bins asks for a recount (when `may_widen`) with the smallest shift
+// that holds the cluster's largest candidate. With bin t found, CTA me's first
+// output slot and first ranking slot follow the winners and bin t entries of
+// CTAs 0 .. me - 1.
+__device__ __forceinline__ void cluster_decide(SmemC& s, int K, int C, int me, int buf, int fsh, bool may_widen,
+                                               uint32_t thr_key) {
+  const int lane = static_cast<int>(lane_id());
+  int c0 = 0, c1 = 0;  // bins 2 lane and 2 lane + 1, over the cluster
+  for (int c = 0; c < C; ++c) {
+    const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, buf, c) + 2 * lane);
+    c0 += v.x;
+    c1 += v.y;
+  }
+  const int n_c = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, lane < C ? static_cast<uint32_t>(s.c_nc[lane]) : 0u));
+  const uint32_t flags = __reduce_or_sync(0xFFFFFFFFu, lane < C ? static_cast<uint32_t>(s.c_fl[lane]) : 0u);
+  const uint32_t cmax = __reduce_max_sync(0xFFFFFFFFu, lane < C ? s.c_mx[lane] : 0u);
+  const int skip = n_c - K;  // the K-th key's bin: the first whose prefix (from bin 0) passes skip
+  const int pair = c0 + c1;
+  int incl = pair;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const int p0 = incl - pair + c0;
+  const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > skip);
+  const int L = hit ? __ffs(hit) - 1 : 0;
+  const bool first = __shfl_sync(0xFFFFFFFFu, p0, L) > skip;
+  const int jt = 2 * L + (first ? 0 : 1);
+  const int cum = first ? __shfl_sync(0xFFFFFFFFu, p0, L) : __shfl_sync(0xFFFFFFFFu, incl, L);
+  const int in_t = first ? __shfl_sync(0xFFFFFFFFu, c0, L) : __shfl_sync(0xFFFFFFFFu, c1, L);
+  const int need = K - (n_c - cum);
+  const bool all_t = need == in_t;
+  const bool base = flags == 0u && n_c >= K;
+  int mode = kModeExact;
+  if (flags & 2u)
+    mode = kModeAbort;
+  else if (base && hit != 0 && (all_t || in_t <= kRank))
+    mode = kModeSelect;
+  else if (base && hit == 0 && may_widen)
+    mode = kModeWide;
+  int fsh2 = fsh;
+  if (mode == kModeWide) {
+    const uint32_t span = cmax - thr_key;
+    while ((span >> fsh2) >= static_cast<uint32_t>(kTrack)) ++fsh2;
+  }
+  // the winners (bins above t, and t when taken whole) and bin t entries of CTAs before this one
+  int ow = 0, os = 0;
+  if (mode == kModeSelect) {
+    for (int c = 0; c < me; ++c) {
+      const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, buf, c) + 2 * lane);
+      const int below = static_cast<int>(__reduce_add_sync(
+          0xFFFFFFFFu, static_cast<uint32_t>((2 * lane <= jt ? v.x : 0) + (2 * lane + 1 <= jt ? v.y : 0))));
+      const int bt = cluster_fc(s, buf, c)[jt];
+      ow += s.c_nc[c] - below + (all_t ? bt : 0);
+      os += all_t ? 0 : bt;
+    }
+  }
+  if (lane == 0) {
+    s.c_dec[0] = mode;
+    s.c_dec[1] = jt;
+    s.c_dec[2] = all_t ? 0 : need;
+    s.c_dec[3] = in_t;
+    s.c_dec[4] = fsh2;
+    s.c_dec[5] = ow;
+    s.c_dec[6] = os;
+  }
+}
+
+// Warp 0: this CTA's fine-bin counts (s.ftot) into buffer `buf` of every CTA of
+// the cluster, and with `all` its candidate count, flags and largest key.
+__device__ __forceinline__ void cluster_push_counts(SmemC& s, int C, int me, int buf, bool all, int n_c, int flags,
+                                                    uint32_t cmax) {
+  const int lane = static_cast<int>(lane_id());
+  const int2 v = *reinterpret_cast<const int2*>(&s.ftot[2 * lane]);
+  for (int c = 0; c < C; ++c) {
+    const uint32_t a = dsmem_addr(cluster_fc(s, buf, me) + 2 * lane, static_cast<uint32_t>(c));
+    dsmem_st(a, static_cast<uint32_t>(v.x));
+    dsmem_st(a + 4u, static_cast<uint32_t>(v.y));
+    if (all && lane == 0) {
+      dsmem_st(dsmem_addr(&s.c_nc[me], static_cast<uint32_t>(c)), static_cast<uint32_t>(n_c));
+      dsmem_st(dsmem_addr(&s.c_fl[me], static_cast<uint32_t>(c)), static_cast<uint32_t>(flags));
+      dsmem_st(dsmem_addr(&s.c_mx[me], static_cast<uint32_t>(c)), cmax);
+    }
+  }
+}
+
+// Ranks bin t's in_t entries (s.rk, s.ri) and writes the first `need` of them
+// at o[K - need ...]: at once up to kRankDirect entries; more are first split
+// on the next 8 bits of key - thr_key (shift fsh - 8), the sub-bins above the
+// one holding the need-th taken whole and that one ranked. Block-wide; uses
+// s.hsub (zero on entry), s.n_win, s.n_bt and the candidate slots.
+__device__ __forceinline__ void finish_bin_t(Smem& s, int in_t, int need, uint32_t thr_key, int fsh, int32_t* o,
+                                             int K) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = static_cast<int>(lane_id());
+  const int c4 = (in_t + 3) & ~3;
+  if (tid >= in_t && tid < c4) {  // padding never beats a real entry
+    s.rk[tid] = 0u;
+    s.ri[tid] = 0x7FFFFFFF;
+  }
+  __syncthreads();
+  if (in_t <= kRankDirect) {
+    rank_out(s.rk, s.ri, in_t, c4, need, o + (K - need));
+    return;
+  }
+  if (tid < in_t) atomicAdd(&s.hsub[((s.rk[tid] - thr_key) >> (fsh - 8)) & 0xFFu], 1u);
+  __syncthreads();
+  if (warp == 0) {
+    int above_b;
+    const int b = warp_find256(s.hsub, need, above_b);
+    if (lane == 0) {
+      s.sub_b = b;
+      s.sub_above = above_b;
+      s.n_win = 0;
+      s.n_bt = 0;
+    }
+  }
+  __syncthreads();
+  const int b = s.sub_b;
+  const int sab = s.sub_above;
+  const int in_b = static_cast<int>(s.hsub[b]);
+  if (tid < in_t) {
+    const uint32_t kj = s.rk[tid];
+    const int32_t ij = s.ri[tid];
+    const int d = static_cast<int>(((kj - thr_key) >> (fsh - 8)) & 0xFFu);
+    if (d > b) {
+      o[K - need + atomicAdd(&s.n_win, 1)] = ij;
+    } else if (d == b) {
+      const int at = atomicAdd(&s.n_bt, 1);
+      s.ckey[at] = kj;
+      s.cidx[at] = ij;
+    }
+  }
+  const int c4b = (in_b + 3) & ~3;
+  if (tid >= in_b && tid < c4b) {
+    s.ckey[tid] = 0u;
+    s.cidx[tid] = 0x7FFFFFFF;
+  }
+  __syncthreads();
+  rank_out(s.ckey, s.cidx, in_b, c4b, need - sab, o + (K - need + sab));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  SmemC& s = *reinterpret_cast<SmemC*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int lane = static_cast<int>(lane_id());
+  const int warp = tid >> 5;
+  const uint32_t lt = lanemask_lt();
+  const int K = p.topk;
+  const int C = p.G;
+  const int me = static_cast<int>(cluster_rank());
+  const int64_t r = blockIdx.x / C;
+  if (r >= p.num_rows) return;  // the whole cluster: its CTAs share the row
+
+  // Set-up: this CTA's first pieces of the blind window (sized by max_len) go
+  // out before the length is read, local piece 0 first and the rest (by warp
+  // 1) after the barrier; local piece i (window piece me + C i) sits in slot
+  // i % kRing.
+  const int32_t len_raw = __ldg(p.lengths + r);
+  const Win wmax = make_win(p, r, static_cast<int>(p.max_len));
+  const int blind = min(wmax.np > me ? (wmax.np - me + C - 1) / C : 0, kRing);
+  if (warp == 0) {
+    if (lane < kRing) {
+      mbar_init(&s.bar[lane], 1u);
+      fence_mbar_init();
+      s.pdone[lane] = 0;
+      s.slot_issues[lane] = 0;
+    }
+    if (lane == 0) s.key_max = 0;
+    if (lane == 0 && blind > 0) issue_piece(s, wmax, me, 0, false);
+  }
+  if (me == 0)
+    for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
+  for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
+  if (tid < 256) s.hsub[tid] = 0;
+  if (tid < kTrack) s.ftot[tid] = 0;
+  if (tid == 0) {
+    s.n_win = 0;
+    s.n_bt = 0;
+    s.cmax = 0;
+  }
+  __syncthreads();
+  const int len = clamp_len(p, len_raw, tid == 0 && me == 0);
+  if (warp == 1 && lane >= 1 && lane < blind) issue_piece(s, wmax, me + C * lane, lane, false);
+  const Win w = make_win(p, r, len);
+  int32_t* o = p.out + r * static_cast<int64_t>(K);
+  const int npl = w.np > me ? (w.np - me + C - 1) / C : 0;  // this CTA's pieces of the window
+  bool aborted = false;
+  bool drain = false;  // pieces may still be in flight at the end: wait for every slot's last copy
+  if (w.nwin == 0) {
+    // every CTA of the cluster reads the same length: none takes a cluster barrier
+    if (me == 0)
+      for (int j = tid; j < K; j += kThreads) o[j] = (j < len) ? j : -1;
+  } else {
+    // every CTA of the cluster is running once this barrier's phase completes:
+    // a CTA waits on it before its first access to another CTA's shared memory
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    // ---- seed (rank 0): piece 0's top 12 key bits, as one CTA seeds a row; the
+    // other CTAs' pieces land meanwhile
+    const int n_seed = min(len, kSeed - w.mis);
+    int wc = 0;  // this warp's candidates
+    bool ok = true;
+    uint32_t seed_key = 0;  // rank 0: the threshold key found
+    if (me == 0) {
+      int target = K;
+      if (warp == 0 && n_seed < len) {
+        const float mu = static_cast<float>(K) * static_cast<float>(n_seed) / static_cast<float>(len);
+        target = max(1, static_cast<int>(ceilf(mu + 3.0f * sqrtf(mu) + 2.0f)));
+      }
+      target = min(target, n_seed);
+      ok = piece_ready(s, 0, 0u, p.timeout_ns);
+      const int seed_hi = min(kSeed, w.nwin);
+      uint32_t kmax = 0;
+      for (int i = tid; i < seed_hi; i += kThreads) {
+        const int e = i - w.mis;
+        if (e >= 0 && e < len) {
+          const uint32_t key = fkey(s.row[i]);
+          kmax = max(kmax, key);
+          atomicAdd(&s.hseed[key >> 20], 1u);
+        }
+      }
+      kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+      if (lane == 0 && kmax) atomicMax(&s.key_max, kmax);
+      if (sync_or(!ok)) {
+        aborted = true;
+      } else {
+        if (warp == 0) {
+          int t0, above0;
+          warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
+          const int c0 = static_cast<int>(s.hseed[t0]);
+          const int need_in = target - above0;
+          // crowded: the seed's projection over the row overflows the cluster's
+          // candidate regions (heavy ties); wide: refine inside the seed bin
+          const int at_or_above = above0 + c0;
+          const bool crowded = n_seed >= K && at_or_above >= K &&
+                               static_cast<int64_t>(at_or_above) * len > (3ll * kCand / 4) * C * n_seed;
+          const bool refine = !crowded && c0 - need_in > max(target / 4, 16);
+          if (lane == 0) {
+            s.target = target;
+            s.t0 = t0;
+            s.crowded = crowded ? 1 : 0;
+            s.refine = refine ? 1 : 0;
+            s.need_in = need_in;
+            s.thr_key = static_cast<uint32_t>(t0) << 20;
+          }
+        }
+        __syncthreads();
+        if (s.refine) {
+          const uint32_t t0 = static_cast<uint32_t>(s.t0);
+          for (int i = tid; i < seed_hi; i += kThreads) {
+            const int e = i - w.mis;
+            if (e >= 0 && e < len) {
+              const uint32_t key = fkey(s.row[i]);
+              if ((key >> 20) == t0) atomicAdd(&s.hsub[(key >> 12) & 0xFFu], 1u);
+            }
+          }
+          __syncthreads();
+          if (warp == 0) {
+            int above_b;
+            const int b = warp_find256(s.hsub, s.need_in, above_b);
+            if (lane == 0) s.thr_key = (t0 << 20) | (static_cast<uint32_t>(b) << 12);
+          }
+          __syncthreads();
+          if (tid < 256) s.hsub[tid] = 0;  // clear again for the ranking (read after later barriers)
+        }
+        seed_key = s.thr_key;
+        if (s.crowded) seed_key = crowded_seed(s, 0, w.mis, n_seed, len, K, wc);  // every thread gets T
+      }
+    }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    if (me == 0 && tid < C) {
+      // the seed into every CTA of the cluster (thread c: CTA c)
+      const uint32_t v[4] = {aborted ? 0u : seed_key, aborted ? 0u : static_cast<uint32_t>(s.crowded),
+                             aborted ? 0u : static_cast<uint32_t>(s.target), aborted ? 1u : 0u};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dsmem_st(dsmem_addr(&s.c_seed[k], static_cast<uint32_t>(tid)), v[k]);
+    }
+    cluster_sync_all();  // the seed is out
+    const bool seed_ok = s.c_seed[3] == 0u;
+    drain = !seed_ok;  // this CTA's pieces were issued but are not read
+    const uint32_t thr_key = s.c_seed[0];
+    const float thr = key_floor_value(s.c_seed[1] ? thr_key + 1u : thr_key);  // crowded: keys above T only
+    const int base = warp * kRegion;
+    int* my_bins = s.wbin[warp];
+    uint32_t kmx = 0;  // this lane's largest candidate key
+    if (seed_ok) {
+      // ---- filter this CTA's pieces: tasks of 128 F window elements, F chosen as
+      // one CTA chooses it for its share; lane l takes float4s l, l + 32, ... of a
+      // task. Local piece i hands its slot to local piece i + kRing once its
+      // tasks are done.
+      const int target = static_cast<int>(s.c_seed[2]);
+      const int nvec = w.nwin >> 2;
+      int F = 8;
+      while (F > 1 && (static_cast<int64_t>(128 * F) * target > static_cast<int64_t>(kTaskSurvivors) * n_seed ||
+                       npl * kPiece < kMinTasks * 128 * F))
+        F >>= 1;
+      const int tsz = 128 * F;
+      const int tpp = kPiece / tsz;  // tasks per piece
+      int ntask = 0;
+      if (npl > 0) {
+        const int j_last = me + C * (npl - 1);
+        const int size_last = min(kPiece, w.nwin - j_last * kPiece);  // only the window's last piece is short
+        ntask = (npl - 1) * tpp + (size_last + tsz - 1) / tsz;
+      }
+#pragma unroll 1
+      for (int task = warp; task < ntask; task += kWarps) {
+        const int jl = task / tpp;             // local piece
+        const int j = me + C * jl;             // window piece
+        const int q = jl % kRing;              // its slot
+        if (!piece_ready(s, q, static_cast<uint32_t>(jl / kRing) & 1u, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const int off = (task % tpp) * tsz;  // the task's first element in the piece
+        const int sb = q * kPiece + off;
+        const int v0 = (j * kPiece + off) >> 2;  // its first float4 in the window
+        uint32_t m = 0;
+        if (v0 + 32 * F <= nvec && 4 * v0 - w.mis >= 0 && 4 * v0 + tsz - w.mis <= len) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (i < F) {
+              const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
+              m |= ((f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                    (f.w >= thr ? 8u : 0u)) << (4 * i);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int v = v0 + lane + 32 * i;
+            if (i < F && v < nvec) {
+              const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
+              uint32_t b = (f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                           (f.w >= thr ? 8u : 0u);
+              const int e0 = 4 * v - w.mis;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                if (e0 + c < 0 || e0 + c >= len) b &= ~(1u << c);
+              m |= b << (4 * i);
+            }
+          }
+        }
+        const int c = __popc(m);
+        uint32_t qb[6];
+#pragma unroll
+        for (int bit = 0; bit < 6; ++bit) qb[bit] = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+        int tot = 0, pre = 0;
+#pragma unroll
+        for (int bit = 0; bit < 6; ++bit) {
+          tot += __popc(qb[bit]) << bit;
+          pre += __popc(qb[bit] & lt) << bit;
+        }
+        if (tot > 0) {
+          if (wc + tot <= kRegion) {
+            int at = base + wc + pre;
+            while (m) {
+              const int jb = __ffs(m) - 1;
+              m &= m - 1;
+              s.cidx[at++] = 4 * (lane + 32 * (jb >> 2)) + (jb & 3);
+            }
+            __syncwarp();
+#pragma unroll 1
+            for (int e0 = 0; e0 < tot; e0 += 32) {
+              const int e = e0 + lane;
+              if (e < tot) {
+                const int pos = s.cidx[base + wc + e];
+                const uint32_t key = fkey(s.row[sb + pos]);
+                kmx = max(kmx, key);
+                s.ckey[base + wc + e] = key;
+                s.cidx[base + wc + e] = j * kPiece + off + pos - w.mis;
+                const uint32_t d = (key - thr_key) >> kFine;
+                if (d < kTrack) atomicAdd(&my_bins[d], 1);
+              }
+            }
+            __syncwarp();
+          }
+          wc += tot;
+        }
+        if (jl + kRing < npl) {
+          __syncwarp();  // every lane's reads of the slot come before the hand-over
+          if (lane == 0 && atom_add_acq_rel_cta(&s.pdone[q], 1) == tpp - 1) {
+            s.pdone[q] = 0;
+            issue_piece(s, w, me + C * (jl + kRing), q, true);
+          }
+        }
+      }
+    }
+    if (lane == 0) s.wcnt[warp] = wc;
+    if (wc > 0) {
+      const int2 v2 = *reinterpret_cast<const int2*>(&my_bins[2 * lane]);
+      if (v2.x) atomicAdd(&s.ftot[2 * lane], v2.x);
+      if (v2.y) atomicAdd(&s.ftot[2 * lane + 1], v2.y);
+    }
+    kmx = __reduce_max_sync(0xFFFFFFFFu, kmx);
+    if (lane == 0 && kmx) atomicMax(&s.cmax, kmx);
+    if (sync_or(!ok)) aborted = true;
+    // ---- this CTA's counts into every CTA of the cluster (warp 0; lane l: warp l's
+    // count, fine bins 2l and 2l + 1); then each CTA finds bin t on its own
+    if (warp == 0) {
+      const int n_l = lane < kWarps ? s.wcnt[lane] : 0;
+      const bool over = __any_sync(0xFFFFFFFFu, n_l > kRegion);
+      const int n_c = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(n_l)));
+      cluster_push_counts(s, C, me, 0, true, n_c, (over ? 1 : 0) | (aborted ? 2 : 0), s.cmax);
+    }
+    cluster_sync_all();  // every CTA's counts are in every CTA
+    if (warp == 0) cluster_decide(s, K, C, me, 0, kFine, true, thr_key);
+    __syncthreads();
+    int mode = s.c_dec[0];
+    int fsh = kFine;  // fine bin of a candidate: (key - thr_key) >> fsh
+    if (mode == kModeWide) {
+      // the K-th key lies above the 64 bins counted: every CTA counts its
+      // candidates again in bins wide enough for the cluster's largest key
+      fsh = s.c_dec[4];
+      const int cnt_w = s.wcnt[warp];  // at most kRegion: no overflow here
+      *reinterpret_cast<int2*>(&my_bins[2 * lane]) = make_int2(0, 0);
+      if (tid < kTrack) s.ftot[tid] = 0;
+      __syncthreads();
+      for (int e = lane; e < cnt_w; e += 32) atomicAdd(&my_bins[(s.ckey[base + e] - thr_key) >> fsh], 1);
+      __syncwarp();
+      if (cnt_w > 0) {
+        const int2 v2 = *reinterpret_cast<const int2*>(&my_bins[2 * lane]);
+        if (v2.x) atomicAdd(&s.ftot[2 * lane], v2.x);
+        if (v2.y) atomicAdd(&s.ftot[2 * lane + 1], v2.y);
+      }
+      __syncthreads();
+      if (warp == 0) cluster_push_counts(s, C, me, 1, false, 0, 0, 0u);
+      cluster_sync_all();  // every CTA's recount is in every CTA
+      if (warp == 0) cluster_decide(s, K, C, me, 1, fsh, false, thr_key);
+      __syncthreads();
+      mode = s.c_dec[0];
+    }
+    const int jt = s.c_dec[1];
+    const int need = s.c_dec[2];
+    const bool all_t = need == 0;
+    if (mode == kModeSelect) {
+      // ---- winners above bin t out, bin t's entries into rank 0's ranking slots,
+      // each CTA from the first slots the decision gave it
+      const int cnt = s.wcnt[warp];  // at most kRegion here
+      const int2 b2 = *reinterpret_cast<const int2*>(&my_bins[2 * lane]);
+      const int below = static_cast<int>(__reduce_add_sync(
+          0xFFFFFFFFu, static_cast<uint32_t>((2 * lane <= jt ? b2.x : 0) + (2 * lane + 1 <= jt ? b2.y : 0))));
+      int bt = my_bins[jt];
+      int nw = cnt - below;
+      if (all_t) {
+        nw += bt;
+        bt = 0;
+      }
+      // this CTA's output range and ranking slots start where the decision put them
+      int ow = 0, os = 0;
+      if (lane == 0) {
+        if (nw) ow = atomicAdd(&s.n_win, nw);
+        if (bt) os = atomicAdd(&s.n_bt, bt);
+      }
+      ow = s.c_dec[5] + __shfl_sync(0xFFFFFFFFu, ow, 0);
+      os = s.c_dec[6] + __shfl_sync(0xFFFFFFFFu, os, 0);
+      const uint32_t rk0 = dsmem_addr(&s.rk[0], 0u);
+      const uint32_t ri0 = dsmem_addr(&s.ri[0], 0u);
+#pragma unroll 1
+      for (int e0 = 0; e0 < cnt; e0 += 32) {
+        const int e = e0 + lane;
+        uint32_t key = 0;
+        int32_t idx = 0;
+        int d = -1;
+        if (e < cnt) {
+          key = s.ckey[base + e];
+          idx = s.cidx[base + e];
+          d = static_cast<int>((key - thr_key) >> fsh);
+        }
+        const bool win = d > jt || (all_t && d == jt);
+        const bool inb = !all_t && d == jt;
+        const uint32_t bw = __ballot_sync(0xFFFFFFFFu, win);
+        if (win) o[ow + __popc(bw & lt)] = idx;
+        ow += __popc(bw);
+        const uint32_t bb = __ballot_sync(0xFFFFFFFFu, inb);
+        if (inb) {
+          const uint32_t at = static_cast<uint32_t>(os + __popc(bb & lt));
+          dsmem_st(rk0 + 4u * at, key);
+          dsmem_st(ri0 + 4u * at, static_cast<uint32_t>(idx));
+        }
+        os += __popc(bb);
+      }
+    }
+    cluster_sync_all();  // B4: bin t's entries are in rank 0; no CTA touches another's memory from here on
+    if (me == 0) {
+      if (mode == kModeSelect && !all_t)
+        finish_bin_t(s, s.c_dec[3], need, thr_key, fsh, o, K);
+      else if (mode == kModeExact)
+        fallback_select(s, p, r, w, Src{w.rowp - w.mis, 1, -1, len});
+    }
+  }
+  // the blind pieces past this CTA's share land before it leaves (lane q: slot q)
+  drain = drain || aborted;
+  if (!drain && warp == 0 && lane >= npl && lane < blind) wait_piece(&s.bar[lane], 0u, p.timeout_ns, nullptr);
+  if (drain && tid == 0) {
+    // a piece did not land in time (flagged), or the seed's did not: wait
+    // (bounded) for the last copy issued into every slot before the CTA leaves
+    if (aborted) atomicOr(p.status, 0x4u);
+    for (int q = 0; q < kRing; ++q) {
+      const int n = s.slot_issues[q];
+      if (n > 0) wait_piece(&s.bar[q], static_cast<uint32_t>(n - 1) & 1u, p.timeout_ns, nullptr);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 int kernel_threads() { return kThreads; }
@@ -1235,28 +1815,56 @@ int kernel_threads() { return kThreads; }
 size_t kernel_smem_bytes() { return sizeof(Smem); }
 
 cudaError_t kernel_configure() {
-  return cudaFuncSetAttribute(topk_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(Smem)));
+  const cudaError_t e = cudaFuncSetAttribute(topk_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(sizeof(Smem)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(topk_short_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sizeof(SmemC)));
 }
 
 cudaError_t kernel_occupancy(int* ctas_per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, topk_short_kernel, kThreads, sizeof(Smem));
 }
 
-cudaError_t kernel_max_clusters(int, int* clusters) {
-  *clusters = 0;
-  return cudaSuccess;
+// Clusters of `cluster_size` CTAs of the cluster kernel that can be resident at once.
+cudaError_t kernel_max_clusters(int cluster_size, int* clusters) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster_size));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(SmemC);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_size);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(clusters, topk_short_cluster_kernel, &cfg);
 }
 
+// G = 1: the whole-row kernel over `grid` persistent CTAs. G > 1 (contiguous
+// rows only): the cluster kernel, clusters of G CTAs, one row each (grid =
+// num_rows * G).
 cudaError_t launch_topk(const Params& p, int grid, bool, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = sizeof(Smem);
   cfg.stream = stream;
-  cfg.attrs = nullptr;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, topk_short_kernel, p);
+  if (p.G <= 1) {
+    cfg.dynamicSmemBytes = sizeof(Smem);
+    return cudaLaunchKernelEx(&cfg, topk_short_kernel, p);
+  }
+  if (p.G > kMaxCluster || p.col_stride != 1 || grid % p.G != 0) return cudaErrorInvalidValue;
+  cfg.dynamicSmemBytes = sizeof(SmemC);
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.G);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_short_cluster_kernel, p);
 }
 
 }  // namespace shortrow

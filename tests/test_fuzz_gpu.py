@@ -117,3 +117,31 @@ def test_random_short_rows_match_oracle(rn, seed):
     got = rn.run(x, lengths, topk, options=rn.options(**opts))
     assert_matches_oracle(x, lengths, got, topk,
                           label=f"short seed {seed}: {x.shape[0]} rows x {x.shape[1]}, K {topk}, {opts}")
+
+
+CLUSTER_CASES = 40
+
+
+def _cluster_case(seed: int):
+    """Rows split over a thread-block cluster of the short-row kernel (2 to 8 CTAs, one row per
+    cluster): lengths from below TopK to past the ring of every CTA, every value mix, TopK up to
+    4096, row starts off the 16-byte grid."""
+    rng = np.random.default_rng(3_000_017 * seed + 11)
+    G = int(rng.integers(2, 9))
+    topk = int(rng.choice([int(rng.integers(1, 65)), 512, 1024, 2048, int(rng.integers(1, 4097))]))
+    stride = int(rng.choice([int(rng.integers(1, 8000)), int(rng.integers(8000, 70000)),
+                             int(rng.integers(70000, 300000))]))
+    num_rows = int(rng.integers(1, min(40, MAX_ELEMENTS // stride) + 1))
+    x = np.stack([_row(rng, stride) for _ in range(num_rows)])
+    lengths = rng.integers(0, stride + 1, size=num_rows)
+    lengths[rng.random(num_rows) < 0.3] = stride
+    return x, lengths.astype(np.int32), topk, int(rng.integers(0, 4)), dict(shape=4, force_ctas_per_group=G)
+
+
+@pytest.mark.parametrize("seed", range(CLUSTER_CASES))
+def test_random_cluster_split_rows_match_oracle(rn, seed):
+    x, lengths, topk, shift, opts = _cluster_case(seed)
+    got = rn.run(x, lengths, topk, options=rn.options(**opts), pad_front=shift)
+    assert_matches_oracle(x, lengths, got, topk,
+                          label=f"cluster seed {seed}: {x.shape[0]} rows x {x.shape[1]}, K {topk}, shift {shift}, "
+                                f"{opts}")

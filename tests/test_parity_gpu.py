@@ -41,7 +41,8 @@ def test_workloads_small_other_shapes(rn, name, rows, shape):
 
 
 @pytest.mark.parametrize("topk", [1, 7, 100, 1000, 2047, 2049, 3000, 4096])
-@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (0, 0, 2), (0, 0, 3), (3, 1, 0), (4, 2, 0), (0, 0, 4)])
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (0, 0, 2), (0, 0, 3), (3, 1, 0), (4, 2, 0), (0, 0, 4),
+                                           (3, 0, 4)])
 def test_runtime_topk(rn, topk, G, merge, shape):
     """TopK outside the pages' 512 / 1024 / 2048, on every path (paired and small shapes up to 2048)."""
     if shape in (2, 3) and topk > 2048:
@@ -162,6 +163,18 @@ def test_workloads_forced_split(rn, name, rows, G, merge):
     assert rn.workspace_clean()
 
 
+@pytest.mark.parametrize("G", [2, 3, 4, 6, 8])
+@pytest.mark.parametrize("name,rows", [("decode_small", 8), ("decode_batch", 6), ("long_coop", 3), ("mtp", 4),
+                                       ("prefill", 4)])
+def test_workloads_short_row_cluster_split(rn, name, rows, G):
+    """Each row split over a thread-block cluster of G short-row CTAs (CTA c takes window
+    pieces c, c + G, ...), merged in the cluster's shared memory."""
+    w = workloads.make(name, rows)
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=4, force_ctas_per_group=G))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} short-row cluster G={G}")
+    assert rn.workspace_clean()
+
+
 @pytest.mark.parametrize("name", workloads.NAMES)
 def test_workloads_full_size(rn, name):
     """Every row of the full workload, in the launch configuration the benchmark times."""
@@ -198,7 +211,7 @@ def _edge_rows(S: int, K: int, rng) -> tuple[np.ndarray, np.ndarray]:
 @pytest.mark.parametrize("topk", [512, 1024, 2048])
 @pytest.mark.parametrize("S", [4096, 9001, 40000])
 @pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 1), (0, 0, 2), (0, 0, 3), (4, 1, 0), (4, 2, 0), (8, 2, 0),
-                                           (0, 0, 4)])
+                                           (0, 0, 4), (2, 0, 4), (5, 0, 4), (8, 0, 4)])
 def test_edge_cases(rn, topk, S, G, merge, shape):
     # with G = 8 and K = 2048 the all-equal row keeps 8 x K candidates at one
     # key, more than the leader's buffer: the cluster merge hands over to the
@@ -234,8 +247,8 @@ def _kth_bin_size(row: np.ndarray, K: int) -> int:
 
 
 @pytest.mark.parametrize("S", [30000, 100000])
-@pytest.mark.parametrize("shape", [0, 4])
-def test_large_kth_key_bin(rn, S, shape):
+@pytest.mark.parametrize("shape,G", [(0, 0), (4, 0), (4, 2), (4, 6)])
+def test_large_kth_key_bin(rn, S, shape, G):
     """Hundreds of elements share the K-th key's bin (a dense cluster): the selection
     splits that bin further before ranking; with equal keys inside it, by index."""
     rng = np.random.default_rng(S + shape)
@@ -244,14 +257,14 @@ def test_large_kth_key_bin(rn, S, shape):
     lens = np.full(x.shape[0], S, np.int32)
     sizes = [_kth_bin_size(r, K) for r in x]
     assert any(192 < n <= 512 for n in sizes), sizes  # the data reach the split
-    got = rn.run(x, lens, K, options=rn.options(shape=shape))
-    assert_matches_oracle(x, lens, got, K, label=f"dense cluster S={S} shape={shape} bins {sizes}")
+    got = rn.run(x, lens, K, options=rn.options(shape=shape, force_ctas_per_group=G))
+    assert_matches_oracle(x, lens, got, K, label=f"dense cluster S={S} shape={shape} G={G} bins {sizes}")
     assert rn.workspace_clean()
 
 
 @pytest.mark.parametrize("S,K", [(4096, 1536), (4096, 2048), (6000, 2800), (8192, 4096), (40000, 4096)])
-@pytest.mark.parametrize("shape", [0, 4])
-def test_kth_key_far_from_the_threshold(rn, S, K, shape):
+@pytest.mark.parametrize("shape,G", [(0, 0), (4, 0), (4, 3)])
+def test_kth_key_far_from_the_threshold(rn, S, K, shape, G):
     """The K-th key lies many binades above the seed's threshold: a selected fraction
     near one half of N(0,1) rows (the K-th value near zero), and rows whose values near
     the K-th span tiny magnitudes of both signs."""
@@ -263,8 +276,8 @@ def test_kth_key_far_from_the_threshold(rn, S, K, shape):
     rows.append(r)
     x = np.stack(rows)
     lens = np.full(x.shape[0], S, np.int32)
-    got = rn.run(x, lens, K, options=rn.options(shape=shape))
-    assert_matches_oracle(x, lens, got, K, label=f"far K-th S={S} K={K} shape={shape}")
+    got = rn.run(x, lens, K, options=rn.options(shape=shape, force_ctas_per_group=G))
+    assert_matches_oracle(x, lens, got, K, label=f"far K-th S={S} K={K} shape={shape} G={G}")
     assert rn.workspace_clean()
 
 
@@ -287,9 +300,9 @@ def test_unaligned_rows(rn, shift, stride_delta):
     S = 20000 + stride_delta
     x = rng.standard_normal((5, S)).astype(np.float32)
     lens = np.array([S, S - 1, 3000, 12345, 2049], np.int32)
-    for G in (1, 2):
-        got = rn.run(x, lens, 2048, pad_front=shift, options=rn.options(force_ctas_per_group=G))
-        assert_matches_oracle(x, lens, got, 2048, label=f"shift={shift} S={S} G={G}")
+    for G, shape in ((1, 0), (2, 0), (3, 4)):
+        got = rn.run(x, lens, 2048, pad_front=shift, options=rn.options(force_ctas_per_group=G, shape=shape))
+        assert_matches_oracle(x, lens, got, 2048, label=f"shift={shift} S={S} G={G} shape={shape}")
 
 
 def test_lengths_are_clamped_and_flagged(rn):

@@ -14,9 +14,10 @@ def _built():
 
 
 def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, pair=(0, 0), small=(0, 0),
-          short=(0, 0)):
-    """A made-up device; clusters maps a cluster size to its co-resident count (none by default);
-    pair, small and short are (shared memory, CTAs per SM) of those shapes (absent by default)."""
+          short=(0, 0), short_clusters=None):
+    """A made-up device; clusters (short_clusters) maps a cluster size to its co-resident count for
+    the wide shape (the short-row kernel's cluster form), none by default; pair, small and short are
+    (shared memory, CTAs per SM) of those shapes (absent by default)."""
     p = sar.TopkDeviceProps()
     p.num_sms, p.ctas_per_sm, p.smem_per_cta, p.max_smem_optin = num_sms, occ, smem, optin
     for c, n in (clusters or {}).items():
@@ -24,6 +25,8 @@ def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, 
     p.pair_smem_per_cta, p.pair_ctas_per_sm = pair
     p.small_smem_per_cta, p.small_ctas_per_sm = small
     p.short_smem_per_cta, p.short_ctas_per_sm = short
+    for c, n in (short_clusters or {}).items():
+        p.short_cluster_groups[c] = n
     return p
 
 
@@ -301,7 +304,16 @@ def test_short_row_kernel():
     assert rc == 0 and pl.shape == 4 and pl.grid == 3
     rc, pl = plan(gb, 10, 400000, shape=4)
     assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1
-    assert plan(gb, 10, 30000, shape=4, force_ctas_per_group=2)[0] == sar.TOPK_ERR_INVALID_ARG
+    # a forced split of the short-row kernel: one row per cluster, merged in the cluster
+    assert plan(gb, 10, 30000, shape=4, force_ctas_per_group=2)[0] == sar.TOPK_ERR_PLAN  # no clusters here
+    gbc = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT,
+                short_clusters=gb300_clusters())
+    for rows, g in ((10, 2), (16, 6), (300, 8), (1, 3)):
+        rc, pl = plan(gbc, rows, 30000, shape=4, force_ctas_per_group=g)
+        assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == g and pl.cluster and not pl.cooperative
+        assert pl.num_groups == rows and pl.grid == rows * g and pl.threads == 1024
+    assert plan(gbc, 10, 30000, shape=4, force_ctas_per_group=9)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gbc, 10, 30000, shape=4, force_ctas_per_group=2, merge=1)[0] == sar.TOPK_ERR_PLAN
     rc, pl = plan(gb, 10, 30000, force_ctas_per_group=2)
     assert rc == 0 and pl.shape == 1 and pl.ctas_per_group == 2
     # the wide shape forced: the split rule of that kernel applies
@@ -313,3 +325,55 @@ def test_short_row_kernel():
     rc, pl = plan(gb10, 8, 4096, topk=512)
     assert rc == 0 and pl.shape == 3
     assert plan(gb10, 8, 4096, topk=512, shape=4)[0] == sar.TOPK_ERR_PLAN
+
+
+def test_short_row_cluster_split():
+    """Few rows of 65536 up to 2^20 elements are split over a thread-block cluster of the
+    short-row kernel: the largest size up to 8 with rows x size within the SMs whose clusters
+    are all resident at once (the crossover that bench.py --sweep measured on a GB300)."""
+    gb = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT,
+               short_clusters=gb300_clusters())
+    for rows, stride, k, g in ((16, 131072, 2048, 6),   # long_coop: 8 and 7 hold only 15 clusters
+                               (64, 163840, 1024, 2),   # mtp
+                               (4, 65536, 2048, 8), (16, 65536, 2048, 6), (1, 500000, 512, 8),
+                               (76, 131072, 2048, 2), (28, 100000, 2048, 5), (30, 100000, 2048, 4), (40, 100000, 2048, 3)):
+        rc, pl = plan(gb, rows, stride, topk=k)
+        assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == g and pl.cluster, (rows, stride, k, pl.ctas_per_group)
+        assert pl.grid == rows * g and pl.num_groups == rows and not pl.cooperative and pl.threads == 1024
+    # whole rows: shorter rows, enough rows for every SM, very long rows
+    for rows, stride, k in ((64, 32768, 2048), (8, 4096, 512), (16, 65535, 2048), (77, 131072, 2048),
+                            (4096, 65536, 2048)):
+        rc, pl = plan(gb, rows, stride, topk=k)
+        assert rc == 0 and pl.ctas_per_group == 1 and not pl.cluster, (rows, stride, k)
+    # very long rows: split over clusters while each CTA's expected candidates (about 8400 on
+    # rows of 2^21 at TopK 2048) stay within 4096, else the wide shape, split or whole
+    rc, pl = plan(gb, 16, 1 << 21)
+    assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 6 and pl.cluster
+    rc, pl = plan(gb, 64, 1 << 21)
+    assert rc == 0 and pl.shape == 1 and pl.ctas_per_group == 2
+    rc, pl = plan(gb, 64, 1 << 20)
+    assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 2 and pl.cluster
+    rc, pl = plan(gb, 128, 1 << 20)
+    assert rc == 0 and pl.shape == 1 and pl.ctas_per_group == 1
+    rc, pl = plan(gb, 128, 1 << 18)
+    assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1
+    # whole rows beyond 2^18 elements, or whose expected candidates exceed 4096 (TopK 4096 of
+    # 65536), take the wide shape; split over clusters they stay on the short-row kernel
+    for rows, stride, k, shape, g in ((128, 1 << 20, 512, 1, 1), (128, 1 << 19, 512, 1, 1), (128, 65536, 4096, 1, 1),
+                                      (64, 65536, 4096, 4, 2), (64, 1 << 19, 4096, 4, 2), (16, 1 << 21, 512, 4, 6)):
+        rc, pl = plan(gb, rows, stride, topk=k)
+        assert rc == 0 and pl.shape == shape and pl.ctas_per_group == g, (rows, stride, k, pl.shape, pl.ctas_per_group)
+    # the short-row kernel forced: the same rule; one CTA per row forced, or the workspace merge
+    # asked for: whole rows
+    rc, pl = plan(gb, 16, 131072, shape=4)
+    assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 6
+    for opt in (dict(force_ctas_per_group=1), dict(merge=1), dict(shape=4, force_ctas_per_group=1)):
+        rc, pl = plan(gb, 16, 131072, **opt)
+        assert rc == 0 and pl.ctas_per_group == 1 and not pl.cluster, opt
+    # a cap on the CTAs bounds rows x size
+    rc, pl = plan(gb, 16, 131072, max_ctas=64)
+    assert rc == 0 and pl.ctas_per_group == 4 and pl.grid == 64
+    # no clusters on the device: whole rows
+    rc, pl = plan(props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT),
+                  16, 131072)
+    assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1
