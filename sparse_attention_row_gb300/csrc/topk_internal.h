@@ -51,13 +51,14 @@ constexpr int64_t kShortSeedLen = 2048;  // elements it samples for its threshol
 // against 41.1 for the other kernel's split), and loses on shorter rows (16384:
 // 14.3 against 12.3), where its merge costs more than the streaming it shares.
 constexpr int64_t kShortClusterStride = 65536;
-// The short-row kernel samples 2048 elements for its threshold, so on very long
+// The short-row kernel samples 2048 elements for its threshold, so on long
 // rows the threshold keeps many more candidates than TopK (expected count:
-// short_row_candidates). A CTA is planned at most this many: more overflow its
-// candidate regions now and then, and the exact fallback that follows reads
-// the row from global memory several times (measured on a GB300, TopK 2048:
-// four rows of 2^20 elements whole, about 6100 candidates each, 654 us; split
-// over clusters of 8 CTAs, 22 us).
+// short_row_candidates). A CTA that streams its row is planned at most this
+// many: more overflow its candidate regions now and then, and the exact
+// fallback that follows reads the row from global memory several times
+// (measured on a GB300: TopK 2048, four rows of 2^20 elements whole, about
+// 6100 candidates each, 654 us, split over clusters of 8 CTAs 22 us; TopK 4096,
+// 64 rows of 65536, about 5200 each, 73.7 us whole, 16.6 us over clusters of 2).
 constexpr double kShortMaxCandidates = 4096.0;
 // Longest row the short-row kernel is planned to select whole: beyond it the
 // 2048-element sample holds so few of the row's TopK best that its threshold

@@ -58,6 +58,8 @@ constexpr int kTrack = 64;                          // fine bins counted during 
 constexpr int kRank = kThreads / 2;                 // entries of the K-th key's fine bin at most (fast path)
 constexpr int kRankDirect = 192;                    // up to this many are ranked at once; more are first
                                                     // split on 8 more key bits
+constexpr int kBlind = 4;                           // pieces of a CTA's first window issued before its
+                                                    // length is known (the rest follow once it is)
 constexpr int kTaskSurvivors = 128;                 // expected survivors a filter task may take
 constexpr int kMinTasks = 8;                        // filter tasks a window is split into at least
 constexpr int kRefineExcess = 256;                  // a resident row refines its seed bin only when that
@@ -723,14 +725,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
 
   // Set-up: warp 0's lanes initialise the slot barriers and, with contiguous
   // rows, lane 0 issues piece 0 of the first row's blind window (sized by
-  // max_len) before anything else; warp 1 issues the rest of it (up to a ring's
-  // worth) after the barrier, so the seed's piece is not queued behind them.
-  // The first length is loaded now, used once the data is in.
+  // max_len, up to kBlind pieces) before anything else; after the barrier,
+  // when the first length is in, warp 1 issues the rest of the blind pieces
+  // and then the row's own window up to a ring's worth, so the seed's piece is
+  // queued behind none of them and few pieces are fetched past the row.
   const int32_t len_raw0 = __ldg(p.lengths + r);
   // thread 0 holds the raw length of the next row, loaded a row ahead of its use
   int32_t nl_raw = (tid == 0 && r + gridDim.x < p.num_rows) ? __ldg(p.lengths + r + gridDim.x) : 0;
   int blind = 0;  // pieces of the first row in flight before its length is known
-  if (bulk) blind = min(make_win(p, r, static_cast<int>(p.max_len)).np, kRing);  // the same in every thread
+  if (bulk) blind = min(make_win(p, r, static_cast<int>(p.max_len)).np, kBlind);  // the same in every thread
   if (warp == 0) {
     if (lane < kRing) {
       mbar_init(&s.bar[lane], 1u);
@@ -755,7 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   }
   __syncthreads();
   int len = clamp_len(p, len_raw0, tid == 0);
-  if (warp == 1 && bulk) issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), 1, blind, 0, false);
+  if (warp == 1 && bulk) {
+    issue_pieces(s, make_win(p, r, static_cast<int>(p.max_len)), 1, blind, 0, false);
+    const Win w0 = make_win(p, r, len);
+    issue_pieces(s, w0, blind, min(w0.np, kRing), 0, false);
+  }
 
   uint32_t par = 0;  // bit q: parity of the next phase of slot q's barrier
   int S = 0;         // ring slot of the current row's piece 0 (rows follow one another round the ring)
@@ -1458,13 +1465,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
   const int64_t r = blockIdx.x / C;
   if (r >= p.num_rows) return;  // the whole cluster: its CTAs share the row
 
-  // Set-up: this CTA's first pieces of the blind window (sized by max_len) go
-  // out before the length is read, local piece 0 first and the rest (by warp
-  // 1) after the barrier; local piece i (window piece me + C i) sits in slot
-  // i % kRing.
+  // Set-up: this CTA's first kBlind pieces of the blind window (sized by
+  // max_len) go out before the length is read, local piece 0 first and the
+  // rest (by warp 1) after the barrier, followed by the row's own pieces up to a
+  // ring's worth; local piece i (window piece me + C i) sits in slot i % kRing.
   const int32_t len_raw = __ldg(p.lengths + r);
   const Win wmax = make_win(p, r, static_cast<int>(p.max_len));
-  const int blind = min(wmax.np > me ? (wmax.np - me + C - 1) / C : 0, kRing);
+  const int blind = min(wmax.np > me ? (wmax.np - me + C - 1) / C : 0, kBlind);
   if (warp == 0) {
     if (lane < kRing) {
       mbar_init(&s.bar[lane], 1u);
@@ -1491,6 +1498,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
   const Win w = make_win(p, r, len);
   int32_t* o = p.out + r * static_cast<int64_t>(K);
   const int npl = w.np > me ? (w.np - me + C - 1) / C : 0;  // this CTA's pieces of the window
+  if (warp == 1 && lane >= blind && lane < min(npl, kRing)) issue_piece(s, w, me + C * lane, lane, false);
   bool aborted = false;
   bool drain = false;  // pieces may still be in flight at the end: wait for every slot's last copy
   if (w.nwin == 0) {

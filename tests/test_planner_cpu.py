@@ -360,7 +360,9 @@ def test_short_row_cluster_split():
     # whole rows beyond 2^18 elements, or whose expected candidates exceed 4096 (TopK 4096 of
     # 65536), take the wide shape; split over clusters they stay on the short-row kernel
     for rows, stride, k, shape, g in ((128, 1 << 20, 512, 1, 1), (128, 1 << 19, 512, 1, 1), (128, 65536, 4096, 1, 1),
-                                      (64, 65536, 4096, 4, 2), (64, 1 << 19, 4096, 4, 2), (16, 1 << 21, 512, 4, 6)):
+                                      (64, 65536, 4096, 4, 2), (64, 1 << 19, 4096, 4, 2), (16, 1 << 21, 512, 4, 6),
+                                      # rows resident in the ring stay whole whatever their candidates
+                                      (152, 32768, 4096, 4, 1), (608, 16384, 4096, 4, 1)):
         rc, pl = plan(gb, rows, stride, topk=k)
         assert rc == 0 and pl.shape == shape and pl.ctas_per_group == g, (rows, stride, k, pl.shape, pl.ctas_per_group)
     # the short-row kernel forced: the same rule; one CTA per row forced, or the workspace merge
