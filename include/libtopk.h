@@ -68,7 +68,8 @@ typedef enum {
 
 /* Tuning and test knobs for topk_ragged_ex. Zero-initialise, then set fields. */
 typedef struct {
-  /* 0 = planner decides; 1 = one CTA per row; 2..16 = that many CTAs split each row. */
+  /* 0 = planner decides; 1 = one CTA per row; 2..16 = that many CTAs split each row
+   * (with shape 4: 2..8, the CTAs of one thread-block cluster per row). */
   int force_ctas_per_group;
   /* 0 = default; rows whose row_stride exceeds this may be split across CTAs. */
   int64_t long_row_threshold;
@@ -96,7 +97,9 @@ typedef struct {
    * low-shared-memory mode for devices or partitions where 1 and 2 do not fit;
    * 4 = the short-row kernel: one CTA of 32 warps per SM owns whole rows, held
    * in a 128 KB shared-memory ring (rows of up to 32768 elements) or streamed
-   * through it. */
+   * through it, or the CTAs of a thread-block cluster share each row (planned
+   * for few long rows, or forced with force_ctas_per_group 2..8; contiguous
+   * rows only: strided views keep whole rows). */
   int shape;
 } topk_options;
 

@@ -1,5 +1,7 @@
 // The short-row kernel: one CTA of 32 warps per SM owns whole rows (any
-// length), held in or streamed through a shared-memory ring.
+// length), held in or streamed through a shared-memory ring; in its cluster
+// form (topk_short_cluster_kernel, further down) the CTAs of a thread-block
+// cluster share one row.
 //
 // This is the single-CTA path of the method: a shared-memory histogram seeds a
 // threshold, a filter keeps the elements at or above it as candidates with
@@ -8,8 +10,8 @@
 // take in the persistent_topk launcher of the vLLM PR #41189 page,
 // "Implementation breakdown"; the single-CTA FilteredTopK there keeps rows in
 // at least 128 KB of shared memory, vLLM PR #54110 page, "Feature and
-// motivation"). Here one CTA also streams rows longer than its ring, so no row
-// up to 2^20 elements is split across CTAs.
+// motivation"). Here one CTA also streams rows longer than its ring, and a
+// launch with too few long rows for the GPU splits each over a cluster.
 //
 // Per row:
 //   - lanes of warp 0 issue the row's window as 8 KB bulk copies
