@@ -275,10 +275,12 @@ class GpuBench:
         merge = "cluster" if pl.cluster else ("workspace" if pl.ctas_per_group > 1 else "none")
         shape = {1: "wide (24 consumer warps, 1 CTA/SM)", 2: "paired (12 consumer warps, 2 CTAs/SM)",
                  3: "small (8 consumer warps)",
-                 4: "short-row (32 warps, 1 CTA/SM, row resident in or streamed through a 128 KB ring)"
+                 4: "short-row (32 warps, 1 CTA/SM, row resident in or streamed through a 128 KB ring)",
+                 5: "short-row, 16 warps (1 CTA/SM, row resident in or streamed through a 128 KB ring)"
                  }.get(pl.shape, str(pl.shape))
-        if pl.shape == 4 and pl.ctas_per_group > 1:
-            shape = (f"short-row cluster ({pl.ctas_per_group} CTAs of 32 warps per row, CTA c streaming "
+        if pl.shape in (4, 5) and pl.ctas_per_group > 1:
+            warps = 32 if pl.shape == 4 else 16
+            shape = (f"short-row cluster ({pl.ctas_per_group} CTAs of {warps} warps per row, CTA c streaming "
                      f"pieces c, c + {pl.ctas_per_group}, ... through its 128 KB ring)")
         return {"ctas_per_row": pl.ctas_per_group, "grid": pl.grid, "merge": merge, "shape": shape}
 
@@ -435,11 +437,12 @@ def run_sweep(args) -> None:
     props = sar.topk_query_device(0)
     K = args.sweep_topk
     gen = t.Generator(device=gb.dev)
-    arms = [("short", dict(shape=4, force_ctas_per_group=1)), ("paired", dict(shape=2)),
-            ("wide", dict(shape=1, force_ctas_per_group=1))]
+    arms = [("short", dict(shape=4, force_ctas_per_group=1)), ("short16", dict(shape=5, force_ctas_per_group=1)),
+            ("paired", dict(shape=2)), ("wide", dict(shape=1, force_ctas_per_group=1))]
     arms += [(f"split{g}", dict(shape=1, force_ctas_per_group=g, merge=2)) for g in (2, 4, 8)]
-    # the short-row kernel with each row split over a cluster of g CTAs
-    arms += [(f"short{g}", dict(shape=4, force_ctas_per_group=g)) for g in (2, 3, 4, 6, 8)]
+    # the short-row kernel with each row split over a cluster of g CTAs (32 and 16 warps)
+    arms += [(f"short{g}", dict(shape=4, force_ctas_per_group=g)) for g in (2, 4, 8)]
+    arms += [(f"s16x{g}", dict(shape=5, force_ctas_per_group=g)) for g in (2, 3, 4, 6, 8)]
     print(f"| row length | rows | planner | {' | '.join(a for a, _ in arms)} | best |")
     print("|---:|---:|---|" + "---:|" * (len(arms) + 1))
     stream = t.cuda.current_stream()
@@ -454,7 +457,7 @@ def run_sweep(args) -> None:
             ln = t.full((R,), L, dtype=t.int32, device=gb.dev)
             out = t.empty((R, K), dtype=t.int32, device=gb.dev)
             rc, pl = sar.topk_make_plan(props, R, L, 1, K)
-            planner = f"{ {1: 'wide', 2: 'paired', 3: 'small', 4: 'short'}.get(pl.shape, '?')}" + (
+            planner = f"{ {1: 'wide', 2: 'paired', 3: 'small', 4: 'short', 5: 'short16'}.get(pl.shape, '?')}" + (
                 f" x{pl.ctas_per_group}" if pl.ctas_per_group > 1 else "")
             times = []
             for _, kw in arms:

@@ -99,7 +99,8 @@ typedef struct {
    * in a 128 KB shared-memory ring (rows of up to 32768 elements) or streamed
    * through it, or the CTAs of a thread-block cluster share each row (planned
    * for few long rows, or forced with force_ctas_per_group 2..8; contiguous
-   * rows only: strided views keep whole rows). */
+   * rows only: strided views keep whole rows); 5 = the same kernel with 16
+   * warps per CTA (512 threads), faster on short rows and split rows. */
   int shape;
 } topk_options;
 
@@ -121,6 +122,9 @@ typedef struct {
   /* short_cluster_groups[c], c = 2..8: resident clusters of c CTAs of the
    * short-row kernel's cluster form (a row split over a cluster). */
   int short_cluster_groups[9];
+  int short16_smem_per_cta; /* the same three for the short-row kernel with 16 warps per CTA */
+  int short16_ctas_per_sm;
+  int short16_cluster_groups[9];
 } topk_device_props;
 
 /* A launch configuration. */
@@ -134,7 +138,7 @@ typedef struct {
   int cluster;        /* 1 when the CTAs of a group form a cluster and merge in its shared memory */
   int shape;          /* 1 = one CTA of 24 consumer warps per SM, 2 = two CTAs of 12 per SM,
                          3 = the small shape (8 consumer warps, low shared memory),
-                         4 = the short-row kernel */
+                         4 = the short-row kernel, 5 = the short-row kernel with 16 warps */
 } topk_plan;
 
 /*

@@ -87,7 +87,10 @@ class TopkDeviceProps(ctypes.Structure):
                 ("small_ctas_per_sm", ctypes.c_int),
                 ("short_smem_per_cta", ctypes.c_int),
                 ("short_ctas_per_sm", ctypes.c_int),
-                ("short_cluster_groups", ctypes.c_int * 9)]
+                ("short_cluster_groups", ctypes.c_int * 9),
+                ("short16_smem_per_cta", ctypes.c_int),
+                ("short16_ctas_per_sm", ctypes.c_int),
+                ("short16_cluster_groups", ctypes.c_int * 9)]
 
 
 class TopkPlan(ctypes.Structure):

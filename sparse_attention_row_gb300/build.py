@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtopk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["topk_kernel.cu", "topk_kernel_pair.cu", "topk_kernel_small.cu", "topk_short.cu", "topk_sort.cu", "topk_api.cu",
+SOURCES = ["topk_kernel.cu", "topk_kernel_pair.cu", "topk_kernel_small.cu", "topk_short.cu", "topk_short16.cu", "topk_sort.cu",
+           "topk_api.cu",
            "topk_static.cu", "planner.cpp"]
 
 

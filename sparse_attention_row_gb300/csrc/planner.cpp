@@ -57,6 +57,9 @@ namespace {
 
 bool topk_supported(int topk) { return topk >= 1 && topk <= ltk::kWideMaxTopK; }
 
+// The two instances of the short-row kernel (32 and 16 warps per CTA).
+bool is_short(int shape) { return shape == ltk::kShapeShort || shape == ltk::kShapeShort16; }
+
 // Candidates the short-row kernel's filter is expected to keep on a row of
 // `stride` elements: its threshold keeps mu + 3 sqrt(mu) + 2 keys of the
 // kShortSeedLen-element sample (mu = topk * kShortSeedLen / stride, the
@@ -79,18 +82,19 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   const int merge = (options != nullptr) ? options->merge : 0;
   if (merge < 0 || merge > 2) return TOPK_ERR_INVALID_ARG;
   const int shape = (options != nullptr) ? options->shape : 0;
-  if (shape < 0 || shape > 4) return TOPK_ERR_INVALID_ARG;
+  if (shape < 0 || shape > ltk::kShapeShort16) return TOPK_ERR_INVALID_ARG;
   const int force = (options != nullptr) ? options->force_ctas_per_group : 0;
   if (force < 0 || force > ltk::kMaxGroup) return TOPK_ERR_INVALID_ARG;
   // the paired and small shapes split no row; the short-row kernel splits one
   // over a thread-block cluster of up to 8 CTAs
-  if (shape > ltk::kShapeWide && force > 1 && (shape != ltk::kShapeShort || force > ltk::kMaxCluster))
+  if (shape > ltk::kShapeWide && force > 1 && (!is_short(shape) || force > ltk::kMaxCluster))
     return TOPK_ERR_INVALID_ARG;
   if (props->num_sms < 1) return TOPK_ERR_PLAN;
   const bool wide_ok = props->ctas_per_sm >= 1 && props->smem_per_cta <= props->max_smem_optin;
   const bool pair_ok = props->pair_ctas_per_sm >= 1 && props->pair_smem_per_cta <= props->max_smem_optin;
   const bool small_ok = props->small_ctas_per_sm >= 1 && props->small_smem_per_cta <= props->max_smem_optin;
   const bool short_ok = props->short_ctas_per_sm >= 1 && props->short_smem_per_cta <= props->max_smem_optin;
+  const bool short16_ok = props->short16_ctas_per_sm >= 1 && props->short16_smem_per_cta <= props->max_smem_optin;
 
   // the CTA shape when it is not the planner's to choose, or when the wide
   // shape does not fit the device (then the largest whole-row shape that fits)
@@ -100,6 +104,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   if (chosen == ltk::kShapePair && !pair_ok) return TOPK_ERR_PLAN;
   if (chosen == ltk::kShapeSmall && !small_ok) return TOPK_ERR_PLAN;
   if (chosen == ltk::kShapeShort && !short_ok) return TOPK_ERR_PLAN;
+  if (chosen == ltk::kShapeShort16 && !short16_ok) return TOPK_ERR_PLAN;
   if (chosen == ltk::kShapePair && topk > ltk::kPairMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
   if (chosen == ltk::kShapeSmall && topk > ltk::kSmallMaxTopK) return TOPK_ERR_UNSUPPORTED_TOPK;
 
@@ -115,16 +120,24 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   // 8 with rows x size within the SMs whose clusters are all resident at once,
   // if its CTAs' expected candidates stay within kShortMaxCandidates (0: none)
   const double candidates = short_row_candidates(row_stride, topk);
-  auto short_cluster_size = [&]() -> int64_t {
-    if (!short_ok || force != 0 || merge == 1 || num_rows < 1 || row_stride < ltk::kShortClusterStride ||
+  // resident clusters of each size for an instance of the short-row kernel
+  auto short_groups = [&](int s) -> const int* {
+    return s == ltk::kShapeShort16 ? props->short16_cluster_groups : props->short_cluster_groups;
+  };
+  auto short_cluster_size = [&](int s) -> int64_t {
+    const bool ok = s == ltk::kShapeShort16 ? short16_ok : short_ok;
+    if (!ok || force != 0 || merge == 1 || num_rows < 1 || row_stride < ltk::kShortClusterStride ||
         2 * static_cast<int64_t>(topk) >= row_stride)
       return 0;
     int64_t sms = props->num_sms;
     if (options != nullptr && options->max_ctas > 0) sms = std::min<int64_t>(sms, options->max_ctas);
     int64_t g = std::min<int64_t>(ltk::kMaxCluster, sms / num_rows);
-    while (g >= 2 && props->short_cluster_groups[g] < num_rows) --g;
+    while (g >= 2 && short_groups(s)[g] < num_rows) --g;
     return (g >= 2 && candidates / static_cast<double>(g) <= ltk::kShortMaxCandidates) ? g : 0;
   };
+  // the split runs on the 16-warp instance where the device holds it (faster:
+  // mtp 19.1 against 20.8 us, long_coop 15.0 against 15.5 us on a GB300)
+  const int split_shape = short16_ok ? ltk::kShapeShort16 : ltk::kShapeShort;
   // whole rows: resident in the short-row kernel's ring (an overflow of its
   // candidate regions then costs an exact pass over the ring: TopK 4096 of
   // 32768, 16.4 us against 22.5 us on the wide shape), or streamed with their
@@ -134,8 +147,8 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
                    (candidates <= ltk::kShortMaxCandidates && row_stride <= ltk::kShortMaxWholeStride));
   int64_t G = 1;
   bool cluster = false;
-  if (chosen == 0 && short_cluster_size() >= 2) {
-    chosen = ltk::kShapeShort;  // few long rows: split over clusters of the short-row kernel
+  if (chosen == 0 && short_cluster_size(split_shape) >= 2) {
+    chosen = split_shape;  // few long rows: split over clusters of the short-row kernel
   } else if (chosen <= ltk::kShapeWide) {  // the wide shape, given or still open
     if (force != 0) {
       G = force;
@@ -177,17 +190,21 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
                         (row_stride <= ltk::kPairMaxStride || !short_ok);
       const bool shrt = G == 1 && short_whole &&
                         (row_stride <= ltk::kShortSeedLen || 2 * static_cast<int64_t>(topk) < row_stride);
-      chosen = pair ? ltk::kShapePair : shrt ? ltk::kShapeShort : ltk::kShapeWide;
+      // short rows on the 16-warp instance, whose block-wide phases cost half
+      // the instructions; longer ones on the 32-warp one, whose filter keeps up
+      const bool shrt16 = short16_ok && (row_stride <= ltk::kShort16MaxStride ||
+                                         (row_stride <= ltk::kShort16MaxLongStride && topk <= ltk::kShort16LongTopK));
+      chosen = pair ? ltk::kShapePair : shrt ? (shrt16 ? ltk::kShapeShort16 : ltk::kShapeShort) : ltk::kShapeWide;
     }
   }
-  if (chosen == ltk::kShapeShort && force > 1) {
+  if (is_short(chosen) && force > 1) {
     // a row split over a cluster of the short-row kernel: one row per cluster,
     // merged in its shared memory only
-    if (merge == 1 || props->short_cluster_groups[force] < 1) return TOPK_ERR_PLAN;
+    if (merge == 1 || short_groups(chosen)[force] < 1) return TOPK_ERR_PLAN;
     G = force;
     cluster = true;
-  } else if (chosen == ltk::kShapeShort && G == 1) {
-    const int64_t g = short_cluster_size();  // also when the short-row kernel was asked for
+  } else if (is_short(chosen) && G == 1) {
+    const int64_t g = short_cluster_size(chosen);  // also when the short-row kernel was asked for
     if (g >= 2) {
       G = g;
       cluster = true;
@@ -200,13 +217,16 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
   } else {
     const int per_sm = chosen == ltk::kShapePair    ? props->pair_ctas_per_sm
                        : chosen == ltk::kShapeSmall ? props->small_ctas_per_sm
-                                                    : props->short_ctas_per_sm;
+                       : chosen == ltk::kShapeShort ? props->short_ctas_per_sm
+                                                    : props->short16_ctas_per_sm;
     plan->threads = chosen == ltk::kShapePair    ? ltk::kPairCtaThreads
                     : chosen == ltk::kShapeSmall ? ltk::kSmallCtaThreads
-                                                 : ltk::kShortCtaThreads;
+                    : chosen == ltk::kShapeShort ? ltk::kShortCtaThreads
+                                                 : ltk::kShort16CtaThreads;
     plan->smem_bytes = chosen == ltk::kShapePair    ? props->pair_smem_per_cta
                        : chosen == ltk::kShapeSmall ? props->small_smem_per_cta
-                                                    : props->short_smem_per_cta;
+                       : chosen == ltk::kShapeShort ? props->short_smem_per_cta
+                                                    : props->short16_smem_per_cta;
     cap = static_cast<int64_t>(props->num_sms) * per_sm;
     if (options != nullptr && options->max_ctas > 0) cap = std::min<int64_t>(cap, options->max_ctas);
   }
@@ -219,7 +239,7 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     return TOPK_OK;
   }
   int64_t groups;
-  if (chosen == ltk::kShapeShort && G > 1) {
+  if (is_short(chosen) && G > 1) {
     // one row per cluster; clusters that are not resident wait for a free slot
     if (num_rows > INT32_MAX / G) return TOPK_ERR_PLAN;
     groups = num_rows;

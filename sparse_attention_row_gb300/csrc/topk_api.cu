@@ -97,6 +97,18 @@ int query_device_locked(int device, topk_device_props* out) {
         }
       }
     }
+    p.short16_smem_per_cta = static_cast<int>(ltk::short16::kernel_smem_bytes());
+    if (rc == TOPK_OK && p.short16_smem_per_cta <= p.max_smem_optin) {
+      if (ltk::short16::kernel_configure() != cudaSuccess ||
+          ltk::short16::kernel_occupancy(&p.short16_ctas_per_sm) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
+      for (int c = 2; rc == TOPK_OK && c <= ltk::kMaxCluster; ++c) {
+        if (ltk::short16::kernel_max_clusters(c, &p.short16_cluster_groups[c]) != cudaSuccess) {
+          cudaGetLastError();
+          p.short16_cluster_groups[c] = 0;
+        }
+      }
+    }
     if (prev != device) cudaSetDevice(prev);
     if (rc != TOPK_OK) {
       cudaGetLastError();
@@ -157,7 +169,8 @@ int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t str
   if (rc != TOPK_OK) return rc;
   // the short-row kernel splits only contiguous rows over a cluster; strided
   // ones stay whole
-  if (plan.shape == kShapeShort && plan.ctas_per_group > 1 && c.col_stride != 1) {
+  const bool short_shape = plan.shape == kShapeShort || plan.shape == kShapeShort16;
+  if (short_shape && plan.ctas_per_group > 1 && c.col_stride != 1) {
     opt.force_ctas_per_group = 1;
     rc = topk_make_plan(&props, c.num_rows, c.max_len, c.next_n, c.topk, &opt, &plan);
     if (rc != TOPK_OK) return rc;
@@ -165,7 +178,8 @@ int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t str
   if (plan.grid < 1) return TOPK_OK;
   // a caller-provided workspace holds num_sms row groups, as many as the planner
   // ever uses (the short-row kernel's cluster split uses none)
-  if (max_groups >= 0 && plan.ctas_per_group > 1 && plan.shape != kShapeShort && plan.num_groups > max_groups)
+  if (max_groups >= 0 && plan.ctas_per_group > 1 && plan.shape != kShapeShort && plan.shape != kShapeShort16 &&
+      plan.num_groups > max_groups)
     return TOPK_ERR_WORKSPACE_TOO_SMALL;
 
   Params p{};

@@ -33,15 +33,18 @@ constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 // only, for devices or partitions with less shared memory per block.
 // kShapeShort: the short-row kernel (topk_short.cu), one CTA of 32 warps per
 // SM; a row of at most kShortMaxLen elements stays resident in its 128 KB ring,
-// a longer one streams through it.
+// a longer one streams through it. kShapeShort16: the same kernel with 16
+// warps per CTA (topk_short16.cu).
 constexpr int kShapeWide = 1;
 constexpr int kShapePair = 2;
 constexpr int kShapeSmall = 3;
 constexpr int kShapeShort = 4;
+constexpr int kShapeShort16 = 5;
 constexpr int kWideCtaThreads = 800;   // 24 consumer warps + the copy warp
 constexpr int kPairCtaThreads = 416;   // 12 consumer warps + the copy warp
 constexpr int kSmallCtaThreads = 288;  // 8 consumer warps + the copy warp
 constexpr int kShortCtaThreads = 1024;
+constexpr int kShort16CtaThreads = 512;
 constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds resident in its ring
 constexpr int64_t kShortSeedLen = 2048;  // elements it samples for its threshold (rows this short: all of them)
 // Rows at least this long, too few to give every SM its own, are split over a
@@ -66,6 +69,13 @@ constexpr double kShortMaxCandidates = 4096.0;
 // wide shape; TopK 2048, 2^19: 354 us against 66 us), while 2^18 still wins
 // (TopK 2048, 152 rows: 36.9 us against 45.1 us).
 constexpr int64_t kShortMaxWholeStride = 1 << 18;
+// Longest rows planned whole on the 16-warp instance of the short-row kernel,
+// at any TopK and at TopK up to kShort16LongTopK (measured on a GB300, bench.py
+// --sweep: TopK 512 of 4096-element rows 10.2 against 11.8 us, of 16384 10.2
+// to 12.3 against 10.3 to 12.3; TopK 2048 of 16384 14.3 against 12.3 us).
+constexpr int64_t kShort16MaxStride = 4096;
+constexpr int64_t kShort16MaxLongStride = 16384;
+constexpr int kShort16LongTopK = 512;
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.
@@ -103,7 +113,7 @@ struct Params {
   int cluster;       // 1: the G CTAs of a group are one cluster and merge through its shared memory
 };
 
-// Host side of one compiled kernel shape (ltk::wide, ltk::pair, ltk::small, ltk::shortrow).
+// Host side of one compiled kernel shape (ltk::wide, ltk::pair, ltk::small, ltk::shortrow, ltk::short16).
 #define LTK_DECLARE_SHAPE(NS)                                                                  \
   namespace NS {                                                                               \
   int kernel_threads();                                                                        \
@@ -117,6 +127,7 @@ LTK_DECLARE_SHAPE(wide)
 LTK_DECLARE_SHAPE(pair)
 LTK_DECLARE_SHAPE(small)
 LTK_DECLARE_SHAPE(shortrow)
+LTK_DECLARE_SHAPE(short16)
 #undef LTK_DECLARE_SHAPE
 
 // One selection as the entry points receive it (device pointers, caller-owned).
@@ -145,6 +156,7 @@ inline cudaError_t launch_shape(int shape, const Params& p, int grid, bool coope
   if (shape == kShapePair) return pair::launch_topk(p, grid, cooperative, stream);
   if (shape == kShapeSmall) return small::launch_topk(p, grid, cooperative, stream);
   if (shape == kShapeShort) return shortrow::launch_topk(p, grid, cooperative, stream);
+  if (shape == kShapeShort16) return short16::launch_topk(p, grid, cooperative, stream);
   return wide::launch_topk(p, grid, cooperative, stream);
 }
 

@@ -43,21 +43,33 @@
 
 #include "topk_internal.h"
 
-namespace ltk {
-namespace shortrow {
+// Two instances are built from this source: ltk::shortrow, 32 warps (the
+// default below), and ltk::short16, 16 warps with twice the candidate slots
+// per warp (topk_short16.cu), whose block-wide phases cost half the
+// instructions: faster on short rows and split rows, slower where the filter
+// sets the pace.
+#ifndef LTK_SHORT_NS
+#define LTK_SHORT_NS shortrow
+#define LTK_SHORT_THREADS kShortCtaThreads
+#define LTK_SHORT_REGION 256
+#endif
 
-constexpr int kThreads = kShortCtaThreads;  // 32 warps
+namespace ltk {
+namespace LTK_SHORT_NS {
+
+constexpr int kThreads = LTK_SHORT_THREADS;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPiece = 2048;                        // elements per bulk copy (8 KB), one mbarrier each
 constexpr int kRing = 16;                           // ring slots of one piece (128 KB): a row of up to 16
                                                     // pieces is resident; longer rows stream through it
 constexpr int kTask = 512;                          // window elements a warp filters at a time (4 float4 per lane)
 constexpr int kSeed = kPiece;                       // window elements histogrammed for the seed (piece 0)
-constexpr int kRegion = 256;                        // candidate slots per warp
+constexpr int kRegion = LTK_SHORT_REGION;           // candidate slots per warp
 constexpr int kCand = kWarps * kRegion;
 constexpr int kFine = 17;                           // fine bins: (key - threshold) >> 17, or coarser
 constexpr int kTrack = 64;                          // fine bins counted during the filter, from the seed bin's edge
-constexpr int kRank = kThreads / 2;                 // entries of the K-th key's fine bin at most (fast path)
+constexpr int kRank = 512;                          // entries of the K-th key's fine bin at most (fast path)
+static_assert(kRank <= kThreads, "one thread per ranked entry at least");
 constexpr int kRankDirect = 192;                    // up to this many are ranked at once; more are first
                                                     // split on 8 more key bits
 constexpr int kBlind = 4;                           // pieces of a CTA's first window issued before its
@@ -608,7 +620,7 @@ __device__ __forceinline__ int warp_find256(const uint32_t* h, int need, int& ab
 // index of every entry of rank < need at out[rank]. Groups of 2^lg lanes (the
 // most that fit the block, at most a warp) share an entry: lane `sub` of a
 // group compares it with entries 4 sub .. 4 sub + 3, then every 4 * 2^lg-th
-// on. Needs n <= kThreads / 2. Block-wide (no barrier).
+// on. Needs n <= kThreads. Block-wide (no barrier).
 __device__ __forceinline__ void rank_out(const uint32_t* kk, const int32_t* ii, int n, int c4, int need,
                                          int32_t* out) {
   const int tid = threadIdx.x;
@@ -1877,5 +1889,5 @@ cudaError_t launch_topk(const Params& p, int grid, bool, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, topk_short_cluster_kernel, p);
 }
 
-}  // namespace shortrow
+}  // namespace LTK_SHORT_NS
 }  // namespace ltk

@@ -108,7 +108,8 @@ def _short_case(seed: int):
     lengths = rng.integers(0, stride + 1, size=num_rows)
     lengths[rng.random(num_rows) < 0.3] = stride
     max_ctas = int(rng.choice([0, 0, 1, 3, 17]))
-    return x, lengths.astype(np.int32), topk, dict(shape=4, max_ctas=max_ctas)
+    return x, lengths.astype(np.int32), topk, dict(shape=int(rng.choice([4, 5])), max_ctas=max_ctas,
+                                                   force_ctas_per_group=1)
 
 
 @pytest.mark.parametrize("seed", range(SHORT_CASES))
@@ -135,7 +136,8 @@ def _cluster_case(seed: int):
     x = np.stack([_row(rng, stride) for _ in range(num_rows)])
     lengths = rng.integers(0, stride + 1, size=num_rows)
     lengths[rng.random(num_rows) < 0.3] = stride
-    return x, lengths.astype(np.int32), topk, int(rng.integers(0, 4)), dict(shape=4, force_ctas_per_group=G)
+    return x, lengths.astype(np.int32), topk, int(rng.integers(0, 4)), dict(shape=int(rng.choice([4, 5])),
+                                                                           force_ctas_per_group=G)
 
 
 @pytest.mark.parametrize("seed", range(CLUSTER_CASES))

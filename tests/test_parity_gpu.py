@@ -27,13 +27,13 @@ def test_workloads_small_auto(rn, name, rows):
     assert rn.workspace_clean()
 
 
-@pytest.mark.parametrize("shape", [1, 2, 3, 4])
+@pytest.mark.parametrize("shape", [1, 2, 3, 4, 5])
 @pytest.mark.parametrize("name,rows", SMALL)
 def test_workloads_small_other_shapes(rn, name, rows, shape):
     """Every CTA shape forced on every workload: the wide one (24 consumer warps), the paired one
     (two CTAs of 12 consumer warps per SM), the small, low-shared-memory one (8 consumer warps), and
-    the short-row kernel (32 warps; rows of up to 16 pieces resident, longer rows streamed through
-    its ring of 16 slots)."""
+    the short-row kernel with 32 or 16 warps (rows of up to 16 pieces resident, longer rows
+    streamed through its ring of 16 slots; long rows of few-row batches split over clusters)."""
     w = workloads.make(name, rows)
     got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=shape))
     assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} shape={shape}")
@@ -42,7 +42,7 @@ def test_workloads_small_other_shapes(rn, name, rows, shape):
 
 @pytest.mark.parametrize("topk", [1, 7, 100, 1000, 2047, 2049, 3000, 4096])
 @pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (0, 0, 2), (0, 0, 3), (3, 1, 0), (4, 2, 0), (0, 0, 4),
-                                           (3, 0, 4)])
+                                           (3, 0, 4), (0, 0, 5), (3, 0, 5)])
 def test_runtime_topk(rn, topk, G, merge, shape):
     """TopK outside the pages' 512 / 1024 / 2048, on every path (paired and small shapes up to 2048)."""
     if shape in (2, 3) and topk > 2048:
@@ -58,7 +58,8 @@ def test_runtime_topk(rn, topk, G, merge, shape):
 
 
 @pytest.mark.parametrize("layout", ["transposed", "every_third_column", "padded_rows"])
-@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 1), (1, 0, 2), (1, 0, 3), (3, 1, 0), (4, 2, 0)])
+@pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 1), (1, 0, 2), (1, 0, 3), (3, 1, 0), (4, 2, 0),
+                                           (1, 0, 4), (1, 0, 5)])
 def test_strided_logits(rn, layout, G, merge, shape):
     """Views with a row pitch and a column stride: transposed, column-strided, padded rows."""
     torch = rn.torch
@@ -163,15 +164,17 @@ def test_workloads_forced_split(rn, name, rows, G, merge):
     assert rn.workspace_clean()
 
 
+@pytest.mark.parametrize("shape", [4, 5])
 @pytest.mark.parametrize("G", [2, 3, 4, 6, 8])
 @pytest.mark.parametrize("name,rows", [("decode_small", 8), ("decode_batch", 6), ("long_coop", 3), ("mtp", 4),
                                        ("prefill", 4)])
-def test_workloads_short_row_cluster_split(rn, name, rows, G):
-    """Each row split over a thread-block cluster of G short-row CTAs (CTA c takes window
-    pieces c, c + G, ...), merged in the cluster's shared memory."""
+def test_workloads_short_row_cluster_split(rn, name, rows, G, shape):
+    """Each row split over a thread-block cluster of G short-row CTAs (32 or 16 warps; CTA c
+    takes window pieces c, c + G, ...), merged in the cluster's shared memory."""
     w = workloads.make(name, rows)
-    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=4, force_ctas_per_group=G))
-    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} short-row cluster G={G}")
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=shape, force_ctas_per_group=G))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n,
+                          label=f"{name} short-row cluster G={G} shape={shape}")
     assert rn.workspace_clean()
 
 
@@ -211,7 +214,7 @@ def _edge_rows(S: int, K: int, rng) -> tuple[np.ndarray, np.ndarray]:
 @pytest.mark.parametrize("topk", [512, 1024, 2048])
 @pytest.mark.parametrize("S", [4096, 9001, 40000])
 @pytest.mark.parametrize("G,merge,shape", [(0, 0, 0), (1, 0, 1), (0, 0, 2), (0, 0, 3), (4, 1, 0), (4, 2, 0), (8, 2, 0),
-                                           (0, 0, 4), (2, 0, 4), (5, 0, 4), (8, 0, 4)])
+                                           (0, 0, 4), (2, 0, 4), (5, 0, 4), (8, 0, 4), (0, 0, 5), (4, 0, 5)])
 def test_edge_cases(rn, topk, S, G, merge, shape):
     # with G = 8 and K = 2048 the all-equal row keeps 8 x K candidates at one
     # key, more than the leader's buffer: the cluster merge hands over to the
@@ -247,7 +250,7 @@ def _kth_bin_size(row: np.ndarray, K: int) -> int:
 
 
 @pytest.mark.parametrize("S", [30000, 100000])
-@pytest.mark.parametrize("shape,G", [(0, 0), (4, 0), (4, 2), (4, 6)])
+@pytest.mark.parametrize("shape,G", [(0, 0), (4, 0), (4, 2), (4, 6), (5, 0), (5, 3)])
 def test_large_kth_key_bin(rn, S, shape, G):
     """Hundreds of elements share the K-th key's bin (a dense cluster): the selection
     splits that bin further before ranking; with equal keys inside it, by index."""
@@ -263,7 +266,7 @@ def test_large_kth_key_bin(rn, S, shape, G):
 
 
 @pytest.mark.parametrize("S,K", [(4096, 1536), (4096, 2048), (6000, 2800), (8192, 4096), (40000, 4096)])
-@pytest.mark.parametrize("shape,G", [(0, 0), (4, 0), (4, 3)])
+@pytest.mark.parametrize("shape,G", [(0, 0), (4, 0), (4, 3), (5, 0), (5, 2)])
 def test_kth_key_far_from_the_threshold(rn, S, K, shape, G):
     """The K-th key lies many binades above the seed's threshold: a selected fraction
     near one half of N(0,1) rows (the K-th value near zero), and rows whose values near
@@ -300,7 +303,7 @@ def test_unaligned_rows(rn, shift, stride_delta):
     S = 20000 + stride_delta
     x = rng.standard_normal((5, S)).astype(np.float32)
     lens = np.array([S, S - 1, 3000, 12345, 2049], np.int32)
-    for G, shape in ((1, 0), (2, 0), (3, 4)):
+    for G, shape in ((1, 0), (2, 0), (3, 4), (1, 5), (2, 5)):
         got = rn.run(x, lens, 2048, pad_front=shift, options=rn.options(force_ctas_per_group=G, shape=shape))
         assert_matches_oracle(x, lens, got, 2048, label=f"shift={shift} S={S} G={G} shape={shape}")
 
@@ -331,9 +334,11 @@ def test_many_rows_per_cta_and_per_group(rn):
     # the small shape, 5 CTAs: 60 rows each
     got = rn.run(x, lens, 1024, options=rn.options(max_ctas=5, shape=3))
     assert_matches_oracle(x, lens, got, 1024, label="small persistent")
-    # the short-row kernel, 7 CTAs: 42 or 43 rows each
+    # the short-row kernel, 7 CTAs: 42 or 43 rows each (32 warps), 9 CTAs (16 warps)
     got = rn.run(x, lens, 1024, options=rn.options(max_ctas=7, shape=4))
     assert_matches_oracle(x, lens, got, 1024, label="short-row persistent")
+    got = rn.run(x, lens, 1024, options=rn.options(max_ctas=9, shape=5))
+    assert_matches_oracle(x, lens, got, 1024, label="short-row 16-warp persistent")
     # the wide shape on whole rows, 6 CTAs
     got = rn.run(x, lens, 1024, options=rn.options(max_ctas=6, shape=1))
     assert_matches_oracle(x, lens, got, 1024, label="wide persistent")

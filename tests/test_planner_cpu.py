@@ -14,7 +14,7 @@ def _built():
 
 
 def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, pair=(0, 0), small=(0, 0),
-          short=(0, 0), short_clusters=None):
+          short=(0, 0), short_clusters=None, short16=(0, 0), short16_clusters=None):
     """A made-up device; clusters (short_clusters) maps a cluster size to its co-resident count for
     the wide shape (the short-row kernel's cluster form), none by default; pair, small and short are
     (shared memory, CTAs per SM) of those shapes (absent by default)."""
@@ -27,6 +27,9 @@ def props(num_sms=152, occ=1, smem=217 * 1024, optin=227 * 1024, clusters=None, 
     p.short_smem_per_cta, p.short_ctas_per_sm = short
     for c, n in (short_clusters or {}).items():
         p.short_cluster_groups[c] = n
+    p.short16_smem_per_cta, p.short16_ctas_per_sm = short16
+    for c, n in (short16_clusters or {}).items():
+        p.short16_cluster_groups[c] = n
     return p
 
 
@@ -204,7 +207,8 @@ def test_paired_shape():
     rc, pl = plan(gb, 16, 131072, shape=2)
     assert rc == 0 and pl.shape == 2 and pl.ctas_per_group == 1
     assert plan(props(), 8, 4096, shape=2)[0] == sar.TOPK_ERR_PLAN
-    assert plan(gb, 8, 4096, shape=5)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 4096, shape=6)[0] == sar.TOPK_ERR_INVALID_ARG
+    assert plan(gb, 8, 4096, shape=5)[0] == sar.TOPK_ERR_PLAN  # no 16-warp short-row kernel on this made-up device
     assert plan(gb, 8, 4096, shape=4)[0] == sar.TOPK_ERR_PLAN  # no short-row kernel on this made-up device
     assert plan(gb, 8, 4096, shape=3)[0] == sar.TOPK_ERR_PLAN  # no small shape on this made-up device
     # TopK above 2048 runs on the wide shape only
@@ -379,3 +383,31 @@ def test_short_row_cluster_split():
     rc, pl = plan(props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT),
                   16, 131072)
     assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 1
+
+
+def test_short_row_kernel_with_16_warps():
+    """The 16-warp instance of the short-row kernel (shape 5) takes whole rows of up to 4096
+    elements (16384 at TopK 512 or less) and every split over a cluster, where the device holds
+    it; the 32-warp instance keeps the longer whole rows (the crossovers bench.py --sweep measured
+    on a GB300)."""
+    gb = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT,
+               short_clusters=gb300_clusters(), short16=GB300_SHORT, short16_clusters=gb300_clusters())
+    for rows, stride, k, shape, g in ((8, 4096, 512, 5, 1), (152, 2048, 1024, 5, 1), (64, 32768, 2048, 4, 1),
+                                      (64, 16384, 512, 5, 1), (64, 16384, 1024, 4, 1), (64, 16385, 512, 4, 1),
+                                      (4096, 65536, 2048, 4, 1), (16, 131072, 2048, 5, 6), (64, 163840, 1024, 5, 2),
+                                      (608, 4096, 512, 2, 1), (64, 4096, 2048, 1, 1)):
+        rc, pl = plan(gb, rows, stride, topk=k)
+        assert rc == 0 and pl.shape == shape and pl.ctas_per_group == g, (rows, stride, k, pl.shape, pl.ctas_per_group)
+        if shape == 5:
+            assert pl.threads == 512 and pl.cluster == (g > 1)
+    # forced: the 16-warp instance whole or split, like shape 4
+    rc, pl = plan(gb, 10, 30000, shape=5, force_ctas_per_group=3)
+    assert rc == 0 and pl.shape == 5 and pl.ctas_per_group == 3 and pl.cluster and pl.grid == 30
+    rc, pl = plan(gb, 64, 32768, shape=5)
+    assert rc == 0 and pl.shape == 5 and pl.ctas_per_group == 1 and pl.grid == 64
+    assert plan(gb, 10, 30000, shape=5, force_ctas_per_group=9)[0] == sar.TOPK_ERR_INVALID_ARG
+    # a device without the 16-warp instance splits on the 32-warp one
+    gb32 = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT,
+                 short_clusters=gb300_clusters())
+    rc, pl = plan(gb32, 16, 131072)
+    assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == 6
