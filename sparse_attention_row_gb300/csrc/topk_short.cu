@@ -1258,36 +1258,32 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
 // single-pass shape; the merge takes the place of the pages' cross-CTA radix
 // histograms). CTA c takes window pieces c, c + C, c + 2 C, ..., a balanced
 // share whatever the length, so each issues its first pieces before the
-// length is read. CTA 0 seeds the threshold from piece 0 as one CTA does and
-// stores it into every CTA; every CTA filters its pieces into its own
-// candidate regions and stores its fine-bin counts into every CTA, so each
-// finds the K-th key's fine bin t on its own, with the same answer, and knows
-// where its winners and bin t entries go; it writes its winners and sends bin
-// t's entries to CTA 0, which ranks them. Three cluster barriers a row after a
-// start barrier (one more when the K-th key lies above the counted bins),
-// taken by every thread of every CTA whatever happened before them, so a CTA
-// that gave up still arrives; no CTA touches another's shared memory after the
-// last one. The exact fallback runs in CTA 0, over the row in global memory.
+// length is read. Every CTA fetches piece 0 too and seeds the threshold from
+// it as one CTA does, so all find the same one without waiting for each
+// other; every CTA filters its pieces into its own candidate regions and
+// stores its fine-bin counts into every CTA, so each finds the K-th key's fine
+// bin t on its own, with the same answer, and knows where its winners and bin
+// t entries go; it writes its winners and sends bin t's entries to CTA 0,
+// which ranks them. Two cluster barriers a row after a start barrier (two more
+// when the K-th key lies above the counted bins), taken by every thread of
+// every CTA whatever happened before them, so a CTA that gave up still
+// arrives; no CTA touches another's shared memory after the last one. The
+// exact fallback runs in CTA 0, over the row in global memory.
 
 // Every CTA of the cluster holds every CTA's counts (each CTA stores its own
-// into all of them), so each takes the same decision on its own. The fine-bin
-// counts of each CTA (two buffers: the second for a coarser recount) sit in
-// the seed histogram's space, unused from the seed's end to the exact path.
+// into all of them), so each takes the same decision on its own.
 struct SmemC : Smem {
+  alignas(16) int c_fc[kMaxCluster][kTrack];  // fine-bin counts of each CTA
   int c_nc[kMaxCluster];             // candidates of each CTA
   int c_fl[kMaxCluster];             // each CTA's flags: bit 0 a candidate region overflowed, bit 1 it gave up
   uint32_t c_mx[kMaxCluster];        // each CTA's largest candidate key
-  uint32_t c_seed[4];                // from rank 0: threshold key; 1: keys above it only; target; 1: gave up
   int c_dec[7];                      // mode, fine bin t, need (0: bin t whole), bin t's entries, bin shift,
                                      // this CTA's first output slot and first ranking slot
 };
 static_assert(sizeof(SmemC) <= 227 * 1024, "the cluster kernel's shared memory fits one SM");
-static_assert(2 * kMaxCluster * kTrack <= kBins, "the cluster's fine-bin counts fit the seed histogram");
 
-// Fine-bin count i of CTA c, buffer b.
-__device__ __forceinline__ int* cluster_fc(SmemC& s, int b, int c) {
-  return reinterpret_cast<int*>(s.hseed) + (b * kMaxCluster + c) * kTrack;
-}
+// The fine-bin counts of CTA c.
+__device__ __forceinline__ int* cluster_fc(SmemC& s, int c) { return s.c_fc[c]; }
 
 constexpr int kModeSelect = 1;  // bin t found: winners out, bin t's entries ranked in rank 0
 constexpr int kModeWide = 2;    // the K-th key lies above the counted bins: count again, coarser
@@ -1320,18 +1316,18 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Warp 0 of each CTA: the K-th key's fine bin from the counts of all C CTAs of
-// the cluster (buffer `buf`, bins of (key - thr_key) >> fsh), into c_dec; every
+// the cluster (bins of (key - thr_key) >> fsh), into c_dec; every
 // CTA reads the same counts and takes the same decision. A K-th key above the
 // counted bins asks for a recount (when `may_widen`) with the smallest shift
 // that holds the cluster's largest candidate. With bin t found, CTA me's first
 // output slot and first ranking slot follow the winners and bin t entries of
 // CTAs 0 .. me - 1.
-__device__ __forceinline__ void cluster_decide(SmemC& s, int K, int C, int me, int buf, int fsh, bool may_widen,
+__device__ __forceinline__ void cluster_decide(SmemC& s, int K, int C, int me, int fsh, bool may_widen,
                                                uint32_t thr_key) {
   const int lane = static_cast<int>(lane_id());
   int c0 = 0, c1 = 0;  // bins 2 lane and 2 lane + 1, over the cluster
   for (int c = 0; c < C; ++c) {
-    const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, buf, c) + 2 * lane);
+    const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, c) + 2 * lane);
     c0 += v.x;
     c1 += v.y;
   }
@@ -1372,10 +1368,10 @@ __device__ __forceinline__ void cluster_decide(SmemC& s, int K, int C, int me, i
   int ow = 0, os = 0;
   if (mode == kModeSelect) {
     for (int c = 0; c < me; ++c) {
-      const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, buf, c) + 2 * lane);
+      const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, c) + 2 * lane);
       const int below = static_cast<int>(__reduce_add_sync(
           0xFFFFFFFFu, static_cast<uint32_t>((2 * lane <= jt ? v.x : 0) + (2 * lane + 1 <= jt ? v.y : 0))));
-      const int bt = cluster_fc(s, buf, c)[jt];
+      const int bt = cluster_fc(s, c)[jt];
       ow += s.c_nc[c] - below + (all_t ? bt : 0);
       os += all_t ? 0 : bt;
     }
@@ -1391,14 +1387,14 @@ __device__ __forceinline__ void cluster_decide(SmemC& s, int K, int C, int me, i
   }
 }
 
-// Warp 0: this CTA's fine-bin counts (s.ftot) into buffer `buf` of every CTA of
+// Warp 0: this CTA's fine-bin counts (s.ftot) into every CTA of
 // the cluster, and with `all` its candidate count, flags and largest key.
-__device__ __forceinline__ void cluster_push_counts(SmemC& s, int C, int me, int buf, bool all, int n_c, int flags,
+__device__ __forceinline__ void cluster_push_counts(SmemC& s, int C, int me, bool all, int n_c, int flags,
                                                     uint32_t cmax) {
   const int lane = static_cast<int>(lane_id());
   const int2 v = *reinterpret_cast<const int2*>(&s.ftot[2 * lane]);
   for (int c = 0; c < C; ++c) {
-    const uint32_t a = dsmem_addr(cluster_fc(s, buf, me) + 2 * lane, static_cast<uint32_t>(c));
+    const uint32_t a = dsmem_addr(cluster_fc(s, me) + 2 * lane, static_cast<uint32_t>(c));
     dsmem_st(a, static_cast<uint32_t>(v.x));
     dsmem_st(a + 4u, static_cast<uint32_t>(v.y));
     if (all && lane == 0) {
@@ -1483,9 +1479,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
   // max_len) go out before the length is read, local piece 0 first and the
   // rest (by warp 1) after the barrier, followed by the row's own pieces up to a
   // ring's worth; local piece i (window piece me + C i) sits in slot i % kRing.
+  // A CTA other than 0 also fetches window piece 0 (the seed sample) into its
+  // last slot, so that every CTA finds the same threshold from the same bytes
+  // without waiting for CTA 0; its own piece kRing - 1 follows once the seed
+  // is read.
   const int32_t len_raw = __ldg(p.lengths + r);
   const Win wmax = make_win(p, r, static_cast<int>(p.max_len));
   const int blind = min(wmax.np > me ? (wmax.np - me + C - 1) / C : 0, kBlind);
+  const int S = me == 0 ? 0 : kRing - 1;  // the seed sample's slot
   if (warp == 0) {
     if (lane < kRing) {
       mbar_init(&s.bar[lane], 1u);
@@ -1495,9 +1496,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
     }
     if (lane == 0) s.key_max = 0;
     if (lane == 0 && blind > 0) issue_piece(s, wmax, me, 0, false);
+    if (lane == kRing - 1 && me != 0 && wmax.np > 0) issue_piece(s, wmax, 0, kRing - 1, false);
   }
-  if (me == 0)
-    for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
+  for (int b = tid; b < kBins; b += kThreads) s.hseed[b] = 0;
   for (int i = tid; i < kWarps * kTrack; i += kThreads) s.wbin[i / kTrack][i % kTrack] = 0;
   if (tid < 256) s.hsub[tid] = 0;
   if (tid < kTrack) s.ftot[tid] = 0;
@@ -1512,102 +1513,105 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
   const Win w = make_win(p, r, len);
   int32_t* o = p.out + r * static_cast<int64_t>(K);
   const int npl = w.np > me ? (w.np - me + C - 1) / C : 0;  // this CTA's pieces of the window
-  if (warp == 1 && lane >= blind && lane < min(npl, kRing)) issue_piece(s, w, me + C * lane, lane, false);
+  const int first_slots = me == 0 ? kRing : kRing - 1;      // slots free before the seed is read
+  if (warp == 1 && lane >= blind && lane < min(npl, first_slots)) issue_piece(s, w, me + C * lane, lane, false);
   bool aborted = false;
   bool drain = false;  // pieces may still be in flight at the end: wait for every slot's last copy
   if (w.nwin == 0) {
     // every CTA of the cluster reads the same length: none takes a cluster barrier
     if (me == 0)
       for (int j = tid; j < K; j += kThreads) o[j] = (j < len) ? j : -1;
+    drain = me != 0 && wmax.np > 0;  // the seed sample's copy
   } else {
     // every CTA of the cluster is running once this barrier's phase completes:
     // a CTA waits on it before its first access to another CTA's shared memory
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-    // ---- seed (rank 0): piece 0's top 12 key bits, as one CTA seeds a row; the
-    // other CTAs' pieces land meanwhile
+    // ---- seed (every CTA, from the same piece 0): its top 12 key bits, as one
+    // CTA seeds a row
     const int n_seed = min(len, kSeed - w.mis);
+    const float* seed = s.row + S * kPiece;
     int wc = 0;  // this warp's candidates
-    bool ok = true;
-    uint32_t seed_key = 0;  // rank 0: the threshold key found
-    if (me == 0) {
-      int target = K;
-      if (warp == 0 && n_seed < len) {
-        const float mu = static_cast<float>(K) * static_cast<float>(n_seed) / static_cast<float>(len);
-        target = max(1, static_cast<int>(ceilf(mu + 3.0f * sqrtf(mu) + 2.0f)));
+    int target = K;
+    if (warp == 0 && n_seed < len) {
+      const float mu = static_cast<float>(K) * static_cast<float>(n_seed) / static_cast<float>(len);
+      target = max(1, static_cast<int>(ceilf(mu + 3.0f * sqrtf(mu) + 2.0f)));
+    }
+    target = min(target, n_seed);
+    bool ok = piece_ready(s, S, 0u, p.timeout_ns);
+    const int seed_hi = min(kSeed, w.nwin);
+    uint32_t kmax = 0;
+    for (int i = tid; i < seed_hi; i += kThreads) {
+      const int e = i - w.mis;
+      if (e >= 0 && e < len) {
+        const uint32_t key = fkey(seed[i]);
+        kmax = max(kmax, key);
+        atomicAdd(&s.hseed[key >> 20], 1u);
       }
-      target = min(target, n_seed);
-      ok = piece_ready(s, 0, 0u, p.timeout_ns);
-      const int seed_hi = min(kSeed, w.nwin);
-      uint32_t kmax = 0;
-      for (int i = tid; i < seed_hi; i += kThreads) {
-        const int e = i - w.mis;
-        if (e >= 0 && e < len) {
-          const uint32_t key = fkey(s.row[i]);
-          kmax = max(kmax, key);
-          atomicAdd(&s.hseed[key >> 20], 1u);
+    }
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    if (lane == 0 && kmax) atomicMax(&s.key_max, kmax);
+    uint32_t thr_key = 0;
+    bool strict = false;  // crowded: the filter keeps keys above thr_key only
+    if (sync_or(!ok)) {
+      aborted = true;
+    } else {
+      if (warp == 0) {
+        int t0, above0;
+        warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
+        const int c0 = static_cast<int>(s.hseed[t0]);
+        const int need_in = target - above0;
+        // crowded: the seed's projection over the row overflows the cluster's
+        // candidate regions (heavy ties); wide: refine inside the seed bin
+        const int at_or_above = above0 + c0;
+        const bool crowded = n_seed >= K && at_or_above >= K &&
+                             static_cast<int64_t>(at_or_above) * len > (3ll * kCand / 4) * C * n_seed;
+        const bool refine = !crowded && c0 - need_in > max(target / 4, 16);
+        if (lane == 0) {
+          s.target = target;
+          s.t0 = t0;
+          s.crowded = crowded ? 1 : 0;
+          s.refine = refine ? 1 : 0;
+          s.need_in = need_in;
+          s.thr_key = static_cast<uint32_t>(t0) << 20;
         }
       }
-      kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-      if (lane == 0 && kmax) atomicMax(&s.key_max, kmax);
-      if (sync_or(!ok)) {
-        aborted = true;
-      } else {
-        if (warp == 0) {
-          int t0, above0;
-          warp_scan_down(s.hseed, static_cast<int>(s.key_max >> 20), target, t0, above0);
-          const int c0 = static_cast<int>(s.hseed[t0]);
-          const int need_in = target - above0;
-          // crowded: the seed's projection over the row overflows the cluster's
-          // candidate regions (heavy ties); wide: refine inside the seed bin
-          const int at_or_above = above0 + c0;
-          const bool crowded = n_seed >= K && at_or_above >= K &&
-                               static_cast<int64_t>(at_or_above) * len > (3ll * kCand / 4) * C * n_seed;
-          const bool refine = !crowded && c0 - need_in > max(target / 4, 16);
-          if (lane == 0) {
-            s.target = target;
-            s.t0 = t0;
-            s.crowded = crowded ? 1 : 0;
-            s.refine = refine ? 1 : 0;
-            s.need_in = need_in;
-            s.thr_key = static_cast<uint32_t>(t0) << 20;
+      __syncthreads();
+      if (s.refine) {
+        const uint32_t t0 = static_cast<uint32_t>(s.t0);
+        for (int i = tid; i < seed_hi; i += kThreads) {
+          const int e = i - w.mis;
+          if (e >= 0 && e < len) {
+            const uint32_t key = fkey(seed[i]);
+            if ((key >> 20) == t0) atomicAdd(&s.hsub[(key >> 12) & 0xFFu], 1u);
           }
         }
         __syncthreads();
-        if (s.refine) {
-          const uint32_t t0 = static_cast<uint32_t>(s.t0);
-          for (int i = tid; i < seed_hi; i += kThreads) {
-            const int e = i - w.mis;
-            if (e >= 0 && e < len) {
-              const uint32_t key = fkey(s.row[i]);
-              if ((key >> 20) == t0) atomicAdd(&s.hsub[(key >> 12) & 0xFFu], 1u);
-            }
-          }
-          __syncthreads();
-          if (warp == 0) {
-            int above_b;
-            const int b = warp_find256(s.hsub, s.need_in, above_b);
-            if (lane == 0) s.thr_key = (t0 << 20) | (static_cast<uint32_t>(b) << 12);
-          }
-          __syncthreads();
-          if (tid < 256) s.hsub[tid] = 0;  // clear again for the ranking (read after later barriers)
+        if (warp == 0) {
+          int above_b;
+          const int b = warp_find256(s.hsub, s.need_in, above_b);
+          if (lane == 0) s.thr_key = (t0 << 20) | (static_cast<uint32_t>(b) << 12);
         }
-        seed_key = s.thr_key;
-        if (s.crowded) seed_key = crowded_seed(s, 0, w.mis, n_seed, len, K, wc);  // every thread gets T
+        __syncthreads();
+        if (tid < 256) s.hsub[tid] = 0;  // clear again for the ranking (read after later barriers)
       }
+      thr_key = s.thr_key;
+      target = s.target;
+      strict = s.crowded != 0;
+      if (strict) {
+        // the seed's K-th key T, exactly (every thread gets it); CTA 0, which
+        // owns piece 0, also takes the seed's ties as its candidates
+        if (me == 0) {
+          thr_key = crowded_seed(s, 0, w.mis, n_seed, len, K, wc);
+        } else {
+          int need_t, equal_t;
+          thr_key = exact_kth(s, Src{nullptr, 1, S * (kPiece / 4), len}, w.mis, n_seed, K, need_t, equal_t);
+        }
+      }
+      __syncthreads();  // the seed sample is read: its slot takes the CTA's own piece kRing - 1
+      if (me != 0 && tid == 0 && npl > kRing - 1) issue_piece(s, w, me + C * (kRing - 1), kRing - 1, true);
     }
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    if (me == 0 && tid < C) {
-      // the seed into every CTA of the cluster (thread c: CTA c)
-      const uint32_t v[4] = {aborted ? 0u : seed_key, aborted ? 0u : static_cast<uint32_t>(s.crowded),
-                             aborted ? 0u : static_cast<uint32_t>(s.target), aborted ? 1u : 0u};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dsmem_st(dsmem_addr(&s.c_seed[k], static_cast<uint32_t>(tid)), v[k]);
-    }
-    cluster_sync_all();  // the seed is out
-    const bool seed_ok = s.c_seed[3] == 0u;
-    drain = !seed_ok;  // this CTA's pieces were issued but are not read
-    const uint32_t thr_key = s.c_seed[0];
-    const float thr = key_floor_value(s.c_seed[1] ? thr_key + 1u : thr_key);  // crowded: keys above T only
+    const bool seed_ok = !aborted;
+    const float thr = key_floor_value(strict ? thr_key + 1u : thr_key);
     const int base = warp * kRegion;
     int* my_bins = s.wbin[warp];
     uint32_t kmx = 0;  // this lane's largest candidate key
@@ -1616,7 +1620,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
       // one CTA chooses it for its share; lane l takes float4s l, l + 32, ... of a
       // task. Local piece i hands its slot to local piece i + kRing once its
       // tasks are done.
-      const int target = static_cast<int>(s.c_seed[2]);
       const int nvec = w.nwin >> 2;
       int F = 8;
       while (F > 1 && (static_cast<int64_t>(128 * F) * target > static_cast<int64_t>(kTaskSurvivors) * n_seed ||
@@ -1635,7 +1638,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
         const int jl = task / tpp;             // local piece
         const int j = me + C * jl;             // window piece
         const int q = jl % kRing;              // its slot
-        if (!piece_ready(s, q, static_cast<uint32_t>(jl / kRing) & 1u, p.timeout_ns)) {
+        // the slot's copies so far: earlier local pieces in it, and (CTAs other
+        // than 0, last slot) the seed sample before them
+        const uint32_t phase = static_cast<uint32_t>(jl / kRing + ((me != 0 && q == kRing - 1) ? 1 : 0));
+        if (!piece_ready(s, q, phase & 1u, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -1723,15 +1729,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
     if (lane == 0 && kmx) atomicMax(&s.cmax, kmx);
     if (sync_or(!ok)) aborted = true;
     // ---- this CTA's counts into every CTA of the cluster (warp 0; lane l: warp l's
-    // count, fine bins 2l and 2l + 1); then each CTA finds bin t on its own
+    // count, fine bins 2l and 2l + 1); then each CTA finds bin t on its own. The
+    // start-up phase of the cluster barrier completes first: every CTA runs.
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     if (warp == 0) {
       const int n_l = lane < kWarps ? s.wcnt[lane] : 0;
       const bool over = __any_sync(0xFFFFFFFFu, n_l > kRegion);
       const int n_c = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(n_l)));
-      cluster_push_counts(s, C, me, 0, true, n_c, (over ? 1 : 0) | (aborted ? 2 : 0), s.cmax);
+      cluster_push_counts(s, C, me, true, n_c, (over ? 1 : 0) | (aborted ? 2 : 0), s.cmax);
     }
     cluster_sync_all();  // every CTA's counts are in every CTA
-    if (warp == 0) cluster_decide(s, K, C, me, 0, kFine, true, thr_key);
+    if (warp == 0) cluster_decide(s, K, C, me, kFine, true, thr_key);
     __syncthreads();
     int mode = s.c_dec[0];
     int fsh = kFine;  // fine bin of a candidate: (key - thr_key) >> fsh
@@ -1750,10 +1758,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
         if (v2.x) atomicAdd(&s.ftot[2 * lane], v2.x);
         if (v2.y) atomicAdd(&s.ftot[2 * lane + 1], v2.y);
       }
-      __syncthreads();
-      if (warp == 0) cluster_push_counts(s, C, me, 1, false, 0, 0, 0u);
+      cluster_sync_all();  // every CTA has read the first counts: they may be overwritten
+      if (warp == 0) cluster_push_counts(s, C, me, false, 0, 0, 0u);
       cluster_sync_all();  // every CTA's recount is in every CTA
-      if (warp == 0) cluster_decide(s, K, C, me, 1, fsh, false, thr_key);
+      if (warp == 0) cluster_decide(s, K, C, me, fsh, false, thr_key);
       __syncthreads();
       mode = s.c_dec[0];
     }
