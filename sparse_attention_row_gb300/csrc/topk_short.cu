@@ -1274,8 +1274,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
 // into all of them), so each takes the same decision on its own.
 struct SmemC : Smem {
   alignas(16) int c_fc[kMaxCluster][kTrack];  // fine-bin counts of each CTA
-  int c_nc[kMaxCluster];             // candidates of each CTA
-  int c_fl[kMaxCluster];             // each CTA's flags: bit 0 a candidate region overflowed, bit 1 it gave up
+  int c_nc[kMaxCluster];             // each CTA's count word: candidates, region overflow, gave up
   uint32_t c_mx[kMaxCluster];        // each CTA's largest candidate key
   int c_dec[7];                      // mode, fine bin t, need (0: bin t whole), bin t's entries, bin shift,
                                      // this CTA's first output slot and first ranking slot
@@ -1326,14 +1325,18 @@ __device__ __forceinline__ void cluster_decide(SmemC& s, int K, int C, int me, i
                                                uint32_t thr_key) {
   const int lane = static_cast<int>(lane_id());
   int c0 = 0, c1 = 0;  // bins 2 lane and 2 lane + 1, over the cluster
+  int below = 0;       // packed: the earlier CTAs' candidates in bins up to t (low 16 bits) and in t (high)
   for (int c = 0; c < C; ++c) {
     const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, c) + 2 * lane);
     c0 += v.x;
     c1 += v.y;
   }
-  const int n_c = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, lane < C ? static_cast<uint32_t>(s.c_nc[lane]) : 0u));
-  const uint32_t flags = __reduce_or_sync(0xFFFFFFFFu, lane < C ? static_cast<uint32_t>(s.c_fl[lane]) : 0u);
-  const uint32_t cmax = __reduce_max_sync(0xFFFFFFFFu, lane < C ? s.c_mx[lane] : 0u);
+  // lane c < C: CTA c's packed count word (see cluster_push_counts); the sum
+  // carries the candidates and how many CTAs overflowed or gave up
+  const uint32_t word_l = lane < C ? static_cast<uint32_t>(s.c_nc[lane]) : 0u;
+  const uint32_t sum = __reduce_add_sync(0xFFFFFFFFu, word_l);
+  const int n_c = static_cast<int>(sum & 0xFFFFFFu);
+  const uint32_t flags = ((sum >> 24) & 0xFu ? 1u : 0u) | ((sum >> 28) ? 2u : 0u);
   const int skip = n_c - K;  // the K-th key's bin: the first whose prefix (from bin 0) passes skip
   const int pair = c0 + c1;
   int incl = pair;
@@ -1361,20 +1364,25 @@ __device__ __forceinline__ void cluster_decide(SmemC& s, int K, int C, int me, i
     mode = kModeWide;
   int fsh2 = fsh;
   if (mode == kModeWide) {
+    const uint32_t cmax = __reduce_max_sync(0xFFFFFFFFu, lane < C ? s.c_mx[lane] : 0u);
     const uint32_t span = cmax - thr_key;
     while ((span >> fsh2) >= static_cast<uint32_t>(kTrack)) ++fsh2;
   }
-  // the winners (bins above t, and t when taken whole) and bin t entries of CTAs before this one
+  // the winners (bins above t, and t when taken whole) and bin t entries of the
+  // CTAs before this one: one packed sum of their bins up to t and in t, and one
+  // of their candidates
   int ow = 0, os = 0;
   if (mode == kModeSelect) {
     for (int c = 0; c < me; ++c) {
       const int2 v = *reinterpret_cast<const int2*>(cluster_fc(s, c) + 2 * lane);
-      const int below = static_cast<int>(__reduce_add_sync(
-          0xFFFFFFFFu, static_cast<uint32_t>((2 * lane <= jt ? v.x : 0) + (2 * lane + 1 <= jt ? v.y : 0))));
-      const int bt = cluster_fc(s, c)[jt];
-      ow += s.c_nc[c] - below + (all_t ? bt : 0);
-      os += all_t ? 0 : bt;
+      below += (2 * lane <= jt ? v.x : 0) + (2 * lane + 1 <= jt ? v.y : 0) +
+               (((2 * lane == jt ? v.x : 0) + (2 * lane + 1 == jt ? v.y : 0)) << 16);
     }
+    const uint32_t bsum = __reduce_add_sync(0xFFFFFFFFu, static_cast<uint32_t>(below));
+    const int n_before = static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, lane < me ? word_l & 0xFFFFFFu : 0u));
+    const int bt = static_cast<int>(bsum >> 16);
+    ow = n_before - static_cast<int>(bsum & 0xFFFFu) + (all_t ? bt : 0);
+    os = all_t ? 0 : bt;
   }
   if (lane == 0) {
     s.c_dec[0] = mode;
@@ -1393,13 +1401,17 @@ __device__ __forceinline__ void cluster_push_counts(SmemC& s, int C, int me, boo
                                                     uint32_t cmax) {
   const int lane = static_cast<int>(lane_id());
   const int2 v = *reinterpret_cast<const int2*>(&s.ftot[2 * lane]);
+  // the count word: candidates (saturated at 2^20: more overflow the regions
+  // anyway) in bits 0..23, 1 in bit 24 for an overflow and in bit 28 for a CTA
+  // that gave up, so that a sum over 8 CTAs keeps every field apart
+  const uint32_t word = static_cast<uint32_t>(min(n_c, 1 << 20)) | ((flags & 1) ? 1u << 24 : 0u) |
+                        ((flags & 2) ? 1u << 28 : 0u);
   for (int c = 0; c < C; ++c) {
     const uint32_t a = dsmem_addr(cluster_fc(s, me) + 2 * lane, static_cast<uint32_t>(c));
     dsmem_st(a, static_cast<uint32_t>(v.x));
     dsmem_st(a + 4u, static_cast<uint32_t>(v.y));
     if (all && lane == 0) {
-      dsmem_st(dsmem_addr(&s.c_nc[me], static_cast<uint32_t>(c)), static_cast<uint32_t>(n_c));
-      dsmem_st(dsmem_addr(&s.c_fl[me], static_cast<uint32_t>(c)), static_cast<uint32_t>(flags));
+      dsmem_st(dsmem_addr(&s.c_nc[me], static_cast<uint32_t>(c)), word);
       dsmem_st(dsmem_addr(&s.c_mx[me], static_cast<uint32_t>(c)), cmax);
     }
   }
