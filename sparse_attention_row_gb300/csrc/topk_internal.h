@@ -48,12 +48,13 @@ constexpr int kShort16CtaThreads = 512;
 constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds resident in its ring
 constexpr int64_t kShortSeedLen = 2048;  // elements it samples for its threshold (rows this short: all of them)
 // Rows at least this long, too few to give every SM its own, are split over a
-// thread-block cluster of the short-row kernel: measured on a GB300 (bench.py
-// --sweep, TopK 2048), a cluster of 2 .. 8 CTAs finishes 65536-element rows in
-// 14.3 us against 16.4 us whole (131072: 14.6 to 20.5 against 22.5; 2^20: 21.9
-// against 41.1 for the other kernel's split), and loses on shorter rows (16384:
-// 14.3 against 12.3), where its merge costs more than the streaming it shares.
-constexpr int64_t kShortClusterStride = 65536;
+// thread-block cluster of the short-row kernel (16 warps per CTA): measured on
+// a GB300 (bench.py --sweep, TopK 2048), clusters of 2 .. 8 CTAs finish
+// 32768-element rows in 12.3 us against 14.1 to 14.3 us whole (1 to 16 rows;
+// 64 rows tie), 65536-element rows in 12.3 against 16.4 us, 2^20 in 20.6
+// against 41.2 us for the other kernel's split; on shorter rows they gain
+// nothing (8192, 16384: 12.3 either way).
+constexpr int64_t kShortClusterStride = 32768;
 // The short-row kernel samples 2048 elements for its threshold, so on long
 // rows the threshold keeps many more candidates than TopK (expected count:
 // short_row_candidates). A CTA that streams its row is planned at most this

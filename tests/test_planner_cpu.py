@@ -340,12 +340,13 @@ def test_short_row_cluster_split():
     for rows, stride, k, g in ((16, 131072, 2048, 6),   # long_coop: 8 and 7 hold only 15 clusters
                                (64, 163840, 1024, 2),   # mtp
                                (4, 65536, 2048, 8), (16, 65536, 2048, 6), (1, 500000, 512, 8),
-                               (76, 131072, 2048, 2), (28, 100000, 2048, 5), (30, 100000, 2048, 4), (40, 100000, 2048, 3)):
+                               (76, 131072, 2048, 2), (28, 100000, 2048, 5), (30, 100000, 2048, 4), (40, 100000, 2048, 3),
+                               (64, 32768, 2048, 2), (16, 32768, 2048, 6)):  # decode_batch: a tie, measured
         rc, pl = plan(gb, rows, stride, topk=k)
         assert rc == 0 and pl.shape == 4 and pl.ctas_per_group == g and pl.cluster, (rows, stride, k, pl.ctas_per_group)
         assert pl.grid == rows * g and pl.num_groups == rows and not pl.cooperative and pl.threads == 1024
     # whole rows: shorter rows, enough rows for every SM, very long rows
-    for rows, stride, k in ((64, 32768, 2048), (8, 4096, 512), (16, 65535, 2048), (77, 131072, 2048),
+    for rows, stride, k in ((64, 32767, 2048), (8, 4096, 512), (16, 16384, 2048), (77, 131072, 2048),
                             (4096, 65536, 2048)):
         rc, pl = plan(gb, rows, stride, topk=k)
         assert rc == 0 and pl.ctas_per_group == 1 and not pl.cluster, (rows, stride, k)
@@ -392,7 +393,8 @@ def test_short_row_kernel_with_16_warps():
     on a GB300)."""
     gb = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT,
                short_clusters=gb300_clusters(), short16=GB300_SHORT, short16_clusters=gb300_clusters())
-    for rows, stride, k, shape, g in ((8, 4096, 512, 5, 1), (152, 2048, 1024, 5, 1), (64, 32768, 2048, 4, 1),
+    for rows, stride, k, shape, g in ((8, 4096, 512, 5, 1), (152, 2048, 1024, 5, 1), (64, 32768, 2048, 5, 2),
+                                      (152, 32768, 2048, 4, 1),
                                       (64, 16384, 512, 5, 1), (64, 16384, 1024, 4, 1), (64, 16385, 512, 4, 1),
                                       (4096, 65536, 2048, 4, 1), (16, 131072, 2048, 5, 6), (64, 163840, 1024, 5, 2),
                                       (608, 4096, 512, 2, 1), (64, 4096, 2048, 1, 1)):
@@ -403,8 +405,8 @@ def test_short_row_kernel_with_16_warps():
     # forced: the 16-warp instance whole or split, like shape 4
     rc, pl = plan(gb, 10, 30000, shape=5, force_ctas_per_group=3)
     assert rc == 0 and pl.shape == 5 and pl.ctas_per_group == 3 and pl.cluster and pl.grid == 30
-    rc, pl = plan(gb, 64, 32768, shape=5)
-    assert rc == 0 and pl.shape == 5 and pl.ctas_per_group == 1 and pl.grid == 64
+    rc, pl = plan(gb, 152, 32768, shape=5)
+    assert rc == 0 and pl.shape == 5 and pl.ctas_per_group == 1 and pl.grid == 152
     assert plan(gb, 10, 30000, shape=5, force_ctas_per_group=9)[0] == sar.TOPK_ERR_INVALID_ARG
     # a device without the 16-warp instance splits on the 32-warp one
     gb32 = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT,
