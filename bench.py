@@ -145,29 +145,32 @@ def read_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no measured peak file)"
 
 
-def read_traffic(workload: str) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+def read_traffic(workload: str, plan: str | None = None) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged since
+    and the workload is still planned as it was then (plan: "shape:ctas_per_row")."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     src_hash = kernel_source_hash()
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[2] == src_hash:
+        if (len(parts) >= 4 and not line.startswith("#") and parts[0] == workload and parts[2] == src_hash and
+                (plan is None or parts[3] == plan)):
             return float(parts[1])
     return None
 
 
 def kernel_source_hash(csrc: str | None = None) -> str:
     """Hash of the library's code with comments and blank lines removed, so that
-    a comment edit does not void a DRAM traffic record taken on the same code."""
+    a comment edit does not void a DRAM traffic record taken on the same code. The
+    planner is left out: a traffic record also names the plan it was taken with."""
     import hashlib
     import re
 
     h = hashlib.sha256()
     csrc = csrc or os.path.join(ROOT, "sparse_attention_row_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".h", ".cpp", ".cuh")):
+        if name.endswith((".cu", ".h", ".cpp", ".cuh")) and name != "planner.cpp":
             text = open(os.path.join(csrc, name), encoding="utf-8").read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
@@ -273,6 +276,7 @@ class GpuBench:
         if rc != 0:
             return {"error": self.sar.topk_status_string(rc)}
         merge = "cluster" if pl.cluster else ("workspace" if pl.ctas_per_group > 1 else "none")
+        plan_id = f"{pl.shape}:{pl.ctas_per_group}"
         shape = {1: "wide (24 consumer warps, 1 CTA/SM)", 2: "paired (12 consumer warps, 2 CTAs/SM)",
                  3: "small (8 consumer warps)",
                  4: "short-row (32 warps, 1 CTA/SM, row resident in or streamed through a 128 KB ring)",
@@ -282,7 +286,7 @@ class GpuBench:
             warps = 32 if pl.shape == 4 else 16
             shape = (f"short-row cluster ({pl.ctas_per_group} CTAs of {warps} warps per row, CTA c streaming "
                      f"pieces c, c + {pl.ctas_per_group}, ... through its 128 KB ring)")
-        return {"ctas_per_row": pl.ctas_per_group, "grid": pl.grid, "merge": merge, "shape": shape}
+        return {"ctas_per_row": pl.ctas_per_group, "grid": pl.grid, "merge": merge, "shape": shape, "id": plan_id}
 
     def flush_l2(self):
         """Evicts the inputs from L2: writes a buffer larger than L2, then reads it
@@ -591,7 +595,7 @@ def run_ours(args) -> None:
         "us_per_call": ms * 1e3,
         "effective_gbs": gbs,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "traffic": read_traffic(HEADLINE), "peak_source": peak_src,
+                     "traffic": read_traffic(HEADLINE, table[HEADLINE]["plan"].get("id")), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": vbytes},
         "cpu_baseline": None if args.no_cpu else {
             "value": head_cpu["rows_per_s"], "unit": "rows/s", "cores": head_cpu["cores"], "kind": "oracle",

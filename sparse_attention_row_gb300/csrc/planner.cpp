@@ -53,6 +53,55 @@
 #include "libtopk.h"
 #include "topk_internal.h"
 
+namespace ltk {
+
+// The planner's rules, from sweeps on a GB300 (bench.py --sweep; the tables
+// behind them are in profiles/planner_sweep.md).
+constexpr int kMinSpan = 8192;                      // fewest elements per CTA when a row is split
+constexpr int64_t kDefaultLongRowThreshold = 32768;  // rows longer than this may be split (wide shape)
+constexpr int64_t kSplitGain = 90000;         // elements a workspace-merged split must save per CTA (measured)
+constexpr int64_t kSplitGainCluster = 24000;  // elements a cluster-merged split must save per CTA
+constexpr int64_t kPairRowsPerSm = 4;         // rows per SM from which the paired shape is planned
+constexpr int64_t kPairMaxStride = 16384;     // ... for rows up to this long (longer: the short-row kernel)
+constexpr int64_t kShortMaxLen = 32768;       // longest row the short-row kernel holds resident in its ring
+constexpr int64_t kShortSeedLen = 2048;       // elements it samples for its threshold (rows this short: all)
+// Rows at least this long, too few to give every SM its own, are split over a
+// thread-block cluster of the short-row kernel (16 warps per CTA): clusters of
+// 2 .. 8 CTAs finish 32768-element rows in 12.3 us against 14.1 to 14.3 us
+// whole (1 to 16 rows; 64 rows tie), 65536-element rows in 12.3 against 16.4
+// us, 2^20 in 20.6 against 41.2 us for the other kernel's split; on shorter
+// rows they gain nothing (8192, 16384: 12.3 either way).
+constexpr int64_t kShortClusterStride = 32768;
+// The short-row kernel samples 2048 elements for its threshold, so on long
+// rows the threshold keeps many more candidates than TopK (expected count:
+// short_row_candidates). A CTA that streams its row is planned at most this
+// many: more overflow its candidate regions now and then, and the exact
+// fallback that follows reads the row from global memory several times (TopK
+// 2048, four rows of 2^20 elements whole, about 6100 candidates each, 654 us,
+// split over clusters of 8 CTAs 22 us; TopK 4096, 64 rows of 65536, about 5200
+// each, 73.7 us whole, 16.6 us over clusters of 2).
+constexpr double kShortMaxCandidates = 4096.0;
+// Longest row the short-row kernel is planned to select whole: beyond it the
+// 2048-element sample holds so few of the row's TopK best that its threshold
+// scatters widely (TopK 512, rows of 2^20: 706 us whole against 476 us on the
+// wide shape; TopK 2048, 2^19: 354 us against 66 us), while 2^18 still wins
+// (TopK 2048, 152 rows: 36.9 us against 45.1 us).
+constexpr int64_t kShortMaxWholeStride = 1 << 18;
+// Longest rows planned whole on the 16-warp instance of the short-row kernel,
+// at any TopK and at TopK up to kShort16LongTopK (TopK 512 of 4096-element
+// rows 10.2 against 11.8 us, of 16384 10.2 to 12.3 against 10.3 to 12.3; TopK
+// 2048 of 16384 14.3 against 12.3 us).
+constexpr int64_t kShort16MaxStride = 4096;
+constexpr int64_t kShort16MaxLongStride = 16384;
+constexpr int kShort16LongTopK = 512;
+// Largest share of a row (elements per CTA) planned on the 16-warp instance
+// when rows are split over clusters; larger shares stream faster on 32 warps
+// (81920 per CTA, mtp, 19.1 against 20.8 us on 16 warps; 131072 per CTA, one
+// row of 2^20 over 8 CTAs, 22.1 against 20.5 us).
+constexpr int64_t kShort16MaxShare = 98304;
+
+}  // namespace ltk
+
 namespace {
 
 bool topk_supported(int topk) { return topk >= 1 && topk <= ltk::kWideMaxTopK; }
@@ -136,8 +185,13 @@ extern "C" int topk_make_plan(const topk_device_props* props, int64_t num_rows, 
     return (g >= 2 && candidates / static_cast<double>(g) <= ltk::kShortMaxCandidates) ? g : 0;
   };
   // the split runs on the 16-warp instance where the device holds it (faster:
-  // mtp 19.1 against 20.8 us, long_coop 15.0 against 15.5 us on a GB300)
-  const int split_shape = short16_ok ? ltk::kShapeShort16 : ltk::kShapeShort;
+  // mtp 19.1 against 20.8 us, long_coop 15.0 against 15.5 us on a GB300),
+  // unless each CTA's share of the row is large
+  int split_shape = short16_ok ? ltk::kShapeShort16 : ltk::kShapeShort;
+  if (split_shape == ltk::kShapeShort16 && short_ok) {
+    const int64_t g16 = short_cluster_size(ltk::kShapeShort16);
+    if (g16 >= 2 && row_stride > ltk::kShort16MaxShare * g16) split_shape = ltk::kShapeShort;
+  }
   // whole rows: resident in the short-row kernel's ring (an overflow of its
   // candidate regions then costs an exact pass over the ring: TopK 4096 of
   // 32768, 16.4 us against 22.5 us on the wide shape), or streamed with their

@@ -18,12 +18,6 @@ constexpr int kMaxGroup = 16;          // CTAs that may split one row
 constexpr int kMaxCluster = 8;         // CTAs of a group that may form one thread-block cluster
 constexpr int kLenCache = 64;          // row lengths cached in shared memory
 constexpr int kSmallSet = 64;          // candidate sets up to this size are ranked by one warp
-constexpr int kMinSpan = 8192;         // fewest elements per CTA when a row is split
-constexpr int64_t kDefaultLongRowThreshold = 32768;
-constexpr int64_t kSplitGain = 90000;         // elements a workspace-merged split must save per CTA (measured)
-constexpr int64_t kSplitGainCluster = 24000;  // elements a cluster-merged split must save per CTA
-constexpr int64_t kPairRowsPerSm = 4;         // rows per SM from which the paired shape is planned
-constexpr int64_t kPairMaxStride = 16384;     // ... for rows up to this long (longer: the short-row kernel)
 constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 // CTA shapes. kShapeWide: one CTA of 24 consumer warps per SM (any row split).
@@ -32,8 +26,8 @@ constexpr uint64_t kDefaultTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 // kShapeSmall: 8 consumer warps in about 83 KB of shared memory, whole rows
 // only, for devices or partitions with less shared memory per block.
 // kShapeShort: the short-row kernel (topk_short.cu), one CTA of 32 warps per
-// SM; a row of at most kShortMaxLen elements stays resident in its 128 KB ring,
-// a longer one streams through it. kShapeShort16: the same kernel with 16
+// SM; a row of at most 32768 elements (16 pieces) stays resident in its 128 KB
+// ring, a longer one streams through it. kShapeShort16: the same kernel with 16
 // warps per CTA (topk_short16.cu).
 constexpr int kShapeWide = 1;
 constexpr int kShapePair = 2;
@@ -45,38 +39,6 @@ constexpr int kPairCtaThreads = 416;   // 12 consumer warps + the copy warp
 constexpr int kSmallCtaThreads = 288;  // 8 consumer warps + the copy warp
 constexpr int kShortCtaThreads = 1024;
 constexpr int kShort16CtaThreads = 512;
-constexpr int64_t kShortMaxLen = 32768;  // longest row the short-row kernel holds resident in its ring
-constexpr int64_t kShortSeedLen = 2048;  // elements it samples for its threshold (rows this short: all of them)
-// Rows at least this long, too few to give every SM its own, are split over a
-// thread-block cluster of the short-row kernel (16 warps per CTA): measured on
-// a GB300 (bench.py --sweep, TopK 2048), clusters of 2 .. 8 CTAs finish
-// 32768-element rows in 12.3 us against 14.1 to 14.3 us whole (1 to 16 rows;
-// 64 rows tie), 65536-element rows in 12.3 against 16.4 us, 2^20 in 20.6
-// against 41.2 us for the other kernel's split; on shorter rows they gain
-// nothing (8192, 16384: 12.3 either way).
-constexpr int64_t kShortClusterStride = 32768;
-// The short-row kernel samples 2048 elements for its threshold, so on long
-// rows the threshold keeps many more candidates than TopK (expected count:
-// short_row_candidates). A CTA that streams its row is planned at most this
-// many: more overflow its candidate regions now and then, and the exact
-// fallback that follows reads the row from global memory several times
-// (measured on a GB300: TopK 2048, four rows of 2^20 elements whole, about
-// 6100 candidates each, 654 us, split over clusters of 8 CTAs 22 us; TopK 4096,
-// 64 rows of 65536, about 5200 each, 73.7 us whole, 16.6 us over clusters of 2).
-constexpr double kShortMaxCandidates = 4096.0;
-// Longest row the short-row kernel is planned to select whole: beyond it the
-// 2048-element sample holds so few of the row's TopK best that its threshold
-// scatters widely (TopK 512, rows of 2^20: 706 us whole against 476 us on the
-// wide shape; TopK 2048, 2^19: 354 us against 66 us), while 2^18 still wins
-// (TopK 2048, 152 rows: 36.9 us against 45.1 us).
-constexpr int64_t kShortMaxWholeStride = 1 << 18;
-// Longest rows planned whole on the 16-warp instance of the short-row kernel,
-// at any TopK and at TopK up to kShort16LongTopK (measured on a GB300, bench.py
-// --sweep: TopK 512 of 4096-element rows 10.2 against 11.8 us, of 16384 10.2
-// to 12.3 against 10.3 to 12.3; TopK 2048 of 16384 14.3 against 12.3 us).
-constexpr int64_t kShort16MaxStride = 4096;
-constexpr int64_t kShort16MaxLongStride = 16384;
-constexpr int kShort16LongTopK = 512;
 
 // Per row group exchange area. Everything but the status word returns to zero
 // at the end of every launch that completes.

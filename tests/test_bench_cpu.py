@@ -55,6 +55,7 @@ def test_peaks_and_traffic_records():
     assert peak > 1000
     # the committed traffic record matches the current kernel sources or is dropped
     t = bench.read_traffic("decode_batch")
+    assert bench.read_traffic("decode_batch", "9:9") is None  # another plan: no record
     assert t is None or t > 5e6
 
 

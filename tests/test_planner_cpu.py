@@ -408,6 +408,11 @@ def test_short_row_kernel_with_16_warps():
     rc, pl = plan(gb, 152, 32768, shape=5)
     assert rc == 0 and pl.shape == 5 and pl.ctas_per_group == 1 and pl.grid == 152
     assert plan(gb, 10, 30000, shape=5, force_ctas_per_group=9)[0] == sar.TOPK_ERR_INVALID_ARG
+    # rows whose share per CTA exceeds 98304 elements split on the 32-warp instance
+    for rows, stride, shape, g in ((1, 1 << 20, 4, 8), (16, 1 << 21, 4, 6), (1, 524288, 5, 8), (64, 196608, 5, 2),
+                                   (64, 196609, 4, 2)):
+        rc, pl = plan(gb, rows, stride)
+        assert rc == 0 and pl.shape == shape and pl.ctas_per_group == g, (rows, stride, pl.shape, pl.ctas_per_group)
     # a device without the 16-warp instance splits on the 32-warp one
     gb32 = props(clusters=gb300_clusters(), pair=GB300_PAIR, small=GB300_SMALL, short=GB300_SHORT,
                  short_clusters=gb300_clusters())
