@@ -78,6 +78,10 @@ constexpr int kTaskSurvivors = 128;                 // expected survivors a filt
 constexpr int kMinTasks = 8;                        // filter tasks a window is split into at least
 constexpr int kRefineExcess = 256;                  // a resident row refines its seed bin only when that
                                                     // keeps more than this many extra survivors out
+constexpr int kClusterRefineExcess = 2048;          // ... a split row only when it keeps more than this
+                                                    // many out of each CTA (a refined, tighter threshold
+                                                    // falls short of K survivors more often, and the
+                                                    // exact path then reads the row from global memory)
 static_assert(kRing <= 32, "slot phases fit one 32-bit mask");
 constexpr int kRingF4 = kRing * kPiece / 4;        // float4s in the ring
 static_assert(kWarps <= 32, "one lane of warp 0 per warp when counts are gathered");
@@ -1573,11 +1577,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
         const int c0 = static_cast<int>(s.hseed[t0]);
         const int need_in = target - above0;
         // crowded: the seed's projection over the row overflows the cluster's
-        // candidate regions (heavy ties); wide: refine inside the seed bin
+        // candidate regions (heavy ties); wide: refine inside the seed bin when
+        // its extra entries would crowd the CTAs' regions
         const int at_or_above = above0 + c0;
         const bool crowded = n_seed >= K && at_or_above >= K &&
                              static_cast<int64_t>(at_or_above) * len > (3ll * kCand / 4) * C * n_seed;
-        const bool refine = !crowded && c0 - need_in > max(target / 4, 16);
+        const bool refine = !crowded && c0 - need_in > max(target / 4, 16) &&
+                            static_cast<int64_t>(c0 - need_in) * len >
+                                static_cast<int64_t>(kClusterRefineExcess) * C * n_seed;
         if (lane == 0) {
           s.target = target;
           s.t0 = t0;
