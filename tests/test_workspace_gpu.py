@@ -123,3 +123,25 @@ def test_timed_out_cluster_sync_reports_and_every_cta_leaves(rn, G):
     got = rn.run(w.logits, w.lengths, w.topk, options=rn.options(force_ctas_per_group=G, merge=2))
     assert_matches_oracle(w.logits, w.lengths, got, w.topk, label=f"cluster G={G} after recovery")
     assert rn.workspace_clean()
+
+
+@pytest.mark.parametrize("shape,G,name,rows", [(5, 2, "decode_batch", 8), (5, 6, "long_coop", 4), (4, 3, "mtp", 4),
+                                               (4, 1, "decode_batch", 8), (5, 1, "decode_batch", 8)])
+def test_short_row_cta_that_gives_up_leaves_cleanly(rn, shape, G, name, rows):
+    """A short-row CTA that gives up (host-chosen: it treats its first copy as late, after the copy
+    has landed) flags TOPK_DEV_STAGE_TIMEOUT and leaves row 0 unwritten; with a split row every CTA
+    of its cluster leaves through the same barriers, and every other row is selected exactly."""
+    sar = rn.sar
+    w = workloads.make(name, rows)
+    assert w.lengths[0] > w.topk  # row 0 reaches the copy wait
+    rn.sel.reset()
+    opts = rn.options(shape=shape, force_ctas_per_group=G, inject_skip_arrival=3)
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=opts, check_status=False)
+    st = rn.sel.status()
+    assert st & sar.TOPK_DEV_STAGE_TIMEOUT, f"status {st:#x}"
+    assert not st & sar.TOPK_DEV_BARRIER_TIMEOUT, f"status {st:#x}"
+    assert (got[0] == -7).all(), "the row of the CTA that gave up is left as it was"
+    assert_matches_oracle(w.logits[1:], w.lengths[1:], got[1:], w.topk, label=f"{name} other rows")
+    rn.sel.reset()
+    got = rn.run(w.logits, w.lengths, w.topk, w.next_n, options=rn.options(shape=shape, force_ctas_per_group=G))
+    assert_matches_oracle(w.logits, w.lengths, got, w.topk, w.next_n, label=f"{name} after the injected give-up")
