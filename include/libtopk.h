@@ -82,12 +82,11 @@ typedef struct {
    * out (TOPK_DEV_BARRIER_TIMEOUT) and all of them leave through the cluster's
    * exit barrier. Either way the workspace must then be re-initialised with
    * topk_workspace_init (see TOPK_DEV_WORKSPACE_DIRTY). 3 = the short-row
-   * kernel (shapes 4 and 5): CTA 0 (whole rows) or CTA 1 of cluster 0 (split
-   * rows) treats the first copy it waits for as late and gives up as on a
-   * time-out: TOPK_DEV_STAGE_TIMEOUT is set, its rows (with whole rows, those
-   * left to CTA 0; split, row 0) are left unwritten, every other row is
-   * selected, and every CTA of the cluster leaves through the same barriers.
-   * The workspace needs no re-initialisation after it. */
+   * kernel's row split over a cluster (shapes 4 and 5 with G > 1): CTA 1 of
+   * cluster 0 treats the first copy it waits for as late and gives up as on a
+   * time-out: TOPK_DEV_STAGE_TIMEOUT is set, row 0 is left unwritten, every
+   * other row is selected, and every CTA of the cluster leaves through the
+   * same barriers. The workspace needs no re-initialisation after it. */
   int inject_skip_arrival;
   /* 0 = unchecked; otherwise the workspace's size, checked against topk_workspace_size. */
   size_t workspace_bytes;

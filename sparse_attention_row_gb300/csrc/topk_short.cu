@@ -832,7 +832,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
       }
       target = min(target, n_seed);
       bool ok = !bulk || piece_ready(s, S, (par >> S) & 1u, p.timeout_ns);
-      if (p.inject == 3 && blockIdx.x == 0 && k == 0) ok = false;  // test: CTA 0 gives up on its first row
       const int seed_hi = min(kSeed, w.nwin);
       const float* seed = s.row + S * kPiece;  // a piece never wraps round the ring
       uint32_t kmax = 0;
