@@ -10,6 +10,8 @@ alphabet, all-equal rows (buffer overflow and re-stream), increasing rows
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 
@@ -17,7 +19,9 @@ from tests.gpu_util import Runner, assert_matches_oracle
 
 pytestmark = pytest.mark.gpu
 
-CASES = 80
+# TOPK_FUZZ_CASES=N runs N seeds of every generator below instead of their defaults
+FUZZ_CASES = int(os.environ.get("TOPK_FUZZ_CASES", "0"))
+CASES = FUZZ_CASES or 80
 MAX_ELEMENTS = 3_000_000  # keeps the oracle to well under a second per case
 
 
@@ -92,7 +96,7 @@ def test_random_case_matches_oracle(rn, seed):
     assert rn.workspace_clean()
 
 
-SHORT_CASES = 40
+SHORT_CASES = FUZZ_CASES or 40
 
 
 def _short_case(seed: int):
@@ -120,7 +124,7 @@ def test_random_short_rows_match_oracle(rn, seed):
                           label=f"short seed {seed}: {x.shape[0]} rows x {x.shape[1]}, K {topk}, {opts}")
 
 
-CLUSTER_CASES = 40
+CLUSTER_CASES = FUZZ_CASES or 40
 
 
 def _cluster_case(seed: int):
