@@ -326,6 +326,40 @@ class GpuBench:
         return {"ms_mean": float(np.mean(ms)), "ms_median": float(np.median(ms)),
                 "ms_min": float(np.min(ms)), "wall_s": wall, "launches": steps, "out": out}
 
+    def time_pairs(self, w, steps: int, warmup: int, mode: int) -> float:
+        """Mean device time of two calls back to back (L2 flushed before each
+        pair, both inside one event pair), with programmatic dependent launch
+        on (mode 1) or off (mode 2): on, the second call's CTAs may start on
+        SMs the first leaves idle and wait there for it to complete."""
+        t = self.torch
+        x, ln, out = self.upload(w)
+        opt = self.sar.TopkOptions()
+        opt.dependent_launch = mode
+        stream = t.cuda.current_stream()
+
+        def call():
+            rc = self.sar.topk_ragged_ex(x, w.row_stride, ln, w.num_rows, w.next_n, w.topk, out,
+                                         self.sel.workspace, self.stream_handle, opt)
+            if rc != 0:
+                raise RuntimeError(f"topk_ragged_ex: {self.sar.topk_status_string(rc)}")
+
+        for _ in range(warmup):
+            self.flush_l2()
+            call()
+            call()
+        starts = [t.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [t.cuda.Event(enable_timing=True) for _ in range(steps)]
+        t.cuda.synchronize()
+        t.cuda._sleep(20_000_000)
+        for i in range(steps):
+            self.flush_l2()
+            starts[i].record(stream)
+            call()
+            call()
+            ends[i].record(stream)
+        t.cuda.synchronize()
+        return float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
+
     def time_e2e(self, w, steps: int, warmup: int) -> dict:
         """Host buffers: pinned H2D of the batch, the call, D2H of the indices, every step."""
         t = self.torch
@@ -568,6 +602,11 @@ def run_ours(args) -> None:
 
     w, r, ms, gbs, vbytes, clocks = head
     e2e = gb.time_e2e(w, max(10, args.steps // 10), args.warmup)
+    # two calls back to back, as in a decode step that selects for two layers:
+    # programmatic dependent launch on (the default) against off
+    npair = max(10, min(300, args.steps // 10))
+    pair_on = gb.time_pairs(w, npair, args.warmup, 1)
+    pair_off = gb.time_pairs(w, npair, args.warmup, 2)
     e2e_ms = max_over_ranks(e2e["ms_per_step"], world, gb.dev)
     if rank != 0:
         if world > 1:
@@ -606,6 +645,9 @@ def run_ours(args) -> None:
                 "ms_per_step": e2e_ms,
                 "note": "host buffers: the whole padded logits batch (num_rows x row_stride fp32) and the lengths "
                         "copied in, the indices copied out, every step; the copy dominates"},
+        "dependent_launch": {"pair_us_on": pair_on * 1e3, "pair_us_off": pair_off * 1e3, "pairs": npair,
+                             "note": "two back-to-back calls on the headline batch inside one event pair, L2 "
+                                     "flushed before each pair; on = programmatic dependent launch (default)"},
         "gpu_launches": r["launches"],
         "clocks": clocks,
         "long_row": None if "prefill" not in table else {

@@ -66,7 +66,11 @@ typedef enum {
  * launch does the same until topk_workspace_init clears the workspace. */
 #define TOPK_DEV_WORKSPACE_DIRTY 0x8u
 
-/* Tuning and test knobs for topk_ragged_ex. Zero-initialise, then set fields. */
+/* Tuning and test knobs for topk_ragged_ex. Zero-initialise, then set fields.
+ * A field left at 0 takes the value of its environment variable, read once per
+ * process, where one exists: LIBTOPK_FORCE_CTAS_PER_GROUP,
+ * LIBTOPK_LONG_ROW_THRESHOLD, LIBTOPK_BARRIER_TIMEOUT_US, LIBTOPK_MERGE and
+ * LIBTOPK_DEPENDENT_LAUNCH (topk_ragged and topk_ragged_static read them too). */
 typedef struct {
   /* 0 = planner decides; 1 = one CTA per row; 2..16 = that many CTAs split each row
    * (with shape 4: 2..8, the CTAs of one thread-block cluster per row). */
@@ -107,6 +111,17 @@ typedef struct {
    * rows only: strided views keep whole rows); 5 = the same kernel with 16
    * warps per CTA (512 threads), faster on short rows and split rows. */
   int shape;
+  /* Programmatic dependent launch of the short-row kernel (shapes 4 and 5).
+   * 0 = default (on); 1 = on; 2 = off. On, the kernel is launched with
+   * programmatic stream serialisation: its CTAs may start while the kernel
+   * before it on `stream` finishes, and every thread waits for that kernel to
+   * complete (griddepcontrol.wait, its writes then visible) before its first
+   * access to global memory; each CTA then lets the next kernel on the stream
+   * start early in the same way (griddepcontrol.launch_dependents), which is
+   * safe only for a kernel that waits likewise before it reads the indices.
+   * Off, plain stream order. The other shapes always launch in plain order.
+   * Any other value: TOPK_ERR_INVALID_ARG. */
+  int dependent_launch;
 } topk_options;
 
 /* Properties of a device as the planner sees them. */

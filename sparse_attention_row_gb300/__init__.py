@@ -72,7 +72,8 @@ class TopkOptions(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t),
                 ("max_ctas", ctypes.c_int),
                 ("merge", ctypes.c_int),
-                ("shape", ctypes.c_int)]
+                ("shape", ctypes.c_int),
+                ("dependent_launch", ctypes.c_int)]
 
 
 class TopkDeviceProps(ctypes.Structure):

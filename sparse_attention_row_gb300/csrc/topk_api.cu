@@ -29,6 +29,7 @@ struct EnvKnobs {
   int force_ctas_per_group = 0;
   uint32_t timeout_us = 0;
   int merge = 0;
+  int dependent_launch = 0;
 };
 
 EnvKnobs read_env() {
@@ -37,6 +38,7 @@ EnvKnobs read_env() {
   if (const char* v = getenv("LIBTOPK_FORCE_CTAS_PER_GROUP")) e.force_ctas_per_group = atoi(v);
   if (const char* v = getenv("LIBTOPK_BARRIER_TIMEOUT_US")) e.timeout_us = static_cast<uint32_t>(atoll(v));
   if (const char* v = getenv("LIBTOPK_MERGE")) e.merge = atoi(v);
+  if (const char* v = getenv("LIBTOPK_DEPENDENT_LAUNCH")) e.dependent_launch = atoi(v);
   return e;
 }
 
@@ -163,6 +165,8 @@ int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t str
   if (opt.force_ctas_per_group == 0) opt.force_ctas_per_group = env.force_ctas_per_group;
   if (opt.barrier_timeout_us == 0) opt.barrier_timeout_us = env.timeout_us;
   if (opt.merge == 0) opt.merge = env.merge;
+  if (opt.dependent_launch == 0) opt.dependent_launch = env.dependent_launch;
+  if (opt.dependent_launch < 0 || opt.dependent_launch > 2) return TOPK_ERR_INVALID_ARG;
 
   topk_plan plan{};
   rc = topk_make_plan(&props, c.num_rows, c.max_len, c.next_n, c.topk, &opt, &plan);
@@ -198,6 +202,7 @@ int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t str
   p.timeout_ns = opt.barrier_timeout_us ? static_cast<uint64_t>(opt.barrier_timeout_us) * 1000ull : kDefaultTimeoutNs;
   p.inject = opt.inject_skip_arrival;
   p.cluster = plan.cluster;
+  p.dependent_launch = opt.dependent_launch != 2 ? 1 : 0;
   if (launch_shape(plan.shape, p, plan.grid, plan.cooperative != 0, stream) != cudaSuccess) {
     cudaGetLastError();
     return TOPK_ERR_CUDA;

@@ -74,6 +74,7 @@ struct Params {
   uint64_t timeout_ns;
   int inject;
   int cluster;       // 1: the G CTAs of a group are one cluster and merge through its shared memory
+  int dependent_launch;  // host side: 1 = launch with programmatic stream serialisation (short-row kernel)
 };
 
 // Host side of one compiled kernel shape (ltk::wide, ltk::pair, ltk::small, ltk::shortrow, ltk::short16).

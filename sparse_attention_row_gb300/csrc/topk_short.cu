@@ -183,6 +183,18 @@ __device__ __noinline__ bool wait_piece(unsigned long long* bar, uint32_t parity
   }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the kernel before it on the stream is still
+// running. Every thread waits here, before its first access to global memory,
+// until that kernel has completed and its writes are visible (at once when
+// there is none, or when the launch did not allow the early start). The signal
+// that follows lets the next kernel on the stream start early in the same way:
+// that kernel waits for this one's completion before it reads its output.
+__device__ __forceinline__ void wait_previous_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Block barrier that ORs a predicate: every thread gets the same answer.
 __device__ __forceinline__ bool sync_or(bool pred) { return __syncthreads_or(pred ? 1 : 0) != 0; }
 
@@ -740,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
   const bool bulk = p.col_stride == 1;
   int64_t r = blockIdx.x;
   if (r >= p.num_rows) return;
+  wait_previous_grid();
 
   // Set-up: warp 0's lanes initialise the slot barriers and, with contiguous
   // rows, lane 0 issues piece 0 of the first row's blind window (sized by
@@ -1490,6 +1503,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
   const int me = static_cast<int>(cluster_rank());
   const int64_t r = blockIdx.x / C;
   if (r >= p.num_rows) return;  // the whole cluster: its CTAs share the row
+  wait_previous_grid();
 
   // Set-up: this CTA's first kBlind pieces of the blind window (sized by
   // max_len) go out before the length is read, local piece 0 first and the
@@ -1902,20 +1916,27 @@ cudaError_t launch_topk(const Params& p, int grid, bool, cudaStream_t stream) {
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
   cfg.numAttrs = 0;
+  if (p.dependent_launch) {
+    // may start while the previous kernel on the stream finishes (the kernel
+    // waits for it before touching global memory)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    ++cfg.numAttrs;
+  }
   if (p.G <= 1) {
     cfg.dynamicSmemBytes = sizeof(Smem);
     return cudaLaunchKernelEx(&cfg, topk_short_kernel, p);
   }
   if (p.G > kMaxCluster || p.col_stride != 1 || grid % p.G != 0) return cudaErrorInvalidValue;
   cfg.dynamicSmemBytes = sizeof(SmemC);
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(p.G);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.numAttrs = 1;
+  attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+  attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(p.G);
+  attr[cfg.numAttrs].val.clusterDim.y = 1;
+  attr[cfg.numAttrs].val.clusterDim.z = 1;
+  ++cfg.numAttrs;
   return cudaLaunchKernelEx(&cfg, topk_short_cluster_kernel, p);
 }
 
