@@ -264,6 +264,10 @@ int topk_ragged_strided(const float* logits, int64_t row_stride, int64_t col_str
  * rule implies; the selection itself returns a set). Logits are addressed as
  * in topk_ragged_strided; an index outside [0, max_len) is treated as -1 and
  * never read. No workspace; the launch needs up to 32 KB of shared memory.
+ * It is launched with programmatic dependent launch (unless
+ * LIBTOPK_DEPENDENT_LAUNCH=2): its CTAs may start while the kernel before it
+ * on `stream` (the selection) finishes, and wait for it to complete before
+ * they read out_idx or the logits.
  * Returns the topk_status codes of topk_ragged (TOPK_OK when num_rows is 0, or
  * when sort is 0 and out_val is NULL: nothing to do).
  */

@@ -140,6 +140,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 namespace ltk {
 
+bool dependent_launch_default() { return env_knobs().dependent_launch != 2; }
+
 int run_selection(const Call& c, void* scratch, int max_groups, cudaStream_t stream, const topk_options* options) {
   if (c.num_rows < 0 || c.row_stride < 0 || c.col_stride < 1 || c.max_len < 1 || c.max_len > INT32_MAX ||
       c.next_n < 1 || (c.num_rows % c.next_n) != 0)

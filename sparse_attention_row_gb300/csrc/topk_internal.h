@@ -77,6 +77,9 @@ struct Params {
   int dependent_launch;  // host side: 1 = launch with programmatic stream serialisation (short-row kernel)
 };
 
+// Programmatic dependent launch unless LIBTOPK_DEPENDENT_LAUNCH=2 (read once).
+bool dependent_launch_default();
+
 // Host side of one compiled kernel shape (ltk::wide, ltk::pair, ltk::small, ltk::shortrow, ltk::short16).
 #define LTK_DECLARE_SHAPE(NS)                                                                  \
   namespace NS {                                                                               \

@@ -43,6 +43,11 @@ __global__ void __launch_bounds__(kThreads) topk_sort_kernel(const SortParams p)
   const int tid = threadIdx.x;
   const int K = p.topk;
   const int P = p.width;
+  // programmatic dependent launch: wait for the kernel before this one on the
+  // stream (typically the selection that wrote the indices) to complete, then
+  // let the next one start early in the same way
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int64_t r = blockIdx.x; r < p.num_rows; r += gridDim.x) {
     int32_t* row_idx = p.idx + r * K;
     float* row_val = p.val ? p.val + r * K : nullptr;
@@ -121,9 +126,19 @@ extern "C" int topk_gather_sort(const float* logits, int64_t row_stride, int64_t
   p.val = out_val;
   p.sort = sort ? 1 : 0;
   const int64_t grid = num_rows < 2ll * sms ? num_rows : 2ll * sms;
-  const size_t smem = static_cast<size_t>(width) * sizeof(unsigned long long);
-  ltk::sortk::topk_sort_kernel<<<static_cast<unsigned>(grid), ltk::sortk::kThreads, smem,
-                                 static_cast<cudaStream_t>(stream)>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return TOPK_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(ltk::sortk::kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(width) * sizeof(unsigned long long);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ltk::dependent_launch_default() ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, ltk::sortk::topk_sort_kernel, p) != cudaSuccess) {
+    cudaGetLastError();
+    return TOPK_ERR_CUDA;
+  }
   return TOPK_OK;
 }

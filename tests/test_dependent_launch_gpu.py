@@ -102,3 +102,34 @@ def test_dependent_launch_value_out_of_range_is_refused(run):
         assert rc == run.sar.TOPK_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert (out.cpu().numpy() == -7).all()
+
+
+@pytest.mark.parametrize("name,rows", [("decode_batch", 24), ("mtp", 8), ("prefill", 160)])
+def test_selection_then_sort_back_to_back(run, name, rows):
+    # selection, then values and order of its rows, for several batches in a
+    # row on one stream with no synchronisation: each sort reads the indices
+    # its selection wrote, after it has written them all
+    import oracle
+
+    torch = run.torch
+    sar = run.sar
+    w = workloads.make(name, rows)
+    R, S = w.logits.shape
+    batches = [w.logits, -w.logits, w.logits * np.float32(0.5) + np.float32(1.0)]
+    srcs = [torch.from_numpy(b).to(run.dev) for b in batches]
+    ln = torch.from_numpy(w.lengths).to(run.dev)
+    outs = [torch.full((R, w.topk), -7, dtype=torch.int32, device=run.dev) for _ in batches]
+    vals = [torch.zeros((R, w.topk), dtype=torch.float32, device=run.dev) for _ in batches]
+    torch.cuda.synchronize()
+    for x, out, val in zip(srcs, outs, vals):
+        _call(run, x, w, ln, out, run.options())
+        assert sar.topk_gather_sort(x, S, 1, S, R, w.topk, out, val, sort=True) == sar.TOPK_OK
+    torch.cuda.synchronize()
+    _status_ok(run)
+    for i, (b, out, val) in enumerate(zip(batches, outs, vals)):
+        want, _ = oracle.topk_ragged(b, w.lengths, w.topk, next_n=w.next_n)
+        got = out.cpu().numpy()
+        assert np.array_equal(got, want), f"{name} batch {i}: rows {np.nonzero((got != want).any(1))[0][:3]}"
+        v = val.cpu().numpy()
+        ok = got >= 0
+        assert np.array_equal(v[ok], b[np.nonzero(ok)[0], got[ok]]) and np.all(np.isneginf(v[~ok]))
