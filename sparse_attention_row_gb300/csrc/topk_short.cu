@@ -947,7 +947,16 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
           const int v0 = task * (tsz / 4);                    // and its first float4 in the window
           uint32_t m = 0;
           if (v0 + 32 * F <= nvec && 4 * v0 - w.mis >= 0 && 4 * v0 + tsz - w.mis <= len) {
-            // a task inside the row: no element needs a bounds check
+            // a task inside the row: no element needs a bounds check (the common
+            // F = 8 spelt out, so that its eight loads go out unconditionally)
+            if (F == 8) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
+                m |= ((f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                      (f.w >= thr ? 8u : 0u)) << (4 * i);
+              }
+            } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               if (i < F) {
@@ -955,6 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
                 m |= ((f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
                       (f.w >= thr ? 8u : 0u)) << (4 * i);
               }
+            }
             }
           } else {
 #pragma unroll
@@ -973,14 +983,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_kernel(const Params p)
             }
           }
           const int c = __popc(m);  // at most 32
-          uint32_t qb[6];
-#pragma unroll
-          for (int bit = 0; bit < 6; ++bit) qb[bit] = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+          // the warp's survivors and this lane's exclusive prefix, one ballot per bit of
+          // the lanes' counts: bits 0..2 always, bits 3..5 only when a lane has 8 or
+          // more (rare: the threshold keeps a few percent of the elements)
           int tot = 0, pre = 0;
 #pragma unroll
-          for (int bit = 0; bit < 6; ++bit) {
-            tot += __popc(qb[bit]) << bit;
-            pre += __popc(qb[bit] & lt) << bit;
+          for (int bit = 0; bit < 3; ++bit) {
+            const uint32_t qb = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+            tot += __popc(qb) << bit;
+            pre += __popc(qb & lt) << bit;
+          }
+          if (__any_sync(0xFFFFFFFFu, c >= 8)) {
+#pragma unroll
+            for (int bit = 3; bit < 6; ++bit) {
+              const uint32_t qb = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+              tot += __popc(qb) << bit;
+              pre += __popc(qb & lt) << bit;
+            }
           }
           if (tot > 0) {
             if (wc + tot <= kRegion) {
@@ -1686,6 +1705,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
         const int v0 = (j * kPiece + off) >> 2;  // its first float4 in the window
         uint32_t m = 0;
         if (v0 + 32 * F <= nvec && 4 * v0 - w.mis >= 0 && 4 * v0 + tsz - w.mis <= len) {
+          if (F == 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = *reinterpret_cast<const float4*>(&s.row[sb + 4 * (lane + 32 * i)]);
+              m |= ((f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
+                    (f.w >= thr ? 8u : 0u)) << (4 * i);
+            }
+          } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             if (i < F) {
@@ -1693,6 +1720,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
               m |= ((f.x >= thr ? 1u : 0u) | (f.y >= thr ? 2u : 0u) | (f.z >= thr ? 4u : 0u) |
                     (f.w >= thr ? 8u : 0u)) << (4 * i);
             }
+          }
           }
         } else {
 #pragma unroll
@@ -1711,14 +1739,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_short_cluster_kernel(const P
           }
         }
         const int c = __popc(m);
-        uint32_t qb[6];
-#pragma unroll
-        for (int bit = 0; bit < 6; ++bit) qb[bit] = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+        // the warp's survivors and this lane's exclusive prefix, one ballot per bit of
+        // the lanes' counts: bits 0..2 always, bits 3..5 only when a lane has 8 or
+        // more (rare: the threshold keeps a few percent of the elements)
         int tot = 0, pre = 0;
 #pragma unroll
-        for (int bit = 0; bit < 6; ++bit) {
-          tot += __popc(qb[bit]) << bit;
-          pre += __popc(qb[bit] & lt) << bit;
+        for (int bit = 0; bit < 3; ++bit) {
+          const uint32_t qb = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+          tot += __popc(qb) << bit;
+          pre += __popc(qb & lt) << bit;
+        }
+        if (__any_sync(0xFFFFFFFFu, c >= 8)) {
+#pragma unroll
+          for (int bit = 3; bit < 6; ++bit) {
+            const uint32_t qb = __ballot_sync(0xFFFFFFFFu, (c >> bit) & 1);
+            tot += __popc(qb) << bit;
+            pre += __popc(qb & lt) << bit;
+          }
         }
         if (tot > 0) {
           if (wc + tot <= kRegion) {
