@@ -71,3 +71,35 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(sar, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         sar.topk_status_string(0)
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    # the ctypes mirrors of topk_options, topk_device_props and topk_plan must
+    # have the header's field offsets and sizes: a C program compiled against
+    # include/libtopk.h prints them
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    mirrors = {"topk_options": sar.TopkOptions, "topk_device_props": sar.TopkDeviceProps,
+               "topk_plan": sar.TopkPlan}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "libtopk.h"', "int main(void) {"]
+    for cname, py in mirrors.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = {}
+    for line in subprocess.check_output([str(exe)], text=True).splitlines():
+        cname, field, value = line.split()
+        got[(cname, field)] = int(value)
+    for cname, py in mirrors.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert got[(cname, fname)] == getattr(py, fname).offset, (cname, fname)
